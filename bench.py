@@ -1,0 +1,432 @@
+"""Benchmark: fused in-place QK RMSNorm + RoPE on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one call of the fused op (qknr_apply, one kernel launch) over the
+whole workload with inputs resident in HBM. Between timed steps the call
+rotates over input replicas totalling at least 4x the L2 size, so no step
+finds its inputs in L2. Rank 0 prints one JSON line.
+
+Metric: effective HBM bandwidth = algorithmic bytes / time, where algorithmic
+bytes = read + write of every Q/K head, one fp32 cos|sin row and one position
+per token, and the two weight vectors; also heads/s and the fraction of the
+measured HBM copy bandwidth.
+
+--impl reference times the double-precision CPU oracle (the reference
+implementation here: there is no runnable upstream code) on the host cores,
+each step a bounded sample of tokens of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+from typing import Dict, List, Optional
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "fused QK-RMSNorm+RoPE effective HBM GB/s (% of GB300 peak) and heads/sec"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_NAME = "qknr_fused_kernel"
+
+
+# ------------------------------------------------------------------ environment
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def measured_peaks() -> Dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "qk_rmsnorm_rope_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str) -> Optional[float]:
+    """DRAM bytes per launch from the committed ncu summary for this workload,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.txt")
+    try:
+        with open(path) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    fields = {}
+    for ln in lines:
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def smi_id(device) -> str:
+    """nvidia-smi selector for a torch device (its UUID, so that a restricted
+    CUDA_VISIBLE_DEVICES still names the right board)."""
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device.index or 0)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str, period_ms: int = 50):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)  # let the first samples land before timing starts
+
+    def stop(self) -> Dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+class PreparedCall:
+    """One qknr_apply call's arguments, built once (pointers of one replica)."""
+
+    def __init__(self, q, dev: Dict[str, torch.Tensor], w: workloads.Workload, stream: int):
+        T, n_qo, D = dev["q"].shape
+        n_kv = dev["k"].shape[1]
+        hs = dev["q"].stride(1) if n_qo > 1 else dev["k"].stride(1)
+        self.fn = q.lib.qknr_apply
+        self.args = (dev["q"].data_ptr(), dev["k"].data_ptr(), dev["q_w"].data_ptr(),
+                     dev["k_w"].data_ptr(), dev["cos_sin_cache"].data_ptr(),
+                     dev["positions"].data_ptr(), T, n_qo, n_kv, D, w.rope_dim, int(w.is_neox),
+                     dev["q"].stride(0), dev["k"].stride(0), hs, w.eps,
+                     q.dtype_code(dev["q"].dtype, dev["positions"].dtype), stream)
+        self.q = q
+
+    def __call__(self):
+        rc = self.fn(*self.args)
+        if rc != 0:
+            raise self.q.QknrError(rc, self.q.qknr_last_error())
+
+
+def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> Optional[Dict]:
+    import qk_rmsnorm_rope_gb300 as q
+
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist = init_dist(world, backend)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    q.init(local)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+
+    cpu = workloads.make_inputs(w)
+    qk_bytes = 2 * (w.n_qo + w.n_kv) * w.num_tokens * w.head_dim
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    n_rep = max(1, math.ceil(4 * l2 / qk_bytes)) if qk_bytes < 4 * l2 else 1
+    reps = [workloads.to_device(cpu, w, device) for _ in range(n_rep)]
+    calls = [PreparedCall(q, r, w, sh) for r in reps]
+    algo = workloads.algorithmic_bytes(w)
+    heads = workloads.num_heads_total(w)
+
+    for i in range(args.warmup):
+        calls[i % n_rep]()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(smi_id(device))
+    sampler.start()
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        calls[i % n_rep]()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(dist, ms, device)
+
+    # end to end through the C ABI from pinned host buffers: H2D of q, k and
+    # positions, the call, D2H of q and k, every step
+    e2e = run_e2e(q, cpu, w, device, stream, args.e2e_steps, dist)
+
+    if rank != 0:
+        return None
+    secs = ms_max / 1e3
+    value = world * algo * args.steps / secs / 1e9
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = float(peak or FALLBACK_HBM_GBS)
+    per_launch_s = secs / args.steps
+    achieved = algo / per_launch_s / 1e9
+    traffic = profiled_traffic(w.name)
+    wm = q.work_map(w.num_tokens, w.n_qo, w.n_kv, w.head_dim, w.rope_dim, w.is_neox,
+                    q.dtype_code(w.torch_dtype, w.pos_torch_dtype))
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": workloads.describe(w),
+                   "storage_dtype": w.dtype, "bytes_per_step": algo, "heads_per_step": heads,
+                   "l2": (f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.0f} MB >= 4x L2)"
+                          if n_rep > 1 else "inputs larger than 4x L2"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "work_map": wm},
+        "heads_per_s": world * heads * args.steps / secs,
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": algo,
+                     "kernel": KERNEL_NAME},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, cpu, budget_s=args.cpu_seconds)
+    return line
+
+
+def run_e2e(q, cpu, w, device, stream, steps: int, dist) -> Dict:
+    dev = workloads.to_device(cpu, w, device)
+    call = PreparedCall(q, dev, w, stream.cuda_stream)
+    if w.fused_total_heads:
+        h_src = [cpu["buffer"].pin_memory()]
+        d_dst = [dev["buffer"]]
+    else:
+        h_src = [cpu["q"].pin_memory(), cpu["k"].pin_memory()]
+        d_dst = [dev["q"], dev["k"]]
+    h_pos = cpu["positions"].pin_memory()
+    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in d_dst]
+    h2d = sum(t.numel() * t.element_size() for t in h_src) + h_pos.numel() * h_pos.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def step():
+        for d, h in zip(d_dst, h_src):
+            d.copy_(h, non_blocking=True)
+        dev["positions"].copy_(h_pos, non_blocking=True)
+        call()
+        for h, d in zip(h_out, d_dst):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    secs = time.perf_counter() - t0   # host wall clock: what the caller waits for
+    world = dist.get_world_size() if dist is not None else 1
+    secs = max_over_ranks(dist, secs, device)
+    algo = workloads.algorithmic_bytes(w)
+    return {"value": round(world * algo * steps / secs / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "path": "pinned host -> qknr_apply (C ABI) -> pinned host, one stream"}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _sample_inputs(cpu, idx):
+    return {"q": cpu["q"][idx], "k": cpu["k"][idx], "q_w": cpu["q_w"], "k_w": cpu["k_w"],
+            "cos_sin_cache": cpu["cos_sin_cache"], "positions": cpu["positions"][idx]}
+
+
+def _sample_bytes(w, n_tok):
+    return workloads.algorithmic_bytes(workloads.scaled(w, n_tok, cache_len=w.cache_len))
+
+
+def cpu_baseline(w, cpu, budget_s: float = 10.0) -> Dict:
+    """The oracle as it stands (one thread, double precision) on a bounded
+    sample: consecutive token blocks of the workload until ~budget_s seconds."""
+    import oracle
+    T = w.num_tokens
+    block = min(T, 512)
+    done_tok, t_used = 0, 0.0
+    start = 0
+    while t_used < budget_s and done_tok < 64 * T:
+        idx = torch.arange(start, start + block) % T
+        sub = _sample_inputs(cpu, idx)
+        t0 = time.perf_counter()
+        oracle.apply(sub["q"], sub["k"], sub["q_w"], sub["k_w"], sub["cos_sin_cache"],
+                     sub["positions"], is_neox=w.is_neox, eps=w.eps)
+        t_used += time.perf_counter() - t0
+        done_tok += block
+        start = (start + block) % T
+    value = _sample_bytes(w, done_tok) / t_used / 1e9
+    return {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done_tok} tokens of {w.name} in blocks of {block} ({t_used:.1f} s, "
+                      f"double precision, single thread)",
+            "heads_per_s": done_tok * (w.n_qo + w.n_kv) / t_used}
+
+
+def run_reference(args, w: workloads.Workload, rank: int, world: int) -> Optional[Dict]:
+    """Reference arm: the CPU oracle, each step a bounded token sample."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.load()
+    cpu = workloads.make_inputs(w)
+    T = w.num_tokens
+    # size the per-step sample so K+W steps take about a minute
+    probe = min(T, 64)
+    t0 = time.perf_counter()
+    sub = _sample_inputs(cpu, torch.arange(probe))
+    oracle.apply(sub["q"], sub["k"], sub["q_w"], sub["k_w"], sub["cos_sin_cache"],
+                 sub["positions"], is_neox=w.is_neox, eps=w.eps)
+    per_tok = max((time.perf_counter() - t0) / probe, 1e-7)
+    target = 60.0 / max(1, args.steps + args.warmup)
+    n_tok = int(max(1, min(T, target / per_tok)))
+
+    def step(i):
+        s0 = (i * n_tok) % T
+        idx = torch.arange(s0, s0 + n_tok) % T
+        sb = _sample_inputs(cpu, idx)
+        oracle.apply(sb["q"], sb["k"], sb["q_w"], sb["k_w"], sb["cos_sin_cache"],
+                     sb["positions"], is_neox=w.is_neox, eps=w.eps)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    secs = time.perf_counter() - t0
+    sample_bytes = _sample_bytes(w, n_tok)
+    value = sample_bytes * args.steps / secs / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": workloads.describe(w),
+                   "storage_dtype": w.dtype, "sample_tokens_per_step": n_tok},
+        "heads_per_s": n_tok * (w.n_qo + w.n_kv) * args.steps / secs,
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n_tok} consecutive tokens of {w.name} per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv: Optional[List[str]] = None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="dit", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    if world != args.gpus and world > 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    w = workloads.get(args.workload)
+    if args.impl == "reference":
+        line = run_reference(args, w, rank, world)
+    else:
+        line = run_ours(args, w, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+/*
+ * qknr.h -- C ABI of libqknr: fused, in-place, per-head QK RMSNorm + rotary
+ * position embedding (RoPE) on NVIDIA GB300 (sm_103a).
+ *
+ * What one call computes (fused_inplace_qknorm_rope deep-dive, §2.1-§2.3):
+ * for every token t and every head h of q (weight q_w) and of k (weight k_w),
+ * with x = the head's head_dim values and p = positions[t]:
+ *
+ *     r   = 1 / sqrt( (1/head_dim) * sum_i x_i^2 + eps )          (§2.1, §4.3)
+ *     n_i = x_i * r * w_i                                          (§2.1)
+ *     c_j = cache[p][j], s_j = cache[p][rope_dim/2 + j]            (§2.2, §3)
+ *     interleaved (GPT-J), j < rope_dim/2:                          (§2.2)
+ *         o_{2j} = n_{2j} c_j - n_{2j+1} s_j,  o_{2j+1} = n_{2j+1} c_j + n_{2j} s_j
+ *     NeoX (LLaMA), d < rope_dim/2:                                 (§2.2, §4.4)
+ *         o_d = n_d c_d - n_{d+R/2} s_d,       o_{d+R/2} = n_{d+R/2} c_d + n_d s_d
+ *     o_i = n_i for rope_dim <= i < head_dim (partial RoPE)         (§2.2)
+ *
+ * and writes o back over x, rounded once to the tensor's dtype (round to
+ * nearest even). All arithmetic is fp32. The tensor contract follows §3 of
+ * the same page: q [T, n_qo, D] and k [T, n_kv, D] in fp16 or bf16 with unit
+ * innermost stride; q_w, k_w [D] in the same dtype; cos_sin_cache fp32
+ * [cache_len, rope_dim], cos in the first half of each row and sin in the
+ * second; positions [T] int32 or int64. The op returns nothing and allocates
+ * nothing per call.
+ *
+ * Thread / device model: every entry point acts on the calling thread's
+ * current CUDA device. qknr_init must have been called for that device.
+ * Calls are asynchronous on the given stream except where stated.
+ *
+ * Errors: every entry point returns a QKNR_* status. Nothing is thrown across
+ * the ABI. On a non-OK status, qknr_last_error() returns a message for the
+ * calling thread. A failed validation launches nothing and leaves q and k
+ * untouched.
+ */
+#ifndef QKNR_H
+#define QKNR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype argument: element type of q, k, q_w, k_w, OR-ed with the positions type */
+#define QKNR_BF16 0x000    /* bfloat16 q/k/weights */
+#define QKNR_FP16 0x001    /* IEEE half q/k/weights */
+#define QKNR_POS_I64 0x100 /* positions are int64 (otherwise int32) */
+
+/* status codes */
+#define QKNR_OK 0
+#define QKNR_ERR_NOT_INITIALIZED 1 /* qknr_init was not called for the current device */
+#define QKNR_ERR_INVALID_ARG 2     /* null pointer, negative size, overlapping q/k, bad dtype */
+#define QKNR_ERR_UNSUPPORTED 3     /* head_dim / rope_dim / pairing outside the accepted set */
+#define QKNR_ERR_MISALIGNED 4      /* pointer or stride breaks the 16-byte vector rule */
+#define QKNR_ERR_CUDA 5            /* a CUDA runtime call failed; message has the CUDA error */
+#define QKNR_ERR_POSITION_OOB 6    /* qknr_apply_checked: a position outside [0, cache_len) */
+
+/*
+ * Prepare the library for CUDA device `device`: reads the SM count and other
+ * limits, and allocates a 16-byte status word used by qknr_apply_checked.
+ * Idempotent; safe to call from several threads. Restores the caller's
+ * current device before returning. Returns QKNR_OK or QKNR_ERR_CUDA /
+ * QKNR_ERR_INVALID_ARG (no such device).
+ */
+int qknr_init(int device);
+
+/*
+ * Release what qknr_init allocated, on every device. Callers must make sure
+ * no launch from this library is still running. After it, qknr_init must be
+ * called again before any apply.
+ */
+int qknr_shutdown(void);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char *qknr_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int qknr_version(void);
+
+/*
+ * Shape gate, the counterpart of the deep-dive's can_use check (§5.2) for
+ * this library's own kernels. Returns 1 if (head_dim, rope_dim, is_neox,
+ * dtype) is in the accepted set, else 0. Accepted: head_dim in {64, 128, 256};
+ * rope_dim even with 0 < rope_dim <= head_dim; interleaved pairing takes
+ * every such rope_dim; NeoX pairing takes rope_dim % 16 == 0 or rope_dim in
+ * {2, 4, 6, 8}. This contains the page's set (head_dim/32 elements per lane,
+ * rotary lanes a power of two) and more.
+ */
+int qknr_can_use(int head_dim, int rope_dim, int is_neox, int dtype);
+
+/*
+ * The fused op, in place, asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream).
+ *
+ * q, k          device pointers to head (t=0, h=0) of q and k; modified in place.
+ * q_w, k_w      device pointers to the [head_dim] RMSNorm weights, q/k dtype.
+ * cos_sin_cache device pointer to fp32 [cache_len, rope_dim], row-major.
+ * positions     device pointer to [num_tokens] int32 or int64 (QKNR_POS_I64).
+ *               A position outside the cache is undefined behaviour here, as
+ *               on the page (§4.4); qknr_apply_checked checks them.
+ * num_tokens    T >= 0 (0: nothing is launched).
+ * n_qo, n_kv    query and key head counts, each >= 1 (GQA: n_qo != n_kv).
+ * head_dim      D; rope_dim R: see qknr_can_use.
+ * is_neox       0 = interleaved (GPT-J) pairing, 1 = NeoX pairing.
+ * q_stride      elements between consecutive tokens of q; k_stride the same for k.
+ * head_stride   elements between consecutive heads, shared by q and k (§3).
+ *               The innermost stride is 1. Heads must not overlap
+ *               (head_stride >= D) and token rows must not overlap.
+ * eps           added to the mean of squares inside the square root.
+ * dtype         QKNR_BF16 or QKNR_FP16, OR-ed with QKNR_POS_I64 for int64 positions.
+ *
+ * Alignment: q, k, q_w, k_w 16-byte aligned; q_stride, k_stride, head_stride
+ * multiples of 8 elements; cos_sin_cache 4-byte aligned; positions aligned to
+ * their size. q and k must not overlap (disjoint views of one fused QKV buffer
+ * are fine). The caller owns every buffer; nothing is retained after return.
+ */
+int qknr_apply(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
+               const void *positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim,
+               int rope_dim, int is_neox, int64_t q_stride, int64_t k_stride, int64_t head_stride,
+               float eps, int dtype, void *stream);
+
+/*
+ * qknr_apply plus a check of every position against [0, cache_len). Tokens
+ * whose position is outside are left untouched; all others are computed as by
+ * qknr_apply. SYNCHRONOUS: waits for `stream` before returning. Returns
+ * QKNR_ERR_POSITION_OOB (message: count and first bad token) if any position
+ * was out of range. Uses the status word that qknr_init allocated, so calls
+ * on one device must not overlap on the GPU (they serialise on the host).
+ */
+int qknr_apply_checked(void *q, void *k, const void *q_w, const void *k_w,
+                       const float *cos_sin_cache, int64_t cache_len, const void *positions,
+                       int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
+                       int is_neox, int64_t q_stride, int64_t k_stride, int64_t head_stride,
+                       float eps, int dtype, void *stream);
+
+/*
+ * Work-map override for tuning and tests (process-wide). passes_per_item
+ * (at most 4): warp passes, of 32/(head_dim/16) heads each, that one warp
+ * item covers; threads_per_cta in {64, 128, 256, 512}; ctas_per_sm caps
+ * resident CTAs per SM. 0 in any of these restores the automatic choice.
+ * use_pdl: 1 launch with programmatic dependent launch, 0 without, -1
+ * automatic (on). The environment variable QKNR_WORK_MAP="ppi,threads,ctas"
+ * sets the same fields at first use.
+ */
+int qknr_set_work_map(int passes_per_item, int threads_per_cta, int ctas_per_sm, int use_pdl);
+
+/*
+ * The launch qknr_apply would make for these sizes (no launch, no pointers).
+ * out[0] grid CTAs, out[1] threads per CTA, out[2] warp items, out[3] chunks
+ * per token, out[4] passes per token, out[5] max passes per item (kernel
+ * unroll class), out[6] resident CTAs per SM, out[7] PDL on (1/0).
+ */
+int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
+                        int is_neox, int dtype, int64_t out[8]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QKNR_H */

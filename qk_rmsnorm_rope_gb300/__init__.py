@@ -1,0 +1,244 @@
+"""Fused in-place per-head QK RMSNorm + RoPE on GB300 (sm_103a).
+
+Thin Python binding over ``libqknr.so`` (C ABI in ``include/qknr.h``). The
+``qknr_*`` functions mirror the C entry points one to one and take raw device
+pointers; ``apply`` / ``apply_checked`` marshal torch CUDA tensors into them
+the way the fused_inplace_qknorm_rope deep-dive's Python op does (§5.3:
+head_dim defaults to q.size(-1), rope_dim to cos_sin_cache.size(-1); the op
+returns None and mutates q and k). Every computation runs in the library's
+CUDA kernels; there is no other code path. Importing this package fails
+loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+__all__ = [
+    "QKNR_BF16", "QKNR_FP16", "QKNR_POS_I64", "QknrError", "library_path",
+    "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
+    "qknr_apply", "qknr_apply_checked", "qknr_set_work_map", "qknr_query_work_map",
+    "init", "apply", "apply_checked", "can_use", "dtype_code", "work_map",
+]
+
+QKNR_BF16 = 0x000
+QKNR_FP16 = 0x001
+QKNR_POS_I64 = 0x100
+
+STATUS_NAMES = {
+    0: "QKNR_OK", 1: "QKNR_ERR_NOT_INITIALIZED", 2: "QKNR_ERR_INVALID_ARG",
+    3: "QKNR_ERR_UNSUPPORTED", 4: "QKNR_ERR_MISALIGNED", 5: "QKNR_ERR_CUDA",
+    6: "QKNR_ERR_POSITION_OOB",
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libqknr.so")
+
+
+class QknrError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {message}")
+        self.code = code
+        self.message = message
+
+
+def _load() -> ctypes.CDLL:
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with `python -m qk_rmsnorm_rope_gb300.build` "
+            "(nvcc for sm_103a). There is no fallback implementation.")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.qknr_init.argtypes = [i32]
+    lib.qknr_shutdown.argtypes = []
+    lib.qknr_last_error.argtypes = []
+    lib.qknr_last_error.restype = ctypes.c_char_p
+    lib.qknr_version.argtypes = []
+    lib.qknr_can_use.argtypes = [i32, i32, i32, i32]
+    lib.qknr_apply.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
+                               i64, i64, i64, f32, i32, vp]
+    lib.qknr_apply_checked.argtypes = [vp, vp, vp, vp, vp, i64, vp, i64, i32, i32, i32, i32, i32,
+                                       i64, i64, i64, f32, i32, vp]
+    lib.qknr_set_work_map.argtypes = [i32, i32, i32, i32]
+    lib.qknr_query_work_map.argtypes = [i64, i32, i32, i32, i32, i32, i32,
+                                        ctypes.POINTER(ctypes.c_int64)]
+    for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
+                 "qknr_apply_checked", "qknr_set_work_map", "qknr_query_work_map"):
+        getattr(lib, name).restype = i32
+    return lib
+
+
+_lib = _load()
+lib = _lib  # the loaded C library, for callers that want the raw ctypes entry points
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise QknrError(rc, qknr_last_error())
+
+
+# --------------------------------------------------------------- raw C entry points
+def qknr_init(device: int) -> int:
+    return _lib.qknr_init(device)
+
+
+def qknr_shutdown() -> int:
+    return _lib.qknr_shutdown()
+
+
+def qknr_last_error() -> str:
+    return (_lib.qknr_last_error() or b"").decode(errors="replace")
+
+
+def qknr_version() -> int:
+    return _lib.qknr_version()
+
+
+def qknr_can_use(head_dim: int, rope_dim: int, is_neox: int, dtype: int) -> int:
+    return _lib.qknr_can_use(head_dim, rope_dim, int(is_neox), dtype)
+
+
+def qknr_apply(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_qo, n_kv, head_dim,
+               rope_dim, is_neox, q_stride, k_stride, head_stride, eps, dtype, stream) -> int:
+    return _lib.qknr_apply(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_qo, n_kv,
+                           head_dim, rope_dim, int(is_neox), q_stride, k_stride, head_stride,
+                           eps, dtype, stream)
+
+
+def qknr_apply_checked(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_tokens, n_qo,
+                       n_kv, head_dim, rope_dim, is_neox, q_stride, k_stride, head_stride, eps,
+                       dtype, stream) -> int:
+    return _lib.qknr_apply_checked(q, k, q_w, k_w, cos_sin_cache, cache_len, positions,
+                                   num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox),
+                                   q_stride, k_stride, head_stride, eps, dtype, stream)
+
+
+def qknr_set_work_map(passes_per_item: int = 0, threads_per_cta: int = 0, ctas_per_sm: int = 0,
+                      use_pdl: int = -1) -> int:
+    return _lib.qknr_set_work_map(passes_per_item, threads_per_cta, ctas_per_sm, use_pdl)
+
+
+def qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, dtype, out) -> int:
+    return _lib.qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox),
+                                    dtype, out)
+
+
+# --------------------------------------------------------------- torch marshalling
+def dtype_code(q_dtype, pos_dtype) -> int:
+    import torch
+    if q_dtype == torch.bfloat16:
+        code = QKNR_BF16
+    elif q_dtype == torch.float16:
+        code = QKNR_FP16
+    else:
+        raise QknrError(2, f"q/k dtype {q_dtype} is not bfloat16 or float16")
+    if pos_dtype == torch.int64:
+        code |= QKNR_POS_I64
+    elif pos_dtype != torch.int32:
+        raise QknrError(2, f"positions dtype {pos_dtype} is not int32 or int64")
+    return code
+
+
+def init(device: Optional[int] = None) -> None:
+    """qknr_init for ``device`` (default: torch's current CUDA device)."""
+    import torch
+    if device is None:
+        device = torch.cuda.current_device()
+    _check(qknr_init(int(device)))
+
+
+def can_use(head_dim: int, rope_dim: int, is_neox: bool, dtype=None) -> bool:
+    import torch
+    code = dtype_code(dtype or torch.bfloat16, torch.int32)
+    return bool(qknr_can_use(head_dim, rope_dim, int(is_neox), code))
+
+
+def _marshal(q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim):
+    import torch
+    if q.dim() != 3 or k.dim() != 3:
+        raise QknrError(2, "q and k must be [num_tokens, heads, head_dim] (reshape 4-D inputs)")
+    T, n_qo, D = q.shape
+    if k.shape[0] != T or k.shape[2] != D:
+        raise QknrError(2, f"k shape {tuple(k.shape)} does not match q {tuple(q.shape)}")
+    n_kv = k.shape[1]
+    head_dim = head_dim or D
+    rope_dim = rope_dim or cos_sin_cache.size(-1)
+    if head_dim != D:
+        raise QknrError(2, f"head_dim {head_dim} != q.size(-1) {D}")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.size(-1) != rope_dim:
+        raise QknrError(2, "cos_sin_cache must be [cache_len, rope_dim]")
+    if cos_sin_cache.dtype != torch.float32 or not cos_sin_cache.is_contiguous():
+        raise QknrError(2, "cos_sin_cache must be contiguous float32")
+    if positions.dim() != 1 or positions.shape[0] != T or not positions.is_contiguous():
+        raise QknrError(2, "positions must be a contiguous [num_tokens] tensor")
+    for name, t in (("q", q), ("k", k)):
+        if t.stride(2) != 1:
+            raise QknrError(4, f"{name} must have unit innermost stride")
+    if k.dtype != q.dtype or q_w.dtype != q.dtype or k_w.dtype != q.dtype:
+        raise QknrError(2, "q, k, q_w and k_w must share one dtype")
+    if q_w.shape != (D,) or k_w.shape != (D,) or not (q_w.is_contiguous() and k_w.is_contiguous()):
+        raise QknrError(2, "q_w and k_w must be contiguous [head_dim]")
+    devs = {t.device for t in (q, k, q_w, k_w, cos_sin_cache, positions)}
+    if len(devs) != 1 or next(iter(devs)).type != "cuda":
+        raise QknrError(2, "all tensors must be on one CUDA device")
+    if n_qo > 1 and n_kv > 1 and q.stride(1) != k.stride(1):
+        raise QknrError(2, "q and k must share one head stride")
+    head_stride = q.stride(1) if n_qo > 1 else (k.stride(1) if n_kv > 1 else D)
+    return (T, n_qo, n_kv, head_dim, rope_dim, q.stride(0), k.stride(0), head_stride,
+            dtype_code(q.dtype, positions.dtype))
+
+
+def apply(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float = 1e-6,
+          head_dim: int = 0, rope_dim: int = 0, stream=None) -> None:
+    """In-place fused QK RMSNorm + RoPE on torch CUDA tensors (returns None).
+
+    q [T, n_qo, D] and k [T, n_kv, D] (bf16/fp16, unit innermost stride, one
+    shared head stride) are overwritten. Runs on ``stream`` (a torch.cuda.Stream
+    or raw handle), default torch's current stream on q's device.
+    """
+    import torch
+    T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(q, k, q_w, k_w, cos_sin_cache, positions,
+                                                      is_neox, head_dim, rope_dim)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    with torch.cuda.device(q.device):
+        _check(qknr_apply(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
+                          cos_sin_cache.data_ptr(), positions.data_ptr(), T, n_qo, n_kv, D, R,
+                          int(bool(is_neox)), qs, ks, hs, float(eps), code, stream))
+
+
+def apply_checked(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float = 1e-6,
+                  head_dim: int = 0, rope_dim: int = 0, stream=None) -> None:
+    """``apply`` plus a device-side check that every position lies inside the
+    cache. Synchronous; raises QknrError (QKNR_ERR_POSITION_OOB) if one does
+    not, leaving those tokens untouched."""
+    import torch
+    T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(q, k, q_w, k_w, cos_sin_cache, positions,
+                                                      is_neox, head_dim, rope_dim)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    with torch.cuda.device(q.device):
+        _check(qknr_apply_checked(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
+                                  cos_sin_cache.data_ptr(), cos_sin_cache.shape[0],
+                                  positions.data_ptr(), T, n_qo, n_kv, D, R, int(bool(is_neox)),
+                                  qs, ks, hs, float(eps), code, stream))
+
+
+def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int,
+             is_neox: bool, dtype: int) -> Dict[str, int]:
+    """The launch qknr_apply would make (grid, threads, items, ...)."""
+    out = (ctypes.c_int64 * 8)()
+    _check(qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox), dtype,
+                               out))
+    keys = ["grid", "threads", "items", "chunks_per_token", "passes_per_token", "unroll",
+            "ctas_per_sm", "pdl"]
+    return dict(zip(keys, [int(v) for v in out]))

@@ -1,0 +1,19 @@
+// qknr_dispatch.h -- kernel table shared by the instantiation units and the C ABI.
+#pragma once
+
+namespace qknr {
+
+// Unroll classes: the kernel keeps up to UMAX warp passes of loads in flight.
+constexpr int kNumUnroll = 2;
+constexpr int kUnrollClass[kNumUnroll] = {2, 4};
+
+// head_dim classes
+constexpr int kNumHeadDim = 3;
+constexpr int kHeadDims[kNumHeadDim] = {64, 128, 256};
+
+// Kernel entry for (position type, head_dim class, mode, unroll class), or
+// nullptr. Defined in qknr_inst_bf16.cu / qknr_inst_fp16.cu.
+const void *kernel_bf16(int pos64, int d_idx, int mode, int u_idx);
+const void *kernel_fp16(int pos64, int d_idx, int mode, int u_idx);
+
+}  // namespace qknr

@@ -1,0 +1,339 @@
+// qknr_kernel.cuh -- fused in-place per-head QK RMSNorm + RoPE for sm_103a.
+//
+// The op (fused_inplace_qknorm_rope deep-dive §2.1-§2.3): per head, sum of
+// squares over head_dim in fp32, r = rsqrt(sum/D + eps), n = x*r*w, rotate the
+// first rope_dim dims with the token's cos|sin row (interleaved or NeoX
+// pairing), round once to the storage dtype and store over the input.
+//
+// Work map (this library's own design for GB300, not the page's warp-per-head):
+//  * A lane owns two 16-byte vectors (8 elements each) of one head, so a head
+//    takes D/16 lanes and a warp pass covers 32/(D/16) heads. Loads and stores
+//    are 128-bit, streaming (evict-first), and every warp instruction touches
+//    whole 32-byte sectors.
+//  * The two vectors are chosen so that no pairing needs a lane exchange:
+//    interleaved pairs (2j, 2j+1) sit inside one vector; for NeoX with
+//    rope_dim % 16 == 0 a lane owns dims [8a, 8a+8) and [8a+R/2, 8a+R/2+8),
+//    i.e. both halves of eight rotation pairs; lanes past the rotated span own
+//    two tail vectors from the two halves of the tail. The only shuffles are
+//    the log2(D/16)-step segmented sum of squares.
+//  * A warp item is (token, chunk of passes). Items are split across warps in
+//    balanced contiguous ranges, so a warp walks consecutive chunks of the same
+//    token and keeps that token's cos/sin values in registers across all its
+//    heads; the position and the cache row are read once per token per warp.
+//  * Each item issues all its loads (up to UMAX passes x 2 vectors per lane)
+//    before any arithmetic, to keep many bytes in flight per SM.
+//  * Grid: persistent, at most one wave of resident CTAs; programmatic
+//    dependent launch lets the next kernel in the stream get resident early.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace qknr {
+
+constexpr int kWarp = 32;
+
+enum Mode : int { kInterleaved = 0, kNeox = 1 };
+
+// Kernel parameters, passed by value as a __grid_constant__.
+struct Params {
+    char *q;                      // head (0,0) of q
+    char *k;                      // head (0,0) of k
+    const uint4 *q_w;             // [D] weights as 16-byte vectors
+    const uint4 *k_w;
+    const float *cache;           // [cache_len, R] fp32
+    const void *positions;        // [T] int32 / int64
+    unsigned long long *status;   // checked variant: {bad-token count, first bad token}
+    long long q_stride_b;         // bytes between tokens of q
+    long long k_stride_b;
+    long long head_stride_b;      // bytes between heads (q and k)
+    long long num_items;          // num_tokens * chunks_per_token
+    long long cache_len;          // > 0: check positions against it
+    int n_qo, n_kv;
+    int rope_dim;
+    int chunks_per_token;         // items per token
+    int passes_per_token;         // ceil((n_qo + n_kv) / heads_per_pass)
+    int cache_vec;                // 1: cos/sin rows may be read as float4
+    float eps;
+    float inv_d;                  // 1 / head_dim (exact: head_dim is a power of two)
+};
+
+template <class T>
+struct Cvt;
+
+template <>
+struct Cvt<__nv_bfloat16> {
+    // bf16 -> fp32 is exact: the 16 bits become the high half of a float.
+    static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
+    static __device__ __forceinline__ float hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // round to nearest even; a -> low half
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+template <>
+struct Cvt<__half> {
+    static __device__ __forceinline__ float lo(uint32_t u) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu)));
+    }
+    static __device__ __forceinline__ float hi(uint32_t u) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16)));
+    }
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+template <class T>
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    f[0] = Cvt<T>::lo(v.x); f[1] = Cvt<T>::hi(v.x);
+    f[2] = Cvt<T>::lo(v.y); f[3] = Cvt<T>::hi(v.y);
+    f[4] = Cvt<T>::lo(v.z); f[5] = Cvt<T>::hi(v.z);
+    f[6] = Cvt<T>::lo(v.w); f[7] = Cvt<T>::hi(v.w);
+}
+
+template <class T>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 v;
+    v.x = Cvt<T>::pack(f[0], f[1]);
+    v.y = Cvt<T>::pack(f[2], f[3]);
+    v.z = Cvt<T>::pack(f[4], f[5]);
+    v.w = Cvt<T>::pack(f[6], f[7]);
+    return v;
+}
+
+// NeoX with rope_dim <= 8: every rotated dim is in vector 0, pairs (e, e+HALF).
+template <int HALF>
+__device__ __forceinline__ void rotate_small_neox(float (&a)[8], const float (&c)[8],
+                                                  const float (&s)[8]) {
+#pragma unroll
+    for (int e = 0; e < HALF; ++e) {
+        const float x0 = a[e], x1 = a[e + HALF];
+        a[e] = x0 * c[e] - x1 * s[e];
+        a[e + HALF] = x1 * c[e] + x0 * s[e];
+    }
+}
+
+template <class P>
+__device__ __forceinline__ long long load_position(const void *positions, long long t) {
+    return static_cast<long long>(__ldg(reinterpret_cast<const P *>(positions) + t));
+}
+
+// T: storage type (bf16/half); P: position type (int / long long);
+// D: head_dim; MODE: pairing; UMAX: max warp passes per item (loads in flight).
+template <class T, class P, int D, int MODE, int UMAX>
+__global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__ Params p) {
+    constexpr int LPH = D / 16;         // lanes per head
+    constexpr int HPW = kWarp / LPH;    // heads per warp pass
+    static_assert(D % 16 == 0 && LPH >= 1 && LPH <= kWarp && (LPH & (LPH - 1)) == 0, "head_dim");
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 900)
+    // Programmatic dependent launch: do not touch memory before the previous
+    // grid in the stream has completed; then let the next grid get resident.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+#endif
+
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int g = lane / LPH;           // head slot within the pass
+    const int l = lane % LPH;           // lane within the head
+    const int R = p.rope_dim;
+    const int half = R >> 1;
+    const int H = p.n_qo + p.n_kv;
+
+    // The two 16-byte vectors (vector v = dims [8v, 8v+8)) this lane owns.
+    int va, vb;
+    bool split = false;                 // NeoX rope_dim % 16 == 0 layout
+    bool rot_lane;                      // this lane holds rotated dims
+    if (MODE == kNeox && (R & 15) == 0) {
+        split = true;
+        const int rl = R >> 4;          // lanes holding rotation pairs
+        if (l < rl) {
+            va = l;
+            vb = l + rl;
+            rot_lane = true;
+        } else {
+            va = (R >> 3) + (l - rl);
+            vb = va + ((D - R) >> 4);
+            rot_lane = false;
+        }
+    } else {
+        va = l;
+        vb = l + LPH;
+        rot_lane = (MODE == kNeox) ? (l == 0) : (8 * va < R);
+    }
+
+    const uint4 wqa = __ldg(p.q_w + va), wqb = __ldg(p.q_w + vb);
+    const uint4 wka = __ldg(p.k_w + va), wkb = __ldg(p.k_w + vb);
+
+    const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long warp_id = gtid / kWarp;
+    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) / kWarp;
+    const long long it_begin = warp_id * p.num_items / nwarps;
+    const long long it_end = (warp_id + 1) * p.num_items / nwarps;
+
+    // cos and (sign-free) sin per owned element. Interleaved: c[m]/s[m] serve
+    // pair m of vector a (m < 4) and pair m-4 of vector b (m >= 4). NeoX split:
+    // c[e]/s[e] serve element e of both vectors. NeoX small: element e < R/2 of
+    // vector 0. Identity (1, 0) wherever nothing rotates.
+    float c[8], s[8];
+    long long cur_t = -1;
+    bool tok_ok = true;
+
+    for (long long it = it_begin; it < it_end; ++it) {
+        const long long t = it / p.chunks_per_token;
+        const int ch = static_cast<int>(it - t * p.chunks_per_token);
+        if (t != cur_t) {
+            cur_t = t;
+            const long long pos = load_position<P>(p.positions, t);
+            if (p.cache_len > 0) {
+                tok_ok = pos >= 0 && pos < p.cache_len;
+                if (!tok_ok && ch == 0 && lane == 0) {
+                    atomicAdd(p.status, 1ull);
+                    atomicMin(p.status + 1, static_cast<unsigned long long>(t));
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { c[e] = 1.f; s[e] = 0.f; }
+            if (tok_ok && rot_lane) {
+                const float *row = p.cache + pos * R;
+                if (MODE == kInterleaved) {
+                    if (p.cache_vec && 8 * va + 8 <= R) {
+                        const float4 ca = __ldg(reinterpret_cast<const float4 *>(row + 4 * va));
+                        const float4 sa = __ldg(reinterpret_cast<const float4 *>(row + half + 4 * va));
+                        c[0] = ca.x; c[1] = ca.y; c[2] = ca.z; c[3] = ca.w;
+                        s[0] = sa.x; s[1] = sa.y; s[2] = sa.z; s[3] = sa.w;
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int j = 4 * va + m;
+                            if (2 * j < R) { c[m] = __ldg(row + j); s[m] = __ldg(row + half + j); }
+                        }
+                    }
+                    if (p.cache_vec && 8 * vb + 8 <= R) {
+                        const float4 cb = __ldg(reinterpret_cast<const float4 *>(row + 4 * vb));
+                        const float4 sb = __ldg(reinterpret_cast<const float4 *>(row + half + 4 * vb));
+                        c[4] = cb.x; c[5] = cb.y; c[6] = cb.z; c[7] = cb.w;
+                        s[4] = sb.x; s[5] = sb.y; s[6] = sb.z; s[7] = sb.w;
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int j = 4 * vb + m;
+                            if (2 * j < R) { c[4 + m] = __ldg(row + j); s[4 + m] = __ldg(row + half + j); }
+                        }
+                    }
+                } else if (split) {
+                    const int j0 = 8 * va;      // dims [j0, j0+8) of the first half
+                    if (p.cache_vec) {
+                        const float4 c0 = __ldg(reinterpret_cast<const float4 *>(row + j0));
+                        const float4 c1 = __ldg(reinterpret_cast<const float4 *>(row + j0 + 4));
+                        const float4 s0 = __ldg(reinterpret_cast<const float4 *>(row + half + j0));
+                        const float4 s1 = __ldg(reinterpret_cast<const float4 *>(row + half + j0 + 4));
+                        c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+                        c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+                        s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+                        s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) { c[e] = __ldg(row + j0 + e); s[e] = __ldg(row + half + j0 + e); }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (e < half) { c[e] = __ldg(row + e); s[e] = __ldg(row + half + e); }
+                    }
+                }
+            }
+        }
+        if (!tok_ok) continue;          // warp-uniform: t is the same for the whole warp
+
+        const int pb = static_cast<int>(static_cast<long long>(ch) * p.passes_per_token / p.chunks_per_token);
+        const int pe = static_cast<int>(static_cast<long long>(ch + 1) * p.passes_per_token / p.chunks_per_token);
+
+        uint4 xa[UMAX], xb[UMAX];
+        char *dst[UMAX];
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u) {
+            const int h = (pb + u) * HPW + g;
+            const bool ok = (pb + u < pe) && (h < H);
+            char *base = (h < p.n_qo)
+                ? p.q + t * p.q_stride_b + static_cast<long long>(h) * p.head_stride_b
+                : p.k + t * p.k_stride_b + static_cast<long long>(h - p.n_qo) * p.head_stride_b;
+            dst[u] = ok ? base : nullptr;
+            if (ok) {
+                xa[u] = __ldcs(reinterpret_cast<const uint4 *>(base) + va);
+                xb[u] = __ldcs(reinterpret_cast<const uint4 *>(base) + vb);
+            } else {
+                xa[u] = make_uint4(0u, 0u, 0u, 0u);
+                xb[u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u) {
+            if (pb + u >= pe) break;    // warp-uniform
+            const int h = (pb + u) * HPW + g;
+            const bool is_q = h < p.n_qo;
+            float a[8], b[8];
+            unpack8<T>(xa[u], a);
+            unpack8<T>(xb[u], b);
+
+            float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                ss0 = fmaf(a[e], a[e], ss0);
+                ss1 = fmaf(b[e], b[e], ss1);
+            }
+            float ss = ss0 + ss1;
+#pragma unroll
+            for (int off = LPH / 2; off > 0; off >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float r = rsqrtf(fmaf(ss, p.inv_d, p.eps));
+
+            float wa[8], wb[8];
+            unpack8<T>(is_q ? wqa : wka, wa);
+            unpack8<T>(is_q ? wqb : wkb, wb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                a[e] = a[e] * r * wa[e];
+                b[e] = b[e] * r * wb[e];
+            }
+
+            if (MODE == kInterleaved) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float a0 = a[2 * m], a1 = a[2 * m + 1];
+                    a[2 * m] = a0 * c[m] - a1 * s[m];
+                    a[2 * m + 1] = a1 * c[m] + a0 * s[m];
+                    const float b0 = b[2 * m], b1 = b[2 * m + 1];
+                    b[2 * m] = b0 * c[4 + m] - b1 * s[4 + m];
+                    b[2 * m + 1] = b1 * c[4 + m] + b0 * s[4 + m];
+                }
+            } else if (split) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float x0 = a[e], x1 = b[e];
+                    a[e] = x0 * c[e] - x1 * s[e];
+                    b[e] = x1 * c[e] + x0 * s[e];
+                }
+            } else if (rot_lane) {
+                switch (half) {
+                    case 1: rotate_small_neox<1>(a, c, s); break;
+                    case 2: rotate_small_neox<2>(a, c, s); break;
+                    case 3: rotate_small_neox<3>(a, c, s); break;
+                    default: rotate_small_neox<4>(a, c, s); break;
+                }
+            }
+
+            if (dst[u] != nullptr) {
+                __stcs(reinterpret_cast<uint4 *>(dst[u]) + va, pack8<T>(a));
+                __stcs(reinterpret_cast<uint4 *>(dst[u]) + vb, pack8<T>(b));
+            }
+        }
+    }
+}
+
+}  // namespace qknr

@@ -36,8 +36,8 @@ from typing import Dict, Optional
 import numpy as np
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "build_cos_sin_cache",
-           "scaled", "algorithmic_bytes", "num_heads_total"]
+__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "to_device", "build_cos_sin_cache",
+           "scaled", "algorithmic_bytes", "num_heads_total", "describe"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -165,16 +165,24 @@ def make_inputs(w: Workload, device: str = "cpu") -> Dict[str, torch.Tensor]:
     out["positions"] = torch.from_numpy(pos).to(w.pos_torch_dtype)
     out["cos_sin_cache"] = build_cos_sin_cache(w.cache_len, w.rope_dim, w.base)
     if device != "cpu":
-        if w.fused_total_heads:
-            buf = out["buffer"].to(device)
-            out["buffer"] = buf
-            out["q"] = buf[:, :w.n_qo, :]
-            out["k"] = buf[:, w.n_qo:w.n_qo + w.n_kv, :]
-        else:
-            out["q"] = out["q"].to(device)
-            out["k"] = out["k"].to(device)
-        for key in ("q_w", "k_w", "positions", "cos_sin_cache"):
-            out[key] = out[key].to(device)
+        out = to_device(out, w, device)
+    return out
+
+
+def to_device(inputs: Dict[str, torch.Tensor], w: Workload, device) -> Dict[str, torch.Tensor]:
+    """Copy an input set to ``device``, keeping q/k as views of the fused
+    buffer for the fused_qkv layout."""
+    out: Dict[str, torch.Tensor] = {}
+    if w.fused_total_heads:
+        buf = inputs["buffer"].to(device)
+        out["buffer"] = buf
+        out["q"] = buf[:, :w.n_qo, :]
+        out["k"] = buf[:, w.n_qo:w.n_qo + w.n_kv, :]
+    else:
+        out["q"] = inputs["q"].to(device)
+        out["k"] = inputs["k"].to(device)
+    for key in ("q_w", "k_w", "positions", "cos_sin_cache"):
+        out[key] = inputs[key].to(device)
     return out
 
 
