@@ -6,8 +6,9 @@ pointers; ``apply`` / ``apply_checked`` marshal torch CUDA tensors into them
 the way the fused_inplace_qknorm_rope deep-dive's Python op does (§5.3:
 head_dim defaults to q.size(-1), rope_dim to cos_sin_cache.size(-1); the op
 returns None and mutates q and k). Every computation runs in the library's
-CUDA kernels; there is no other code path. Importing this package fails
-loudly when the library has not been built.
+CUDA kernels; there is no other code path. The library is loaded at first
+use, and that use raises ImportError when it has not been built (so that the
+build step itself can import this package).
 """
 from __future__ import annotations
 
@@ -73,8 +74,21 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-_lib = _load()
-lib = _lib  # the loaded C library, for callers that want the raw ctypes entry points
+_lib: Optional[ctypes.CDLL] = None
+
+
+def _get_lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def __getattr__(name: str):
+    # ``qk_rmsnorm_rope_gb300.lib``: the loaded C library (raw ctypes entry points)
+    if name == "lib":
+        return _get_lib()
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
 
 
 def _check(rc: int) -> None:
@@ -84,48 +98,49 @@ def _check(rc: int) -> None:
 
 # --------------------------------------------------------------- raw C entry points
 def qknr_init(device: int) -> int:
-    return _lib.qknr_init(device)
+    return _get_lib().qknr_init(device)
 
 
 def qknr_shutdown() -> int:
-    return _lib.qknr_shutdown()
+    return _get_lib().qknr_shutdown()
 
 
 def qknr_last_error() -> str:
-    return (_lib.qknr_last_error() or b"").decode(errors="replace")
+    return (_get_lib().qknr_last_error() or b"").decode(errors="replace")
 
 
 def qknr_version() -> int:
-    return _lib.qknr_version()
+    return _get_lib().qknr_version()
 
 
 def qknr_can_use(head_dim: int, rope_dim: int, is_neox: int, dtype: int) -> int:
-    return _lib.qknr_can_use(head_dim, rope_dim, int(is_neox), dtype)
+    return _get_lib().qknr_can_use(head_dim, rope_dim, int(is_neox), dtype)
 
 
 def qknr_apply(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_qo, n_kv, head_dim,
                rope_dim, is_neox, q_stride, k_stride, head_stride, eps, dtype, stream) -> int:
-    return _lib.qknr_apply(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_qo, n_kv,
-                           head_dim, rope_dim, int(is_neox), q_stride, k_stride, head_stride,
-                           eps, dtype, stream)
+    return _get_lib().qknr_apply(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_qo,
+                                 n_kv, head_dim, rope_dim, int(is_neox), q_stride, k_stride,
+                                 head_stride, eps, dtype, stream)
 
 
 def qknr_apply_checked(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_tokens, n_qo,
                        n_kv, head_dim, rope_dim, is_neox, q_stride, k_stride, head_stride, eps,
                        dtype, stream) -> int:
-    return _lib.qknr_apply_checked(q, k, q_w, k_w, cos_sin_cache, cache_len, positions,
-                                   num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox),
-                                   q_stride, k_stride, head_stride, eps, dtype, stream)
+    return _get_lib().qknr_apply_checked(q, k, q_w, k_w, cos_sin_cache, cache_len, positions,
+                                         num_tokens, n_qo, n_kv, head_dim, rope_dim,
+                                         int(is_neox), q_stride, k_stride, head_stride, eps,
+                                         dtype, stream)
 
 
 def qknr_set_work_map(passes_per_item: int = 0, threads_per_cta: int = 0, ctas_per_sm: int = 0,
                       use_pdl: int = -1) -> int:
-    return _lib.qknr_set_work_map(passes_per_item, threads_per_cta, ctas_per_sm, use_pdl)
+    return _get_lib().qknr_set_work_map(passes_per_item, threads_per_cta, ctas_per_sm, use_pdl)
 
 
 def qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, dtype, out) -> int:
-    return _lib.qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox),
-                                    dtype, out)
+    return _get_lib().qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim,
+                                          int(is_neox), dtype, out)
 
 
 # --------------------------------------------------------------- torch marshalling
