@@ -1,0 +1,94 @@
+"""Host logic of bench.py on the CPU: the multi-rank timing reduction (gloo,
+world size 2), rank-0-only output, the reference arm's JSON line, and the
+roofline-traffic lookup that must ignore summaries taken on other sources."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, out_path):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    r, w, local = bench.dist_env()
+    assert (r, w, local) == (rank, world, rank)
+    dist = bench.init_dist(w, "gloo")
+    try:
+        bench.barrier(dist)
+        mx = bench.max_over_ranks(dist, 10.0 + rank, torch.device("cpu"))
+        with open(f"{out_path}.{rank}", "w") as f:
+            f.write(repr(mx))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2(tmp_path):
+    port = _free_port()
+    out = str(tmp_path / "mx")
+    mp.start_processes(_rank_main, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
+    for r in range(2):
+        with open(f"{out}.{r}") as f:
+            assert float(f.read()) == 11.0
+
+
+def _run_bench(args, env_extra=None):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+
+
+def test_reference_arm_line():
+    r = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "5", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["config"]["workload"] == "tiny"
+
+
+def test_reference_arm_other_ranks_are_silent():
+    r = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "5", "--warmup", "3",
+                    "--gpus", "2"], {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0, r.stderr
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_warmup_floor():
+    r = _run_bench(["--impl", "reference", "--steps", "5", "--warmup", "2"])
+    assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_profiled_traffic_requires_matching_sources(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "qk_rmsnorm_rope_gb300").symlink_to(os.path.join(ROOT, "qk_rmsnorm_rope_gb300"))
+    f = prof / f"{bench.KERNEL_NAME}_dit.txt"
+    f.write_text(f"source_sha256: {bench.kernel_source_hash()}\ntraffic_bytes_per_launch: 123\n")
+    assert bench.profiled_traffic("dit") == 123.0
+    f.write_text("source_sha256: 00\ntraffic_bytes_per_launch: 123\n")
+    assert bench.profiled_traffic("dit") is None
+    assert bench.profiled_traffic("gqa") is None
