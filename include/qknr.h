@@ -134,6 +134,32 @@ int qknr_apply_checked(void *q, void *k, const void *q_w, const void *k_w,
                        float eps, int dtype, void *stream);
 
 /*
+ * qknr_apply_checked without any allocation, for callers that cannot call
+ * cudaMalloc (a runtime that owns every device allocation or a pre-sized
+ * pool, a plug-in whose host reserves the allocator). The op itself has no
+ * counterpart of this entry point on the deep-dive page; it exists only for
+ * such callers.
+ *
+ * Same arguments, results and QKNR_ERR_POSITION_OOB report as
+ * qknr_apply_checked, but qknr_init is not needed and nothing is allocated:
+ * the 16-byte position status lives in a 256-byte file-scope __device__ array
+ * of the library, which every GPU that loads the library holds until the
+ * process exits. A call needs those 16 bytes whatever its num_tokens, so no
+ * problem size exceeds the array. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. Each call resets the status
+ * it reads, and waits for `stream` before returning. All calls share the one
+ * array: calls on one device are serialised on the host, and two launches
+ * that used the array at the same time on the GPU would race.
+ */
+int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_w,
+                               const float *cos_sin_cache, int64_t cache_len,
+                               const void *positions, int64_t num_tokens, int n_qo, int n_kv,
+                               int head_dim, int rope_dim, int is_neox, int64_t q_stride,
+                               int64_t k_stride, int64_t head_stride, float eps, int dtype,
+                               void *stream);
+
+/*
  * Work-map override for tuning and tests (process-wide). passes_per_item
  * (at most 4): warp passes, of 32/(head_dim/16) heads each, that one warp
  * item covers; threads_per_cta in {64, 128, 256, 512}; ctas_per_sm caps

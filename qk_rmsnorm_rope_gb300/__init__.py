@@ -19,7 +19,8 @@ from typing import Dict, Optional
 __all__ = [
     "QKNR_BF16", "QKNR_FP16", "QKNR_POS_I64", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
-    "qknr_apply", "qknr_apply_checked", "qknr_set_work_map", "qknr_query_work_map",
+    "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_set_work_map",
+    "qknr_query_work_map",
     "init", "apply", "apply_checked", "can_use", "dtype_code", "work_map",
 ]
 
@@ -65,11 +66,13 @@ def _load() -> ctypes.CDLL:
                                i64, i64, i64, f32, i32, vp]
     lib.qknr_apply_checked.argtypes = [vp, vp, vp, vp, vp, i64, vp, i64, i32, i32, i32, i32, i32,
                                        i64, i64, i64, f32, i32, vp]
+    lib.qknr_apply_checked_noalloc.argtypes = lib.qknr_apply_checked.argtypes
     lib.qknr_set_work_map.argtypes = [i32, i32, i32, i32]
     lib.qknr_query_work_map.argtypes = [i64, i32, i32, i32, i32, i32, i32,
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
-                 "qknr_apply_checked", "qknr_set_work_map", "qknr_query_work_map"):
+                 "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_set_work_map",
+                 "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -131,6 +134,16 @@ def qknr_apply_checked(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_
                                          num_tokens, n_qo, n_kv, head_dim, rope_dim,
                                          int(is_neox), q_stride, k_stride, head_stride, eps,
                                          dtype, stream)
+
+
+def qknr_apply_checked_noalloc(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_tokens,
+                               n_qo, n_kv, head_dim, rope_dim, is_neox, q_stride, k_stride,
+                               head_stride, eps, dtype, stream) -> int:
+    """The allocation-free checked call (no qknr_init needed); see include/qknr.h."""
+    return _get_lib().qknr_apply_checked_noalloc(q, k, q_w, k_w, cos_sin_cache, cache_len,
+                                                 positions, num_tokens, n_qo, n_kv, head_dim,
+                                                 rope_dim, int(is_neox), q_stride, k_stride,
+                                                 head_stride, eps, dtype, stream)
 
 
 def qknr_set_work_map(passes_per_item: int = 0, threads_per_cta: int = 0, ctas_per_sm: int = 0,

@@ -313,6 +313,120 @@ int apply_impl(void *q, void *k, const void *q_w, const void *k_w, const float *
     return QKNR_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free checked variant.
+//
+// Some callers cannot call cudaMalloc at all: code that runs where allocation
+// is forbidden or already accounted for (a pre-sized memory pool, an embedded
+// runtime that owns every device allocation, a plug-in loaded into a host
+// that reserves the allocator for itself). qknr_apply_checked needs a 16-byte
+// status word, which qknr_init allocates. This variant keeps that word in
+// the file-scope array below instead, so it needs neither qknr_init nor any
+// allocation. The array is part of the library image: every GPU that loads
+// the library holds its 256 bytes until the process exits.
+constexpr int kNoAllocStatusWords = 32;  // 256 bytes; one call uses the first 2 words
+static __device__ __align__(256) unsigned long long g_noalloc_status[kNoAllocStatusWords];
+
+struct NoAllocSlot {
+    std::once_flag once;
+    int setup_rc = QKNR_OK;
+    std::string setup_err;
+    DeviceState state;   // status = device address of g_noalloc_status; no host buffer
+    std::mutex call_mu;  // one call at a time per device (the array is shared)
+};
+NoAllocSlot g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: resolve the array's device
+// address (in host code its name is only a host-side stand-in) and read the
+// SM count. Nothing is allocated.
+void noalloc_setup(NoAllocSlot &slot, int dev) {
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_status);
+    if (e != cudaSuccess) {
+        slot.setup_rc = fail_cuda(e, "cudaGetSymbolAddress(static status)");
+        slot.setup_err = t_last_error;
+        return;
+    }
+    e = cudaDeviceGetAttribute(&slot.state.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        slot.setup_rc = fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+        slot.setup_err = t_last_error;
+        return;
+    }
+    slot.state.status = static_cast<unsigned long long *>(ptr);
+    slot.state.status_host = nullptr;
+    slot.state.ready.store(true, std::memory_order_release);
+}
+
+int apply_checked_noalloc_impl(void *q, void *k, const void *q_w, const void *k_w,
+                               const float *cache, long long cache_len, const void *positions,
+                               long long num_tokens, int n_qo, int n_kv, int head_dim,
+                               int rope_dim, int is_neox, long long q_stride, long long k_stride,
+                               long long head_stride, float eps, int dtype, void *stream) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(QKNR_ERR_INVALID_ARG, "device %d out of range", dev);
+    NoAllocSlot &slot = g_noalloc[dev];
+    std::call_once(slot.once, noalloc_setup, std::ref(slot), dev);
+    if (slot.setup_rc) return fail(slot.setup_rc, "%s", slot.setup_err.c_str());
+
+    int rc = validate(q, k, q_w, k_w, cache, positions, num_tokens, n_qo, n_kv, head_dim, rope_dim,
+                      is_neox, q_stride, k_stride, head_stride, eps, dtype);
+    if (rc) return rc;
+    if (cache_len < 0) return fail(QKNR_ERR_INVALID_ARG, "cache_len %lld < 0", cache_len);
+    if (num_tokens == 0) return QKNR_OK;
+    if (cache_len == 0) return fail(QKNR_ERR_POSITION_OOB, "cache_len is 0: every position is out of range");
+    // The status this call needs is 2 words whatever the problem size, so the
+    // fixed array always covers it; guard the invariant all the same.
+    static_assert(kNoAllocStatusWords >= 2, "static status array too small");
+
+    WorkMap wm;
+    rc = plan(slot.state, num_tokens, n_qo, n_kv, head_dim, is_neox, dtype, &wm);
+    if (rc) return rc;
+
+    Params prm = {};
+    prm.q = static_cast<char *>(q);
+    prm.k = static_cast<char *>(k);
+    prm.q_w = static_cast<const uint4 *>(q_w);
+    prm.k_w = static_cast<const uint4 *>(k_w);
+    prm.cache = cache;
+    prm.positions = positions;
+    prm.status = slot.state.status;
+    prm.q_stride_b = q_stride * 2;
+    prm.k_stride_b = k_stride * 2;
+    prm.head_stride_b = head_stride * 2;
+    prm.num_items = wm.items;
+    prm.cache_len = cache_len;
+    prm.n_qo = n_qo;
+    prm.n_kv = n_kv;
+    prm.rope_dim = rope_dim;
+    prm.chunks_per_token = wm.chunks_per_token;
+    prm.passes_per_token = wm.passes_per_token;
+    prm.cache_vec = (rope_dim % 8 == 0) && aligned(cache, 16);
+    prm.eps = eps;
+    prm.inv_d = 1.0f / static_cast<float>(head_dim);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(slot.call_mu);
+    // The array keeps the previous call's contents: reset count and first-bad index.
+    e = cudaMemsetAsync(slot.state.status, 0, sizeof(unsigned long long), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(slot.state.status + 1, 0xff, sizeof(unsigned long long), s);
+    if (e != cudaSuccess) return fail_cuda(e, "static status reset");
+    rc = launch(slot.state, wm, prm, s);
+    if (rc) return rc;
+    unsigned long long host_status[2] = {0ull, 0ull};
+    e = cudaMemcpyAsync(host_status, slot.state.status, sizeof host_status, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "static status read-back");
+    if (host_status[0]) {
+        return fail(QKNR_ERR_POSITION_OOB,
+                    "%llu token(s) have positions outside [0, %lld); first bad token index %llu (left untouched)",
+                    host_status[0], cache_len, host_status[1]);
+    }
+    return QKNR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -442,6 +556,16 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     out[6] = wm.ctas_per_sm;
     out[7] = wm.pdl;
     return QKNR_OK;
+}
+
+int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_w,
+                               const float *cos_sin_cache, int64_t cache_len, const void *positions,
+                               int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
+                               int is_neox, int64_t q_stride, int64_t k_stride, int64_t head_stride,
+                               float eps, int dtype, void *stream) {
+    return apply_checked_noalloc_impl(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_tokens,
+                                      n_qo, n_kv, head_dim, rope_dim, is_neox ? 1 : 0, q_stride,
+                                      k_stride, head_stride, eps, dtype, stream);
 }
 
 }  // extern "C"
