@@ -39,7 +39,7 @@ import workloads  # noqa: E402
 METRIC = "fused QK-RMSNorm+RoPE effective HBM GB/s (% of GB300 peak) and heads/sec"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_NAME = "qknr_fused_kernel"
+KERNEL_NAMES = {"bulk": "qknr_bulk_kernel", "register": "qknr_fused_kernel"}
 
 
 # ------------------------------------------------------------------ environment
@@ -91,10 +91,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(workload: str) -> Optional[float]:
-    """DRAM bytes per launch from the committed ncu summary for this workload,
-    if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.txt")
+def profiled_traffic(kernel: str, workload: str) -> Optional[float]:
+    """DRAM bytes per launch from the committed ncu summary for this kernel and
+    workload, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     try:
         with open(path) as f:
             lines = f.read().splitlines()
@@ -180,11 +180,12 @@ class ClockSampler:
 class PreparedCall:
     """One qknr_apply call's arguments, built once (pointers of one replica)."""
 
-    def __init__(self, q, dev: Dict[str, torch.Tensor], w: workloads.Workload, stream: int):
+    def __init__(self, q, dev: Dict[str, torch.Tensor], w: workloads.Workload, stream: int,
+                 entry: str = "qknr_apply"):
         T, n_qo, D = dev["q"].shape
         n_kv = dev["k"].shape[1]
         hs = dev["q"].stride(1) if n_qo > 1 else dev["k"].stride(1)
-        self.fn = q.lib.qknr_apply
+        self.fn = getattr(q.lib, entry)
         self.args = (dev["q"].data_ptr(), dev["k"].data_ptr(), dev["q_w"].data_ptr(),
                      dev["k_w"].data_ptr(), dev["cos_sin_cache"].data_ptr(),
                      dev["positions"].data_ptr(), T, n_qo, n_kv, D, w.rope_dim, int(w.is_neox),
@@ -214,7 +215,9 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     n_rep = max(1, math.ceil(4 * l2 / qk_bytes)) if qk_bytes < 4 * l2 else 1
     reps = [workloads.to_device(cpu, w, device) for _ in range(n_rep)]
-    calls = [PreparedCall(q, r, w, sh) for r in reps]
+    entry = "qknr_apply_unfused" if args.variant == "unfused" else "qknr_apply"
+    launches_per_step = 2 if args.variant == "unfused" else 1
+    calls = [PreparedCall(q, r, w, sh, entry) for r in reps]
     algo = workloads.algorithmic_bytes(w)
     heads = workloads.num_heads_total(w)
 
@@ -240,7 +243,7 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
 
     # end to end through the C ABI from pinned host buffers: H2D of q, k and
     # positions, the call, D2H of q and k, every step
-    e2e = run_e2e(q, cpu, w, device, stream, args.e2e_steps, dist)
+    e2e = run_e2e(q, cpu, w, device, stream, args.e2e_steps, dist, entry)
 
     if rank != 0:
         return None
@@ -252,9 +255,13 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     peak = float(peak or FALLBACK_HBM_GBS)
     per_launch_s = secs / args.steps
     achieved = algo / per_launch_s / 1e9
-    traffic = profiled_traffic(w.name)
     wm = q.work_map(w.num_tokens, w.n_qo, w.n_kv, w.head_dim, w.rope_dim, w.is_neox,
                     q.dtype_code(w.torch_dtype, w.pos_torch_dtype))
+    kernel = KERNEL_NAMES.get(wm["kernel"], str(wm["kernel"]))
+    if args.variant == "unfused":
+        kernel = "qknr_fused_kernel<..., kOpNorm> + qknr_fused_kernel<..., kOpRope>"
+        wm = {"kernel": "register (norm step, rope step)"}
+    traffic = profiled_traffic(kernel, w.name) if args.variant == "fused" else None
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
@@ -271,19 +278,22 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": algo,
-                     "kernel": KERNEL_NAME},
+                     "kernel": kernel},
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
     }
+    if args.variant == "unfused":
+        line["variant"] = ("unfused baseline: RMSNorm kernel then RoPE kernel, in place "
+                           "(value counts the fused op's algorithmic bytes)")
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, cpu, budget_s=args.cpu_seconds)
     return line
 
 
-def run_e2e(q, cpu, w, device, stream, steps: int, dist) -> Dict:
+def run_e2e(q, cpu, w, device, stream, steps: int, dist, entry: str = "qknr_apply") -> Dict:
     dev = workloads.to_device(cpu, w, device)
-    call = PreparedCall(q, dev, w, stream.cuda_stream)
+    call = PreparedCall(q, dev, w, stream.cuda_stream, entry)
     if w.fused_total_heads:
         h_src = [cpu["buffer"].pin_memory()]
         d_dst = [dev["buffer"]]
@@ -412,6 +422,8 @@ def main(argv: Optional[List[str]] = None) -> int:
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
+                    help="unfused: time the two-kernel RMSNorm-then-RoPE chain instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -54,10 +54,12 @@ extern "C" {
 #define QKNR_ERR_MISALIGNED 4      /* pointer or stride breaks the 16-byte vector rule */
 #define QKNR_ERR_CUDA 5            /* a CUDA runtime call failed; message has the CUDA error */
 #define QKNR_ERR_POSITION_OOB 6    /* qknr_apply_checked: a position outside [0, cache_len) */
+#define QKNR_ERR_WATCHDOG 7        /* a bounded wait inside a kernel ran out; that call's output is incomplete */
 
 /*
  * Prepare the library for CUDA device `device`: reads the SM count and other
- * limits, and allocates a 16-byte status word used by qknr_apply_checked.
+ * limits, and allocates a 24-byte status block (position-check counters and
+ * the kernels' watchdog flag) used by qknr_apply_checked and qknr_sync.
  * Idempotent; safe to call from several threads. Restores the caller's
  * current device before returning. Returns QKNR_OK or QKNR_ERR_CUDA /
  * QKNR_ERR_INVALID_ARG (no such device).
@@ -134,6 +136,23 @@ int qknr_apply_checked(void *q, void *k, const void *q_w, const void *k_w,
                        float eps, int dtype, void *stream);
 
 /*
+ * The unfused two-kernel chain that the fused op replaces, for measuring the
+ * fusion benefit on this GPU (deep-dive §2.4 table, and the §6 fallback of
+ * RMSNorm then RoPE): an RMSNorm kernel writes the normalised, weighted q and
+ * k back in place, rounded to their dtype; a RoPE kernel then reads them
+ * again, rotates the first rope_dim dims and writes them. Two launches, two
+ * reads and two writes of Q and K instead of one of each. Same arguments and
+ * errors as qknr_apply; asynchronous on `stream`. The intermediate rounding
+ * makes results differ from qknr_apply by up to one unit in the last place
+ * of each rotated pair's length.
+ */
+int qknr_apply_unfused(void *q, void *k, const void *q_w, const void *k_w,
+                       const float *cos_sin_cache, const void *positions, int64_t num_tokens,
+                       int n_qo, int n_kv, int head_dim, int rope_dim, int is_neox,
+                       int64_t q_stride, int64_t k_stride, int64_t head_stride, float eps,
+                       int dtype, void *stream);
+
+/*
  * qknr_apply_checked without any allocation, for callers that cannot call
  * cudaMalloc (a runtime that owns every device allocation or a pre-sized
  * pool, a plug-in whose host reserves the allocator). The op itself has no
@@ -142,9 +161,9 @@ int qknr_apply_checked(void *q, void *k, const void *q_w, const void *k_w,
  *
  * Same arguments, results and QKNR_ERR_POSITION_OOB report as
  * qknr_apply_checked, but qknr_init is not needed and nothing is allocated:
- * the 16-byte position status lives in a 256-byte file-scope __device__ array
+ * the 24-byte status block lives in a 256-byte file-scope __device__ array
  * of the library, which every GPU that loads the library holds until the
- * process exits. A call needs those 16 bytes whatever its num_tokens, so no
+ * process exits. A call needs those 24 bytes whatever its num_tokens, so no
  * problem size exceeds the array. The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture. Each call resets the status
@@ -160,24 +179,53 @@ int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_
                                void *stream);
 
 /*
- * Work-map override for tuning and tests (process-wide). passes_per_item
- * (at most 4): warp passes, of 32/(head_dim/16) heads each, that one warp
- * item covers; threads_per_cta in {64, 128, 256, 512}; ctas_per_sm caps
- * resident CTAs per SM. 0 in any of these restores the automatic choice.
- * use_pdl: 1 launch with programmatic dependent launch, 0 without, -1
- * automatic (on). The environment variable QKNR_WORK_MAP="ppi,threads,ctas"
- * sets the same fields at first use.
+ * Reports whether any earlier call on the current device had a kernel wait
+ * run out (the bulk kernel bounds every wait at about one second; it never
+ * runs out in normal operation). Waits for `stream`, then returns QKNR_OK or
+ * QKNR_ERR_WATCHDOG and clears the flag. qknr_apply is asynchronous, so this
+ * is how a caller checks it; the checked entry points report it themselves.
  */
-int qknr_set_work_map(int passes_per_item, int threads_per_cta, int ctas_per_sm, int use_pdl);
+int qknr_sync(void *stream);
+
+/* kernels (QKNR_TUNE_KERNEL values and qknr_query_work_map out[0]) */
+#define QKNR_KERNEL_AUTO 0
+#define QKNR_KERNEL_REGISTER 1 /* loads straight into registers; every accepted shape */
+#define QKNR_KERNEL_BULK 2     /* cp.async.bulk ring in shared memory; rope_dim % 8 == 0, 16-byte aligned table */
+
+/* tuning keys for qknr_set_tuning / qknr_get_tuning */
+#define QKNR_TUNE_RESET 0       /* qknr_set_tuning(QKNR_TUNE_RESET, 0): every key back to automatic */
+#define QKNR_TUNE_KERNEL 1      /* 0 auto (the register kernel), 1 register, 2 bulk */
+#define QKNR_TUNE_PASSES 2      /* register kernel: warp passes per item, 1..4 (0 auto = 4) */
+#define QKNR_TUNE_THREADS 3     /* register kernel: threads per CTA, 64/128/256/512 (0 auto = 256) */
+#define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy; bulk: 1) */
+#define QKNR_TUNE_PDL 5         /* programmatic dependent launch: -1 auto (on), 0 off, 1 on */
+#define QKNR_TUNE_CONSUMERS 6   /* bulk kernel: consumer warps per CTA, 1..16 (0 auto = 8) */
+#define QKNR_TUNE_STAGES 7      /* bulk kernel: ring depth, 1..32 (0 auto: what fits); rounded down to a
+                                   multiple of the consumer count */
+#define QKNR_TUNE_TILE_BYTES 8  /* bulk kernel: max bytes of heads per tile (0 auto = 24576) */
 
 /*
- * The launch qknr_apply would make for these sizes (no launch, no pointers).
- * out[0] grid CTAs, out[1] threads per CTA, out[2] warp items, out[3] chunks
- * per token, out[4] passes per token, out[5] max passes per item (kernel
- * unroll class), out[6] resident CTAs per SM, out[7] PDL on (1/0).
+ * Process-wide launch tuning, for benchmarks and tests; results do not depend
+ * on it (every setting gives the same bits). Invalid values return
+ * QKNR_ERR_INVALID_ARG and change nothing. The environment variable
+ * QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=1,pdl=1,consumers=8,stages=16,tile=24576"
+ * sets the same keys at first use.
+ */
+int qknr_set_tuning(int key, int value);
+int qknr_get_tuning(int key, int *value);
+
+#define QKNR_WORK_MAP_FIELDS 12
+/*
+ * The launch qknr_apply would make for these sizes (no launch, no pointers;
+ * assumes a 16-byte aligned cos|sin table). out[QKNR_WORK_MAP_FIELDS]:
+ *  0 kernel (QKNR_KERNEL_REGISTER / QKNR_KERNEL_BULK)  1 grid CTAs  2 threads per CTA
+ *  3 work items (warp items / tiles)  4 items per token  5 resident CTAs per SM
+ *  6 PDL on  7 passes per token (register) / heads per tile (bulk)
+ *  8 unroll class (register) / ring stages (bulk)  9 consumer warps (bulk)
+ * 10 dynamic shared memory bytes  11 bytes per ring stage
  */
 int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
-                        int is_neox, int dtype, int64_t out[8]);
+                        int is_neox, int dtype, int64_t *out);
 
 #ifdef __cplusplus
 }

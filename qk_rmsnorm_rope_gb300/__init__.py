@@ -19,9 +19,11 @@ from typing import Dict, Optional
 __all__ = [
     "QKNR_BF16", "QKNR_FP16", "QKNR_POS_I64", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
-    "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_set_work_map",
-    "qknr_query_work_map",
-    "init", "apply", "apply_checked", "can_use", "dtype_code", "work_map",
+    "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
+    "qknr_sync",
+    "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map", "TUNE_KEYS",
+    "init", "apply", "apply_checked", "apply_unfused", "can_use", "dtype_code", "work_map", "set_tuning",
+    "get_tuning", "sync",
 ]
 
 QKNR_BF16 = 0x000
@@ -31,8 +33,15 @@ QKNR_POS_I64 = 0x100
 STATUS_NAMES = {
     0: "QKNR_OK", 1: "QKNR_ERR_NOT_INITIALIZED", 2: "QKNR_ERR_INVALID_ARG",
     3: "QKNR_ERR_UNSUPPORTED", 4: "QKNR_ERR_MISALIGNED", 5: "QKNR_ERR_CUDA",
-    6: "QKNR_ERR_POSITION_OOB",
+    6: "QKNR_ERR_POSITION_OOB", 7: "QKNR_ERR_WATCHDOG",
 }
+
+QKNR_KERNEL_AUTO, QKNR_KERNEL_REGISTER, QKNR_KERNEL_BULK = 0, 1, 2
+# QKNR_TUNE_* keys (include/qknr.h)
+TUNE_KEYS = {"reset": 0, "kernel": 1, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5,
+             "consumers": 6, "stages": 7, "tile_bytes": 8}
+WORK_MAP_FIELDS = ["kernel", "grid", "threads", "items", "items_per_token", "ctas_per_sm", "pdl",
+                   "passes_or_heads", "unroll_or_stages", "consumers", "smem_bytes", "stage_bytes"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -67,12 +76,16 @@ def _load() -> ctypes.CDLL:
     lib.qknr_apply_checked.argtypes = [vp, vp, vp, vp, vp, i64, vp, i64, i32, i32, i32, i32, i32,
                                        i64, i64, i64, f32, i32, vp]
     lib.qknr_apply_checked_noalloc.argtypes = lib.qknr_apply_checked.argtypes
-    lib.qknr_set_work_map.argtypes = [i32, i32, i32, i32]
+    lib.qknr_apply_unfused.argtypes = lib.qknr_apply.argtypes
+    lib.qknr_sync.argtypes = [vp]
+    lib.qknr_set_tuning.argtypes = [i32, i32]
+    lib.qknr_get_tuning.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
     lib.qknr_query_work_map.argtypes = [i64, i32, i32, i32, i32, i32, i32,
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
-                 "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_set_work_map",
-                 "qknr_query_work_map"):
+                 "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
+                 "qknr_sync",
+                 "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -146,9 +159,24 @@ def qknr_apply_checked_noalloc(q, k, q_w, k_w, cos_sin_cache, cache_len, positio
                                                  head_stride, eps, dtype, stream)
 
 
-def qknr_set_work_map(passes_per_item: int = 0, threads_per_cta: int = 0, ctas_per_sm: int = 0,
-                      use_pdl: int = -1) -> int:
-    return _get_lib().qknr_set_work_map(passes_per_item, threads_per_cta, ctas_per_sm, use_pdl)
+def qknr_apply_unfused(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_qo, n_kv,
+                       head_dim, rope_dim, is_neox, q_stride, k_stride, head_stride, eps, dtype,
+                       stream) -> int:
+    return _get_lib().qknr_apply_unfused(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens,
+                                         n_qo, n_kv, head_dim, rope_dim, int(is_neox), q_stride,
+                                         k_stride, head_stride, eps, dtype, stream)
+
+
+def qknr_sync(stream) -> int:
+    return _get_lib().qknr_sync(stream)
+
+
+def qknr_set_tuning(key: int, value: int) -> int:
+    return _get_lib().qknr_set_tuning(key, value)
+
+
+def qknr_get_tuning(key: int, value) -> int:
+    return _get_lib().qknr_get_tuning(key, value)
 
 
 def qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, dtype, out) -> int:
@@ -261,12 +289,55 @@ def apply_checked(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, ep
                                   qs, ks, hs, float(eps), code, stream))
 
 
+def apply_unfused(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float = 1e-6,
+                  head_dim: int = 0, rope_dim: int = 0, stream=None) -> None:
+    """The unfused two-kernel baseline (RMSNorm kernel, then RoPE kernel), in
+    place; for measuring what fusion saves. See qknr_apply_unfused."""
+    import torch
+    T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(q, k, q_w, k_w, cos_sin_cache, positions,
+                                                      is_neox, head_dim, rope_dim)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    with torch.cuda.device(q.device):
+        _check(qknr_apply_unfused(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
+                                  cos_sin_cache.data_ptr(), positions.data_ptr(), T, n_qo, n_kv, D,
+                                  R, int(bool(is_neox)), qs, ks, hs, float(eps), code, stream))
+
+
+def set_tuning(**kw) -> None:
+    """Set launch tuning keys by name (see TUNE_KEYS); ``reset=True`` first
+    returns every key to automatic."""
+    if kw.pop("reset", False):
+        _check(qknr_set_tuning(0, 0))
+    for name, value in kw.items():
+        _check(qknr_set_tuning(TUNE_KEYS[name], int(value)))
+
+
+def get_tuning(name: str) -> int:
+    v = ctypes.c_int(0)
+    _check(qknr_get_tuning(TUNE_KEYS[name], ctypes.byref(v)))
+    return v.value
+
+
+def sync(stream=None) -> None:
+    """qknr_sync on ``stream`` (default: torch's current stream); raises
+    QknrError(QKNR_ERR_WATCHDOG) if a kernel wait ran out since the last check."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    _check(qknr_sync(stream))
+
+
 def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int,
              is_neox: bool, dtype: int) -> Dict[str, int]:
-    """The launch qknr_apply would make (grid, threads, items, ...)."""
-    out = (ctypes.c_int64 * 8)()
+    """The launch qknr_apply would make (kernel, grid, threads, items, ...)."""
+    out = (ctypes.c_int64 * len(WORK_MAP_FIELDS))()
     _check(qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox), dtype,
                                out))
-    keys = ["grid", "threads", "items", "chunks_per_token", "passes_per_token", "unroll",
-            "ctas_per_sm", "pdl"]
-    return dict(zip(keys, [int(v) for v in out]))
+    d = dict(zip(WORK_MAP_FIELDS, [int(v) for v in out]))
+    d["kernel"] = {1: "register", 2: "bulk"}.get(d["kernel"], d["kernel"])
+    return d

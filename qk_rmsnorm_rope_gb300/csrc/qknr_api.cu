@@ -4,7 +4,17 @@
 // deep-dive §3 and the host checks of §4.7 (shape/stride/dtype checks before
 // launch, int32 or int64 positions, grid sized from occupancy x SM count, the
 // CUDA launch error checked), restated for this library's kernels.
+//
+// Two kernels compute the op (identical arithmetic and lane mapping):
+//   register kernel  qknr_fused_kernel  (qknr_kernel.cuh): loads straight into
+//                    registers; any accepted shape and alignment.
+//   bulk kernel      qknr_bulk_kernel   (qknr_bulk_kernel.cuh): cp.async.bulk
+//                    copies into a shared-memory ring; needs rope_dim % 8 == 0
+//                    and a 16-byte aligned cos|sin table.
+// The automatic choice is the register kernel (measured faster on GB300 so far);
+// the bulk kernel runs when QKNR_TUNE_KERNEL asks for it.
 #include "../../include/qknr.h"
+#include "qknr_bulk_kernel.cuh"
 #include "qknr_dispatch.h"
 #include "qknr_kernel.cuh"
 
@@ -17,15 +27,21 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <string>
 
 namespace {
 
+using qknr::BulkParams;
 using qknr::Params;
 
 constexpr int kMaxDevices = 64;
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;             // 1.1.0
+constexpr int kStatusWords = 3;             // {bad-token count, first bad token, watchdog bits}
+constexpr int kMaxBulkSmem = 232448;        // dynamic shared memory per CTA on sm_100/sm_103 (227 KB)
+constexpr int kDefaultTileBytes = 24576;    // bulk kernel: max bytes of heads per tile
+constexpr int kMaxStages = 32;
 
 thread_local std::string t_last_error;
 
@@ -43,35 +59,100 @@ int fail_cuda(cudaError_t e, const char *what) {
     return fail(QKNR_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
+// ------------------------------------------------------------------ tuning
+constexpr int kNumTuneKeys = 9;   // keys 1..8 (QKNR_TUNE_*); slot 0 unused
+// the value that means "automatic" for each key
+constexpr int kTuneAuto[kNumTuneKeys] = {0, 0, 0, 0, 0, -1, 0, 0, 0};
+std::atomic<int> g_tune[kNumTuneKeys] = {{0}, {0}, {0}, {0}, {0}, {-1}, {0}, {0}, {0}};
+std::once_flag g_env_once;
+
+int tune_check(int key, int value) {
+    switch (key) {
+        case QKNR_TUNE_KERNEL:
+            return (value >= 0 && value <= 2)
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "kernel must be 0 (auto), 1 (register) or 2 (bulk)");
+        case QKNR_TUNE_PASSES:
+            return (value >= 0 && value <= qknr::kUnrollClass[qknr::kNumUnroll - 1])
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "passes per item must be in [0, %d]",
+                              qknr::kUnrollClass[qknr::kNumUnroll - 1]);
+        case QKNR_TUNE_THREADS:
+            return (value == 0 || value == 64 || value == 128 || value == 256 || value == 512)
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "threads per CTA must be 0 or one of 64/128/256/512");
+        case QKNR_TUNE_CTAS_PER_SM:
+            return (value >= 0 && value <= 32) ? QKNR_OK
+                                               : fail(QKNR_ERR_INVALID_ARG, "CTAs per SM must be in [0, 32]");
+        case QKNR_TUNE_PDL:
+            return (value >= -1 && value <= 1) ? QKNR_OK
+                                                : fail(QKNR_ERR_INVALID_ARG, "use_pdl must be -1, 0 or 1");
+        case QKNR_TUNE_CONSUMERS:
+            return (value >= 0 && value <= 16) ? QKNR_OK
+                                               : fail(QKNR_ERR_INVALID_ARG, "consumer warps must be in [0, 16]");
+        case QKNR_TUNE_STAGES:
+            return (value >= 0 && value <= kMaxStages)
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "stages must be in [0, %d]", kMaxStages);
+        case QKNR_TUNE_TILE_BYTES:
+            return (value == 0 || (value >= 512 && value <= 196608))
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "tile bytes must be 0 or in [512, 196608]");
+        default:
+            return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
+    }
+}
+
+// QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=1,pdl=1,consumers=8,stages=16,tile=24576"
+void read_env_tuning() {
+    const char *s = std::getenv("QKNR_TUNE");
+    if (!s) return;
+    static const struct {
+        const char *name;
+        int key;
+    } names[] = {{"kernel", QKNR_TUNE_KERNEL},   {"passes", QKNR_TUNE_PASSES},
+                 {"threads", QKNR_TUNE_THREADS}, {"ctas", QKNR_TUNE_CTAS_PER_SM},
+                 {"pdl", QKNR_TUNE_PDL},         {"consumers", QKNR_TUNE_CONSUMERS},
+                 {"stages", QKNR_TUNE_STAGES},   {"tile", QKNR_TUNE_TILE_BYTES}};
+    std::string spec(s);
+    size_t pos = 0;
+    while (pos < spec.size()) {
+        size_t end = spec.find(',', pos);
+        if (end == std::string::npos) end = spec.size();
+        const std::string item = spec.substr(pos, end - pos);
+        const size_t eq = item.find('=');
+        if (eq != std::string::npos) {
+            const std::string k = item.substr(0, eq);
+            const int v = std::atoi(item.c_str() + eq + 1);
+            for (const auto &n : names)
+                if (k == n.name && tune_check(n.key, v) == QKNR_OK) g_tune[n.key] = v;
+        }
+        pos = end + 1;
+    }
+}
+
+int tune(int key) {
+    std::call_once(g_env_once, read_env_tuning);
+    return g_tune[key].load(std::memory_order_relaxed);
+}
+
+// ------------------------------------------------------------------ devices
 struct DeviceState {
     std::atomic<bool> ready{false};
     int sm_count = 0;
-    unsigned long long *status = nullptr;       // device: {bad-token count, first bad token}
-    unsigned long long *status_host = nullptr;  // pinned host copy
-    std::mutex checked_mu;                      // serialises qknr_apply_checked on this device
-    // resident CTAs per SM, by (dtype, pos64, d_idx, mode, u_idx, threads class); 0 = unknown
+    unsigned long long *status = nullptr;       // device: kStatusWords words
+    unsigned long long *status_host = nullptr;  // pinned host copy (qknr_init) or nullptr
+    std::mutex checked_mu;                      // serialises status read-backs on this device
+    // resident CTAs per SM for the register kernel, by (dtype, pos64, d_idx, mode, u_idx, threads class)
     std::atomic<int> occupancy[2][2][qknr::kNumHeadDim][2][qknr::kNumUnroll][4];
+    // bulk kernels whose dynamic shared-memory limit was raised, by (dtype, pos64, d_idx, mode)
+    std::atomic<bool> bulk_attr[2][2][qknr::kNumHeadDim][2];
+    // resident CTAs per SM of the unfused-baseline kernels, by (dtype, op-1, pos64, d_idx, mode)
+    std::atomic<int> unfused_occ[2][2][2][qknr::kNumHeadDim][2];
 };
 
 DeviceState g_dev[kMaxDevices];
 std::mutex g_init_mu;
-
-// process-wide work-map overrides (0 / -1 = automatic)
-std::atomic<int> g_force_ppi{0}, g_force_threads{0}, g_force_ctas_per_sm{0}, g_force_pdl{-1};
-std::once_flag g_env_once;
-
-void read_env_overrides() {
-    // QKNR_WORK_MAP="passes_per_item,threads_per_cta,ctas_per_sm"
-    if (const char *s = std::getenv("QKNR_WORK_MAP")) {
-        int a = 0, b = 0, c = 0;
-        if (std::sscanf(s, "%d,%d,%d", &a, &b, &c) >= 1) {
-            g_force_ppi = std::max(a, 0);
-            g_force_threads = std::max(b, 0);
-            g_force_ctas_per_sm = std::max(c, 0);
-        }
-    }
-    if (const char *s = std::getenv("QKNR_PDL")) g_force_pdl = std::atoi(s) ? 1 : 0;
-}
 
 int head_dim_index(int d) {
     for (int i = 0; i < qknr::kNumHeadDim; ++i)
@@ -99,10 +180,28 @@ bool shape_ok(int head_dim, int rope_dim, int is_neox) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// ------------------------------------------------------------------ one call
+struct Call {
+    void *q = nullptr, *k = nullptr;
+    const void *q_w = nullptr, *k_w = nullptr;
+    const float *cache = nullptr;
+    const void *positions = nullptr;
+    long long cache_len = 0;  // > 0: checked
+    long long num_tokens = 0;
+    int n_qo = 0, n_kv = 0, head_dim = 0, rope_dim = 0, is_neox = 0;
+    long long q_stride = 0, k_stride = 0, head_stride = 0;  // elements
+    float eps = 0.f;
+    int dtype = 0;
+};
+
 struct WorkMap {
-    int grid = 0, threads = 0, chunks_per_token = 0, passes_per_token = 0, max_passes = 0;
-    int u_idx = 0, ctas_per_sm = 0, pdl = 1;
-    long long items = 0;
+    int kind = QKNR_KERNEL_REGISTER;
+    int grid = 0, threads = 0, ctas_per_sm = 0, pdl = 1;
+    long long items = 0;  // warp items (register kernel) or tiles (bulk kernel)
+    int chunks_per_token = 0;
+    int passes_per_token = 0, max_passes = 0, u_idx = 0;  // register kernel
+    int heads_per_chunk = 0, stages = 0, consumers = 0;   // bulk kernel
+    int stage_bytes = 0, smem_bytes = 0;
     const void *kernel = nullptr;
 };
 
@@ -120,56 +219,158 @@ int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u
     return QKNR_OK;
 }
 
-// Choose the launch for one call. Items are (token, chunk of warp passes);
-// the default aims at 4 passes per item (8 x 16-byte loads in flight per lane).
-int plan(DeviceState &st, long long num_tokens, int n_qo, int n_kv, int head_dim, int is_neox,
-         int dtype, WorkMap *wm) {
-    std::call_once(g_env_once, read_env_overrides);
-    const int d_idx = head_dim_index(head_dim);
-    const int lph = head_dim / 16;
+// Register kernel: items are (token, chunk of warp passes); the default is the
+// largest unroll class (8 x 16-byte loads in flight per lane).
+int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
+    const int d_idx = head_dim_index(c.head_dim);
+    const int lph = c.head_dim / 16;
     const int hpw = qknr::kWarp / lph;
-    const int heads = n_qo + n_kv;
+    const int heads = c.n_qo + c.n_kv;
+    wm->kind = QKNR_KERNEL_REGISTER;
     wm->passes_per_token = (heads + hpw - 1) / hpw;
-
-    int ppi = g_force_ppi.load();
-    if (ppi <= 0) ppi = 4;
-    ppi = std::min(ppi, qknr::kUnrollClass[qknr::kNumUnroll - 1]);
+    int ppi = tune(QKNR_TUNE_PASSES);
+    if (ppi <= 0) ppi = qknr::kUnrollClass[qknr::kNumUnroll - 1];
     wm->chunks_per_token = (wm->passes_per_token + ppi - 1) / ppi;
     wm->max_passes = (wm->passes_per_token + wm->chunks_per_token - 1) / wm->chunks_per_token;
     wm->u_idx = wm->max_passes <= 2 ? 0 : 1;
-    wm->items = num_tokens * wm->chunks_per_token;
-
-    int threads = g_force_threads.load();
+    wm->items = c.num_tokens * wm->chunks_per_token;
+    int threads = tune(QKNR_TUNE_THREADS);
     if (threads_index(threads) < 0) threads = 256;
     wm->threads = threads;
 
-    const int dt = (dtype & 0xff) == QKNR_FP16 ? 1 : 0;
-    const int pos64 = (dtype & QKNR_POS_I64) ? 1 : 0;
-    const int mode = is_neox ? qknr::kNeox : qknr::kInterleaved;
+    const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
+    const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
+    const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
     wm->kernel = dt ? qknr::kernel_fp16(pos64, d_idx, mode, wm->u_idx)
                     : qknr::kernel_bf16(pos64, d_idx, mode, wm->u_idx);
     if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no kernel for this shape");
-
     int occ = 0;
     int rc = resident_ctas(st, dt, pos64, d_idx, mode, wm->u_idx, threads, wm->kernel, &occ);
     if (rc) return rc;
-    const int force_cps = g_force_ctas_per_sm.load();
-    if (force_cps > 0) occ = std::min(occ, force_cps);
+    const int force = tune(QKNR_TUNE_CTAS_PER_SM);
+    if (force > 0) occ = std::min(occ, force);
     wm->ctas_per_sm = occ;
     const long long warps_per_cta = threads / qknr::kWarp;
     const long long needed = (wm->items + warps_per_cta - 1) / warps_per_cta;
-    const long long cap = static_cast<long long>(occ) * st.sm_count;
-    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, cap)));
-    const int pdl = g_force_pdl.load();
+    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(occ) * st.sm_count)));
+    return QKNR_OK;
+}
+
+bool bulk_applies(const Call &c) { return (c.rope_dim % 8) == 0 && aligned(c.cache, 16); }
+
+// Bulk kernel: tiles are (token, chunk of heads) of at most `tile` bytes of
+// heads; one producer warp and `consumers` consumer warps per CTA; the ring
+// depth is the largest multiple of the consumer count that fits the shared
+// memory of the CTAs resident per SM (default one CTA per SM).
+int plan_bulk(DeviceState &st, const Call &c, WorkMap *wm) {
+    const int d_idx = head_dim_index(c.head_dim);
+    const int heads = c.n_qo + c.n_kv;
+    const int head_b = 2 * c.head_dim;
+    const int row_b = 4 * c.rope_dim;
+    wm->kind = QKNR_KERNEL_BULK;
+    int tile = tune(QKNR_TUNE_TILE_BYTES);
+    if (tile <= 0) tile = kDefaultTileBytes;
+    const int max_heads = std::max(1, tile / head_b);
+    wm->chunks_per_token = (heads + max_heads - 1) / max_heads;
+    wm->heads_per_chunk = (heads + wm->chunks_per_token - 1) / wm->chunks_per_token;
+    wm->stage_bytes = (wm->heads_per_chunk * head_b + row_b + 127) / 128 * 128;
+    wm->items = c.num_tokens * wm->chunks_per_token;
+
+    int ctas = tune(QKNR_TUNE_CTAS_PER_SM);
+    if (ctas <= 0) ctas = 1;
+    const int smem_cap = std::min(kMaxBulkSmem, (228 * 1024) / ctas - 1024);
+    const int fit = (smem_cap - qknr::bulk_stage_offset(kMaxStages)) / wm->stage_bytes;
+    if (fit < 1) return fail(QKNR_ERR_UNSUPPORTED, "a %d-byte tile does not fit shared memory", wm->stage_bytes);
+    int consumers = tune(QKNR_TUNE_CONSUMERS);
+    if (consumers <= 0) consumers = 8;
+    int stages = tune(QKNR_TUNE_STAGES);
+    if (stages <= 0) stages = kMaxStages;
+    stages = std::min(stages, fit);
+    if (consumers > stages) consumers = stages;
+    stages = stages / consumers * consumers;  // each stage belongs to one consumer warp
+    wm->stages = stages;
+    wm->consumers = consumers;
+    wm->threads = qknr::kWarp * (1 + consumers);
+    wm->smem_bytes = qknr::bulk_stage_offset(stages) + stages * wm->stage_bytes;
+
+    const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
+    const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
+    const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
+    wm->kernel = dt ? qknr::bulk_kernel_fp16(pos64, d_idx, mode) : qknr::bulk_kernel_bf16(pos64, d_idx, mode);
+    if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no bulk kernel for this shape");
+    std::atomic<bool> &attr = st.bulk_attr[dt][pos64][d_idx][mode];
+    if (!attr.load(std::memory_order_acquire)) {
+        cudaError_t e =
+            cudaFuncSetAttribute(wm->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxBulkSmem);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        attr.store(true, std::memory_order_release);
+    }
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wm->kernel, wm->threads, wm->smem_bytes);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(bulk)");
+    if (occ <= 0)
+        return fail(QKNR_ERR_CUDA, "bulk kernel cannot be resident (%d bytes of shared memory)", wm->smem_bytes);
+    wm->ctas_per_sm = std::min(occ, ctas);
+    wm->grid = static_cast<int>(
+        std::max(1LL, std::min(wm->items, static_cast<long long>(wm->ctas_per_sm) * st.sm_count)));
+    return QKNR_OK;
+}
+
+int plan(DeviceState &st, const Call &c, WorkMap *wm) {
+    const int kind = tune(QKNR_TUNE_KERNEL);
+    int rc;
+    if (kind != QKNR_KERNEL_BULK) {
+        rc = plan_register(st, c, wm);
+    } else {
+        if (!bulk_applies(c))
+            return fail(QKNR_ERR_UNSUPPORTED,
+                        "the bulk kernel needs rope_dim %% 8 == 0 and a 16-byte aligned cos|sin table");
+        rc = plan_bulk(st, c, wm);
+    }
+    if (rc) return rc;
+    const int pdl = tune(QKNR_TUNE_PDL);
     wm->pdl = pdl < 0 ? 1 : pdl;
     return QKNR_OK;
 }
 
-DeviceState *current_state(int *dev_out) {
+// One step of the unfused baseline: the register kernel's work map (4 passes
+// per item, 256 threads) with the norm-only or rope-only instantiation.
+int plan_unfused(DeviceState &st, const Call &c, int op, WorkMap *wm) {
+    const int d_idx = head_dim_index(c.head_dim);
+    const int hpw = qknr::kWarp / (c.head_dim / 16);
+    wm->kind = QKNR_KERNEL_REGISTER;
+    wm->passes_per_token = (c.n_qo + c.n_kv + hpw - 1) / hpw;
+    wm->chunks_per_token = (wm->passes_per_token + 3) / 4;
+    wm->max_passes = (wm->passes_per_token + wm->chunks_per_token - 1) / wm->chunks_per_token;
+    wm->u_idx = 1;
+    wm->items = c.num_tokens * wm->chunks_per_token;
+    wm->threads = 256;
+    const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
+    const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
+    const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
+    wm->kernel = dt ? qknr::unfused_kernel_fp16(op, pos64, d_idx, mode)
+                    : qknr::unfused_kernel_bf16(op, pos64, d_idx, mode);
+    if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no unfused kernel for this shape");
+    std::atomic<int> &slot = st.unfused_occ[dt][op - 1][pos64][d_idx][mode];
+    int occ = slot.load(std::memory_order_relaxed);
+    if (occ == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wm->kernel, wm->threads, 0);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(unfused)");
+        if (occ <= 0) return fail(QKNR_ERR_CUDA, "unfused kernel cannot be resident");
+        slot.store(occ, std::memory_order_relaxed);
+    }
+    wm->ctas_per_sm = occ;
+    const long long needed = (wm->items + 7) / 8;
+    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(occ) * st.sm_count)));
+    const int pdl = tune(QKNR_TUNE_PDL);
+    wm->pdl = pdl < 0 ? 1 : pdl;
+    return QKNR_OK;
+}
+
+DeviceState *current_state() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     if (!g_dev[dev].ready.load(std::memory_order_acquire)) return nullptr;
-    if (dev_out) *dev_out = dev;
     return &g_dev[dev];
 }
 
@@ -178,51 +379,50 @@ long long row_bytes(int n, long long head_stride_b, int head_dim) {
     return static_cast<long long>(n - 1) * head_stride_b + 2LL * head_dim;
 }
 
-int validate(void *q, void *k, const void *q_w, const void *k_w, const float *cache,
-             const void *positions, long long num_tokens, int n_qo, int n_kv, int head_dim,
-             int rope_dim, int is_neox, long long q_stride, long long k_stride,
-             long long head_stride, float eps, int dtype) {
+int validate(const Call &c) {
+    const int dtype = c.dtype;
     if ((dtype & ~(0xff | QKNR_POS_I64)) != 0 || ((dtype & 0xff) != QKNR_BF16 && (dtype & 0xff) != QKNR_FP16))
         return fail(QKNR_ERR_INVALID_ARG, "dtype 0x%x is not QKNR_BF16/QKNR_FP16 [| QKNR_POS_I64]", dtype);
-    if (num_tokens < 0) return fail(QKNR_ERR_INVALID_ARG, "num_tokens %lld < 0", num_tokens);
-    if (n_qo < 1 || n_kv < 1) return fail(QKNR_ERR_INVALID_ARG, "head counts n_qo=%d n_kv=%d must be >= 1", n_qo, n_kv);
-    if (!shape_ok(head_dim, rope_dim, is_neox))
+    if (c.num_tokens < 0) return fail(QKNR_ERR_INVALID_ARG, "num_tokens %lld < 0", c.num_tokens);
+    if (c.n_qo < 1 || c.n_kv < 1)
+        return fail(QKNR_ERR_INVALID_ARG, "head counts n_qo=%d n_kv=%d must be >= 1", c.n_qo, c.n_kv);
+    if (!shape_ok(c.head_dim, c.rope_dim, c.is_neox))
         return fail(QKNR_ERR_UNSUPPORTED,
                     "unsupported head_dim=%d rope_dim=%d is_neox=%d (head_dim in {64,128,256}; rope_dim even, "
                     "0 < rope_dim <= head_dim; NeoX needs rope_dim %% 16 == 0 or rope_dim <= 8)",
-                    head_dim, rope_dim, is_neox);
-    if (!std::isfinite(eps) || eps < 0.f) return fail(QKNR_ERR_INVALID_ARG, "eps must be a finite value >= 0");
-    if (!q || !k || !q_w || !k_w || !cache || !positions)
+                    c.head_dim, c.rope_dim, c.is_neox);
+    if (!std::isfinite(c.eps) || c.eps < 0.f) return fail(QKNR_ERR_INVALID_ARG, "eps must be a finite value >= 0");
+    if (!c.q || !c.k || !c.q_w || !c.k_w || !c.cache || !c.positions)
         return fail(QKNR_ERR_INVALID_ARG, "null pointer argument");
-    if (q_stride < 0 || k_stride < 0 || head_stride < 0)
-        return fail(QKNR_ERR_INVALID_ARG, "negative stride");
-    if ((n_qo > 1 || n_kv > 1) && head_stride < head_dim)
-        return fail(QKNR_ERR_INVALID_ARG, "head_stride %lld < head_dim %d: heads overlap", head_stride, head_dim);
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(q_w, 16) || !aligned(k_w, 16))
+    if (c.q_stride < 0 || c.k_stride < 0 || c.head_stride < 0) return fail(QKNR_ERR_INVALID_ARG, "negative stride");
+    if ((c.n_qo > 1 || c.n_kv > 1) && c.head_stride < c.head_dim)
+        return fail(QKNR_ERR_INVALID_ARG, "head_stride %lld < head_dim %d: heads overlap", c.head_stride,
+                    c.head_dim);
+    if (!aligned(c.q, 16) || !aligned(c.k, 16) || !aligned(c.q_w, 16) || !aligned(c.k_w, 16))
         return fail(QKNR_ERR_MISALIGNED, "q, k, q_w and k_w must be 16-byte aligned");
-    if ((q_stride % 8) || (k_stride % 8) || (head_stride % 8))
+    if ((c.q_stride % 8) || (c.k_stride % 8) || (c.head_stride % 8))
         return fail(QKNR_ERR_MISALIGNED, "q_stride, k_stride and head_stride must be multiples of 8 elements");
-    if (!aligned(cache, 4)) return fail(QKNR_ERR_MISALIGNED, "cos_sin_cache must be 4-byte aligned");
-    if (!aligned(positions, (dtype & QKNR_POS_I64) ? 8 : 4))
+    if (!aligned(c.cache, 4)) return fail(QKNR_ERR_MISALIGNED, "cos_sin_cache must be 4-byte aligned");
+    if (!aligned(c.positions, (dtype & QKNR_POS_I64) ? 8 : 4))
         return fail(QKNR_ERR_MISALIGNED, "positions must be aligned to their element size");
 
-    const long long hs_b = head_stride * 2, qs_b = q_stride * 2, ks_b = k_stride * 2;
-    const long long q_row = row_bytes(n_qo, hs_b, head_dim), k_row = row_bytes(n_kv, hs_b, head_dim);
-    if (num_tokens > 1 && (qs_b < q_row || ks_b < k_row))
+    const long long hs_b = c.head_stride * 2, qs_b = c.q_stride * 2, ks_b = c.k_stride * 2;
+    const long long q_row = row_bytes(c.n_qo, hs_b, c.head_dim), k_row = row_bytes(c.n_kv, hs_b, c.head_dim);
+    if (c.num_tokens > 1 && (qs_b < q_row || ks_b < k_row))
         return fail(QKNR_ERR_INVALID_ARG, "token stride smaller than one token's heads: rows overlap");
-    if (num_tokens > 0) {
+    if (c.num_tokens > 0) {
         // q and k must be disjoint. Either their address ranges do not meet, or
         // they interleave inside rows of one common token stride.
-        const uintptr_t qa = reinterpret_cast<uintptr_t>(q), ka = reinterpret_cast<uintptr_t>(k);
-        const uintptr_t q_end = qa + static_cast<uintptr_t>((num_tokens - 1) * qs_b + q_row);
-        const uintptr_t k_end = ka + static_cast<uintptr_t>((num_tokens - 1) * ks_b + k_row);
+        const uintptr_t qa = reinterpret_cast<uintptr_t>(c.q), ka = reinterpret_cast<uintptr_t>(c.k);
+        const uintptr_t q_end = qa + static_cast<uintptr_t>((c.num_tokens - 1) * qs_b + q_row);
+        const uintptr_t k_end = ka + static_cast<uintptr_t>((c.num_tokens - 1) * ks_b + k_row);
         const bool apart = q_end <= ka || k_end <= qa;
         if (!apart) {
             bool ok = false;
             if (qs_b == ks_b && qs_b > 0) {
                 const long long S = qs_b;
                 const long long diff = static_cast<long long>(ka) - static_cast<long long>(qa);
-                const long long off = ((diff % S) + S) % S;   // k row start inside a q row period
+                const long long off = ((diff % S) + S) % S;  // k row start inside a q row period
                 ok = off >= q_row && off + k_row <= S;
             }
             if (!ok) return fail(QKNR_ERR_INVALID_ARG, "q and k overlap in memory");
@@ -231,86 +431,116 @@ int validate(void *q, void *k, const void *q_w, const void *k_w, const float *ca
     return QKNR_OK;
 }
 
-int launch(DeviceState &st, const WorkMap &wm, const Params &prm, cudaStream_t stream) {
+int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(wm.grid));
     cfg.blockDim = dim3(static_cast<unsigned>(wm.threads));
-    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = wm.pdl ? 1 : 0;
-    void *args[] = {const_cast<Params *>(&prm)};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
+    cudaError_t e;
+    if (wm.kind == QKNR_KERNEL_BULK) {
+        BulkParams prm = {};
+        prm.q = static_cast<char *>(c.q);
+        prm.k = static_cast<char *>(c.k);
+        prm.q_w = static_cast<const uint4 *>(c.q_w);
+        prm.k_w = static_cast<const uint4 *>(c.k_w);
+        prm.cache = c.cache;
+        prm.positions = c.positions;
+        prm.status = status;
+        prm.q_stride_b = c.q_stride * 2;
+        prm.k_stride_b = c.k_stride * 2;
+        prm.head_stride_b = c.head_stride * 2;
+        prm.num_tiles = wm.items;
+        prm.cache_len = c.cache_len;
+        prm.n_qo = c.n_qo;
+        prm.n_kv = c.n_kv;
+        prm.rope_dim = c.rope_dim;
+        prm.chunks_per_token = wm.chunks_per_token;
+        prm.heads_per_chunk = wm.heads_per_chunk;
+        prm.stages = wm.stages;
+        prm.stage_bytes = wm.stage_bytes;
+        prm.heads_contig = (c.head_stride == c.head_dim) ? 1 : 0;
+        prm.eps = c.eps;
+        prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
+        cfg.dynamicSmemBytes = static_cast<size_t>(wm.smem_bytes);
+        void *args[] = {&prm};
+        e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
+    } else {
+        Params prm = {};
+        prm.q = static_cast<char *>(c.q);
+        prm.k = static_cast<char *>(c.k);
+        prm.q_w = static_cast<const uint4 *>(c.q_w);
+        prm.k_w = static_cast<const uint4 *>(c.k_w);
+        prm.cache = c.cache;
+        prm.positions = c.positions;
+        prm.status = status;
+        prm.q_stride_b = c.q_stride * 2;
+        prm.k_stride_b = c.k_stride * 2;
+        prm.head_stride_b = c.head_stride * 2;
+        prm.num_items = wm.items;
+        prm.cache_len = c.cache_len;
+        prm.n_qo = c.n_qo;
+        prm.n_kv = c.n_kv;
+        prm.rope_dim = c.rope_dim;
+        prm.chunks_per_token = wm.chunks_per_token;
+        prm.passes_per_token = wm.passes_per_token;
+        prm.cache_vec = (c.rope_dim % 8 == 0) && aligned(c.cache, 16);
+        prm.eps = c.eps;
+        prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
+        cfg.dynamicSmemBytes = 0;
+        void *args[] = {&prm};
+        e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
+    }
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
-    (void)st;
     return QKNR_OK;
 }
 
-int apply_impl(void *q, void *k, const void *q_w, const void *k_w, const float *cache,
-               long long cache_len, const void *positions, long long num_tokens, int n_qo,
-               int n_kv, int head_dim, int rope_dim, int is_neox, long long q_stride,
-               long long k_stride, long long head_stride, float eps, int dtype, void *stream,
-               bool checked) {
-    int dev = -1;
-    DeviceState *st = current_state(&dev);
-    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
-    int rc = validate(q, k, q_w, k_w, cache, positions, num_tokens, n_qo, n_kv, head_dim, rope_dim,
-                      is_neox, q_stride, k_stride, head_stride, eps, dtype);
-    if (rc) return rc;
-    if (checked && cache_len < 0) return fail(QKNR_ERR_INVALID_ARG, "cache_len %lld < 0", cache_len);
-    if (num_tokens == 0) return QKNR_OK;
-
-    WorkMap wm;
-    rc = plan(*st, num_tokens, n_qo, n_kv, head_dim, is_neox, dtype, &wm);
-    if (rc) return rc;
-
-    Params prm = {};
-    prm.q = static_cast<char *>(q);
-    prm.k = static_cast<char *>(k);
-    prm.q_w = static_cast<const uint4 *>(q_w);
-    prm.k_w = static_cast<const uint4 *>(k_w);
-    prm.cache = cache;
-    prm.positions = positions;
-    prm.status = st->status;
-    prm.q_stride_b = q_stride * 2;
-    prm.k_stride_b = k_stride * 2;
-    prm.head_stride_b = head_stride * 2;
-    prm.num_items = wm.items;
-    prm.cache_len = 0;
-    prm.n_qo = n_qo;
-    prm.n_kv = n_kv;
-    prm.rope_dim = rope_dim;
-    prm.chunks_per_token = wm.chunks_per_token;
-    prm.passes_per_token = wm.passes_per_token;
-    prm.cache_vec = (rope_dim % 8 == 0) && aligned(cache, 16);
-    prm.eps = eps;
-    prm.inv_d = 1.0f / static_cast<float>(head_dim);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    if (!checked) return launch(*st, wm, prm, s);
-
-    if (cache_len == 0) return fail(QKNR_ERR_POSITION_OOB, "cache_len is 0: every position is out of range");
-    prm.cache_len = cache_len;
-    std::lock_guard<std::mutex> lock(st->checked_mu);
-    cudaError_t e = cudaMemsetAsync(st->status, 0, sizeof(unsigned long long), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(st->status + 1, 0xff, sizeof(unsigned long long), s);
+// Checked calls: reset the position status, launch, read the status back, report.
+int run_checked(DeviceState &st, const WorkMap &wm, const Call &c, cudaStream_t s,
+                unsigned long long *host_words) {
+    cudaError_t e = cudaMemsetAsync(st.status, 0, sizeof(unsigned long long), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(st.status + 1, 0xff, sizeof(unsigned long long), s);
     if (e != cudaSuccess) return fail_cuda(e, "status reset");
-    rc = launch(*st, wm, prm, s);
+    int rc = launch(wm, c, st.status, s);
     if (rc) return rc;
-    e = cudaMemcpyAsync(st->status_host, st->status, 2 * sizeof(unsigned long long),
+    e = cudaMemcpyAsync(host_words, st.status, kStatusWords * sizeof(unsigned long long),
                         cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail_cuda(e, "status read-back");
-    const unsigned long long bad = st->status_host[0], first = st->status_host[1];
-    if (bad) {
+    if (host_words[2]) {
+        e = cudaMemsetAsync(st.status + 2, 0, sizeof(unsigned long long), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        return fail(QKNR_ERR_WATCHDOG, "a kernel wait ran out (watchdog bits 0x%llx): results are incomplete",
+                    host_words[2]);
+    }
+    if (host_words[0]) {
         return fail(QKNR_ERR_POSITION_OOB,
                     "%llu token(s) have positions outside [0, %lld); first bad token index %llu (left untouched)",
-                    bad, cache_len, first);
+                    host_words[0], c.cache_len, host_words[1]);
     }
     return QKNR_OK;
+}
+
+int apply_impl(const Call &c, void *stream, bool checked) {
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    int rc = validate(c);
+    if (rc) return rc;
+    if (checked && c.cache_len < 0) return fail(QKNR_ERR_INVALID_ARG, "cache_len %lld < 0", c.cache_len);
+    if (c.num_tokens == 0) return QKNR_OK;
+    if (checked && c.cache_len == 0)
+        return fail(QKNR_ERR_POSITION_OOB, "cache_len is 0: every position is out of range");
+    WorkMap wm;
+    rc = plan(*st, c, &wm);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!checked) return launch(wm, c, st->status, s);
+    std::lock_guard<std::mutex> lock(st->checked_mu);
+    return run_checked(*st, wm, c, s, st->status_host);
 }
 
 // ---------------------------------------------------------------------------
@@ -319,20 +549,20 @@ int apply_impl(void *q, void *k, const void *q_w, const void *k_w, const float *
 // Some callers cannot call cudaMalloc at all: code that runs where allocation
 // is forbidden or already accounted for (a pre-sized memory pool, an embedded
 // runtime that owns every device allocation, a plug-in loaded into a host
-// that reserves the allocator for itself). qknr_apply_checked needs a 16-byte
+// that reserves the allocator for itself). qknr_apply_checked needs a small
 // status word, which qknr_init allocates. This variant keeps that word in
 // the file-scope array below instead, so it needs neither qknr_init nor any
 // allocation. The array is part of the library image: every GPU that loads
 // the library holds its 256 bytes until the process exits.
-constexpr int kNoAllocStatusWords = 32;  // 256 bytes; one call uses the first 2 words
+constexpr int kNoAllocStatusWords = 32;  // 256 bytes; one call uses the first kStatusWords
+static_assert(kNoAllocStatusWords >= kStatusWords, "static status array too small");
 static __device__ __align__(256) unsigned long long g_noalloc_status[kNoAllocStatusWords];
 
 struct NoAllocSlot {
     std::once_flag once;
     int setup_rc = QKNR_OK;
     std::string setup_err;
-    DeviceState state;   // status = device address of g_noalloc_status; no host buffer
-    std::mutex call_mu;  // one call at a time per device (the array is shared)
+    DeviceState state;  // status = device address of g_noalloc_status; no host buffer
 };
 NoAllocSlot g_noalloc[kMaxDevices];
 
@@ -358,11 +588,7 @@ void noalloc_setup(NoAllocSlot &slot, int dev) {
     slot.state.ready.store(true, std::memory_order_release);
 }
 
-int apply_checked_noalloc_impl(void *q, void *k, const void *q_w, const void *k_w,
-                               const float *cache, long long cache_len, const void *positions,
-                               long long num_tokens, int n_qo, int n_kv, int head_dim,
-                               int rope_dim, int is_neox, long long q_stride, long long k_stride,
-                               long long head_stride, float eps, int dtype, void *stream) {
+int apply_checked_noalloc_impl(const Call &c, void *stream) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
@@ -371,60 +597,45 @@ int apply_checked_noalloc_impl(void *q, void *k, const void *q_w, const void *k_
     std::call_once(slot.once, noalloc_setup, std::ref(slot), dev);
     if (slot.setup_rc) return fail(slot.setup_rc, "%s", slot.setup_err.c_str());
 
-    int rc = validate(q, k, q_w, k_w, cache, positions, num_tokens, n_qo, n_kv, head_dim, rope_dim,
-                      is_neox, q_stride, k_stride, head_stride, eps, dtype);
+    int rc = validate(c);
     if (rc) return rc;
-    if (cache_len < 0) return fail(QKNR_ERR_INVALID_ARG, "cache_len %lld < 0", cache_len);
-    if (num_tokens == 0) return QKNR_OK;
-    if (cache_len == 0) return fail(QKNR_ERR_POSITION_OOB, "cache_len is 0: every position is out of range");
-    // The status this call needs is 2 words whatever the problem size, so the
-    // fixed array always covers it; guard the invariant all the same.
-    static_assert(kNoAllocStatusWords >= 2, "static status array too small");
-
+    if (c.cache_len < 0) return fail(QKNR_ERR_INVALID_ARG, "cache_len %lld < 0", c.cache_len);
+    if (c.num_tokens == 0) return QKNR_OK;
+    if (c.cache_len == 0) return fail(QKNR_ERR_POSITION_OOB, "cache_len is 0: every position is out of range");
+    // A call needs kStatusWords words whatever its problem size, so the fixed
+    // array always covers it (static_assert above).
     WorkMap wm;
-    rc = plan(slot.state, num_tokens, n_qo, n_kv, head_dim, is_neox, dtype, &wm);
+    rc = plan(slot.state, c, &wm);
     if (rc) return rc;
+    std::lock_guard<std::mutex> lock(slot.state.checked_mu);
+    unsigned long long host_words[kStatusWords] = {0ull, 0ull, 0ull};
+    return run_checked(slot.state, wm, c, static_cast<cudaStream_t>(stream), host_words);
+}
 
-    Params prm = {};
-    prm.q = static_cast<char *>(q);
-    prm.k = static_cast<char *>(k);
-    prm.q_w = static_cast<const uint4 *>(q_w);
-    prm.k_w = static_cast<const uint4 *>(k_w);
-    prm.cache = cache;
-    prm.positions = positions;
-    prm.status = slot.state.status;
-    prm.q_stride_b = q_stride * 2;
-    prm.k_stride_b = k_stride * 2;
-    prm.head_stride_b = head_stride * 2;
-    prm.num_items = wm.items;
-    prm.cache_len = cache_len;
-    prm.n_qo = n_qo;
-    prm.n_kv = n_kv;
-    prm.rope_dim = rope_dim;
-    prm.chunks_per_token = wm.chunks_per_token;
-    prm.passes_per_token = wm.passes_per_token;
-    prm.cache_vec = (rope_dim % 8 == 0) && aligned(cache, 16);
-    prm.eps = eps;
-    prm.inv_d = 1.0f / static_cast<float>(head_dim);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    std::lock_guard<std::mutex> lock(slot.call_mu);
-    // The array keeps the previous call's contents: reset count and first-bad index.
-    e = cudaMemsetAsync(slot.state.status, 0, sizeof(unsigned long long), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(slot.state.status + 1, 0xff, sizeof(unsigned long long), s);
-    if (e != cudaSuccess) return fail_cuda(e, "static status reset");
-    rc = launch(slot.state, wm, prm, s);
-    if (rc) return rc;
-    unsigned long long host_status[2] = {0ull, 0ull};
-    e = cudaMemcpyAsync(host_status, slot.state.status, sizeof host_status, cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return fail_cuda(e, "static status read-back");
-    if (host_status[0]) {
-        return fail(QKNR_ERR_POSITION_OOB,
-                    "%llu token(s) have positions outside [0, %lld); first bad token index %llu (left untouched)",
-                    host_status[0], cache_len, host_status[1]);
-    }
-    return QKNR_OK;
+Call make_call(void *q, void *k, const void *q_w, const void *k_w, const float *cache, long long cache_len,
+               const void *positions, long long num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
+               int is_neox, long long q_stride, long long k_stride, long long head_stride, float eps,
+               int dtype) {
+    Call c;
+    c.q = q;
+    c.k = k;
+    c.q_w = q_w;
+    c.k_w = k_w;
+    c.cache = cache;
+    c.cache_len = cache_len;
+    c.positions = positions;
+    c.num_tokens = num_tokens;
+    c.n_qo = n_qo;
+    c.n_kv = n_kv;
+    c.head_dim = head_dim;
+    c.rope_dim = rope_dim;
+    c.is_neox = is_neox ? 1 : 0;
+    c.q_stride = q_stride;
+    c.k_stride = k_stride;
+    c.head_stride = head_stride;
+    c.eps = eps;
+    c.dtype = dtype;
+    return c;
 }
 
 }  // namespace
@@ -455,14 +666,13 @@ int qknr_init(int device) {
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
     if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return fail_cuda(e, "cudaSetDevice");
     int rc = QKNR_OK;
+    const size_t words = kStatusWords * sizeof(unsigned long long);
     e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) rc = fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
-    if (!rc && (e = cudaMalloc(&st.status, 2 * sizeof(unsigned long long))) != cudaSuccess)
-        rc = fail_cuda(e, "cudaMalloc(status)");
-    if (!rc && (e = cudaMallocHost(&st.status_host, 2 * sizeof(unsigned long long))) != cudaSuccess)
+    if (!rc && (e = cudaMalloc(&st.status, words)) != cudaSuccess) rc = fail_cuda(e, "cudaMalloc(status)");
+    if (!rc && (e = cudaMallocHost(&st.status_host, words)) != cudaSuccess)
         rc = fail_cuda(e, "cudaMallocHost(status)");
-    if (!rc && (e = cudaMemset(st.status, 0, 2 * sizeof(unsigned long long))) != cudaSuccess)
-        rc = fail_cuda(e, "cudaMemset(status)");
+    if (!rc && (e = cudaMemset(st.status, 0, words)) != cudaSuccess) rc = fail_cuda(e, "cudaMemset(status)");
     if (!rc) {
         for (auto &a : st.occupancy)
             for (auto &b : a)
@@ -502,70 +712,120 @@ int qknr_shutdown(void) {
 }
 
 int qknr_apply(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
-               const void *positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim,
-               int rope_dim, int is_neox, int64_t q_stride, int64_t k_stride, int64_t head_stride,
-               float eps, int dtype, void *stream) {
-    return apply_impl(q, k, q_w, k_w, cos_sin_cache, 0, positions, num_tokens, n_qo, n_kv, head_dim,
-                      rope_dim, is_neox ? 1 : 0, q_stride, k_stride, head_stride, eps, dtype, stream,
-                      false);
+               const void *positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
+               int is_neox, int64_t q_stride, int64_t k_stride, int64_t head_stride, float eps, int dtype,
+               void *stream) {
+    return apply_impl(make_call(q, k, q_w, k_w, cos_sin_cache, 0, positions, num_tokens, n_qo, n_kv, head_dim,
+                                rope_dim, is_neox, q_stride, k_stride, head_stride, eps, dtype),
+                      stream, false);
 }
 
-int qknr_apply_checked(void *q, void *k, const void *q_w, const void *k_w,
-                       const float *cos_sin_cache, int64_t cache_len, const void *positions,
-                       int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
-                       int is_neox, int64_t q_stride, int64_t k_stride, int64_t head_stride,
+int qknr_apply_checked(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
+                       int64_t cache_len, const void *positions, int64_t num_tokens, int n_qo, int n_kv,
+                       int head_dim, int rope_dim, int is_neox, int64_t q_stride, int64_t k_stride,
+                       int64_t head_stride, float eps, int dtype, void *stream) {
+    return apply_impl(make_call(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_tokens, n_qo, n_kv,
+                                head_dim, rope_dim, is_neox, q_stride, k_stride, head_stride, eps, dtype),
+                      stream, true);
+}
+
+int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
+                               int64_t cache_len, const void *positions, int64_t num_tokens, int n_qo,
+                               int n_kv, int head_dim, int rope_dim, int is_neox, int64_t q_stride,
+                               int64_t k_stride, int64_t head_stride, float eps, int dtype, void *stream) {
+    return apply_checked_noalloc_impl(make_call(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_tokens,
+                                                n_qo, n_kv, head_dim, rope_dim, is_neox, q_stride, k_stride,
+                                                head_stride, eps, dtype),
+                                      stream);
+}
+
+int qknr_apply_unfused(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
+                       const void *positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim,
+                       int rope_dim, int is_neox, int64_t q_stride, int64_t k_stride, int64_t head_stride,
                        float eps, int dtype, void *stream) {
-    return apply_impl(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_tokens, n_qo, n_kv,
-                      head_dim, rope_dim, is_neox ? 1 : 0, q_stride, k_stride, head_stride, eps,
-                      dtype, stream, true);
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    const Call c = make_call(q, k, q_w, k_w, cos_sin_cache, 0, positions, num_tokens, n_qo, n_kv, head_dim,
+                             rope_dim, is_neox, q_stride, k_stride, head_stride, eps, dtype);
+    int rc = validate(c);
+    if (rc) return rc;
+    if (c.num_tokens == 0) return QKNR_OK;
+    WorkMap norm, rope;
+    rc = plan_unfused(*st, c, qknr::kOpNorm, &norm);
+    if (!rc) rc = plan_unfused(*st, c, qknr::kOpRope, &rope);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = launch(norm, c, st->status, s);
+    if (!rc) rc = launch(rope, c, st->status, s);
+    return rc;
 }
 
-int qknr_set_work_map(int passes_per_item, int threads_per_cta, int ctas_per_sm, int use_pdl) {
-    std::call_once(g_env_once, read_env_overrides);
-    if (passes_per_item < 0 || passes_per_item > qknr::kUnrollClass[qknr::kNumUnroll - 1])
-        return fail(QKNR_ERR_INVALID_ARG, "passes_per_item must be in [0, %d]",
-                    qknr::kUnrollClass[qknr::kNumUnroll - 1]);
-    if (threads_per_cta != 0 && threads_index(threads_per_cta) < 0)
-        return fail(QKNR_ERR_INVALID_ARG, "threads_per_cta must be 0 or one of 64/128/256/512");
-    if (ctas_per_sm < 0) return fail(QKNR_ERR_INVALID_ARG, "ctas_per_sm must be >= 0");
-    if (use_pdl < -1 || use_pdl > 1) return fail(QKNR_ERR_INVALID_ARG, "use_pdl must be -1, 0 or 1");
-    g_force_ppi = passes_per_item;
-    g_force_threads = threads_per_cta;
-    g_force_ctas_per_sm = ctas_per_sm;
-    g_force_pdl = use_pdl;
+int qknr_sync(void *stream) {
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(st->checked_mu);
+    cudaError_t e = cudaMemcpyAsync(st->status_host + 2, st->status + 2, sizeof(unsigned long long),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "qknr_sync");
+    const unsigned long long bits = st->status_host[2];
+    if (bits) {
+        e = cudaMemsetAsync(st->status + 2, 0, sizeof(unsigned long long), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        return fail(QKNR_ERR_WATCHDOG, "a kernel wait ran out (watchdog bits 0x%llx): results are incomplete",
+                    bits);
+    }
     return QKNR_OK;
 }
 
-int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
-                        int is_neox, int dtype, int64_t out[8]) {
+int qknr_set_tuning(int key, int value) {
+    std::call_once(g_env_once, read_env_tuning);
+    if (key == QKNR_TUNE_RESET) {
+        for (int i = 0; i < kNumTuneKeys; ++i) g_tune[i] = kTuneAuto[i];
+        return QKNR_OK;
+    }
+    int rc = tune_check(key, value);
+    if (rc) return rc;
+    g_tune[key] = value;
+    return QKNR_OK;
+}
+
+int qknr_get_tuning(int key, int *value) {
+    if (!value) return fail(QKNR_ERR_INVALID_ARG, "value is null");
+    if (key <= 0 || key >= kNumTuneKeys) return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
+    *value = tune(key);
+    return QKNR_OK;
+}
+
+int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim, int is_neox,
+                        int dtype, int64_t *out) {
     if (!out) return fail(QKNR_ERR_INVALID_ARG, "out is null");
-    DeviceState *st = current_state(nullptr);
+    DeviceState *st = current_state();
     if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
     if (num_tokens < 0 || n_qo < 1 || n_kv < 1) return fail(QKNR_ERR_INVALID_ARG, "bad sizes");
     if (!qknr_can_use(head_dim, rope_dim, is_neox, dtype))
         return fail(QKNR_ERR_UNSUPPORTED, "shape outside the accepted set");
+    // the plan depends on the table only through its alignment: use an aligned stand-in
+    Call c = make_call(nullptr, nullptr, nullptr, nullptr, reinterpret_cast<const float *>(uintptr_t(256)), 0,
+                       nullptr, num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, 0, 0, head_dim, 1e-6f,
+                       dtype);
     WorkMap wm;
-    int rc = plan(*st, num_tokens, n_qo, n_kv, head_dim, is_neox, dtype, &wm);
+    int rc = plan(*st, c, &wm);
     if (rc) return rc;
-    out[0] = wm.grid;
-    out[1] = wm.threads;
-    out[2] = wm.items;
-    out[3] = wm.chunks_per_token;
-    out[4] = wm.passes_per_token;
-    out[5] = qknr::kUnrollClass[wm.u_idx];
-    out[6] = wm.ctas_per_sm;
-    out[7] = wm.pdl;
+    out[0] = wm.kind;
+    out[1] = wm.grid;
+    out[2] = wm.threads;
+    out[3] = wm.items;
+    out[4] = wm.chunks_per_token;
+    out[5] = wm.ctas_per_sm;
+    out[6] = wm.pdl;
+    out[7] = wm.kind == QKNR_KERNEL_BULK ? wm.heads_per_chunk : wm.passes_per_token;
+    out[8] = wm.kind == QKNR_KERNEL_BULK ? wm.stages : qknr::kUnrollClass[wm.u_idx];
+    out[9] = wm.kind == QKNR_KERNEL_BULK ? wm.consumers : 0;
+    out[10] = wm.smem_bytes;
+    out[11] = wm.stage_bytes;
     return QKNR_OK;
-}
-
-int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_w,
-                               const float *cos_sin_cache, int64_t cache_len, const void *positions,
-                               int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
-                               int is_neox, int64_t q_stride, int64_t k_stride, int64_t head_stride,
-                               float eps, int dtype, void *stream) {
-    return apply_checked_noalloc_impl(q, k, q_w, k_w, cos_sin_cache, cache_len, positions, num_tokens,
-                                      n_qo, n_kv, head_dim, rope_dim, is_neox ? 1 : 0, q_stride,
-                                      k_stride, head_stride, eps, dtype, stream);
 }
 
 }  // extern "C"

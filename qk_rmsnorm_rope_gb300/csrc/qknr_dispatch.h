@@ -16,4 +16,13 @@ constexpr int kHeadDims[kNumHeadDim] = {64, 128, 256};
 const void *kernel_bf16(int pos64, int d_idx, int mode, int u_idx);
 const void *kernel_fp16(int pos64, int d_idx, int mode, int u_idx);
 
+// Bulk-copy ring kernel entry for (position type, head_dim class, mode).
+const void *bulk_kernel_bf16(int pos64, int d_idx, int mode);
+const void *bulk_kernel_fp16(int pos64, int d_idx, int mode);
+
+// One step of the unfused two-kernel baseline (op = kOpNorm or kOpRope), the
+// register kernel with 4 passes per item. Norm-only ignores pos64 and mode.
+const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode);
+const void *unfused_kernel_fp16(int op, int pos64, int d_idx, int mode);
+
 }  // namespace qknr

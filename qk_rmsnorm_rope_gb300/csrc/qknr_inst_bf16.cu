@@ -1,5 +1,6 @@
-// qknr_inst_bf16.cu -- explicit instantiations of the fused kernel for bf16 storage.
+// qknr_inst_bf16.cu -- explicit instantiations of the fused kernels (register and bulk-copy ring) for bf16 storage.
 #include "qknr_dispatch.h"
+#include "qknr_bulk_kernel.cuh"
 #include "qknr_kernel.cuh"
 
 namespace qknr {
@@ -34,7 +35,49 @@ const void *by_head_dim(int d_idx, int mode, int u_idx) {
     }
 }
 
+template <class P, int D>
+const void *bulk_by_mode(int mode) {
+    return mode == kNeox ? reinterpret_cast<const void *>(&qknr_bulk_kernel<__nv_bfloat16, P, D, kNeox>)
+                         : reinterpret_cast<const void *>(&qknr_bulk_kernel<__nv_bfloat16, P, D, kInterleaved>);
+}
+
+template <class P>
+const void *bulk_by_head_dim(int d_idx, int mode) {
+    switch (d_idx) {
+        case 0: return bulk_by_mode<P, 64>(mode);
+        case 1: return bulk_by_mode<P, 128>(mode);
+        case 2: return bulk_by_mode<P, 256>(mode);
+        default: return nullptr;
+    }
+}
+
+template <int D>
+const void *unfused_by_op(int op, int pos64, int mode) {
+    if (op == kOpNorm)
+        return reinterpret_cast<const void *>(&qknr_fused_kernel<__nv_bfloat16, int, D, kInterleaved, 4, kOpNorm>);
+    if (op != kOpRope) return nullptr;
+    if (pos64)
+        return mode == kNeox
+                   ? reinterpret_cast<const void *>(&qknr_fused_kernel<__nv_bfloat16, long long, D, kNeox, 4, kOpRope>)
+                   : reinterpret_cast<const void *>(&qknr_fused_kernel<__nv_bfloat16, long long, D, kInterleaved, 4, kOpRope>);
+    return mode == kNeox ? reinterpret_cast<const void *>(&qknr_fused_kernel<__nv_bfloat16, int, D, kNeox, 4, kOpRope>)
+                         : reinterpret_cast<const void *>(&qknr_fused_kernel<__nv_bfloat16, int, D, kInterleaved, 4, kOpRope>);
+}
+
 }  // namespace
+
+const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode) {
+    switch (d_idx) {
+        case 0: return unfused_by_op<64>(op, pos64, mode);
+        case 1: return unfused_by_op<128>(op, pos64, mode);
+        case 2: return unfused_by_op<256>(op, pos64, mode);
+        default: return nullptr;
+    }
+}
+
+const void *bulk_kernel_bf16(int pos64, int d_idx, int mode) {
+    return pos64 ? bulk_by_head_dim<long long>(d_idx, mode) : bulk_by_head_dim<int>(d_idx, mode);
+}
 
 const void *kernel_bf16(int pos64, int d_idx, int mode, int u_idx) {
     return pos64 ? by_head_dim<long long>(d_idx, mode, u_idx) : by_head_dim<int>(d_idx, mode, u_idx);

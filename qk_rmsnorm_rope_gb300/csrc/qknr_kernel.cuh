@@ -36,6 +36,10 @@ constexpr int kWarp = 32;
 
 enum Mode : int { kInterleaved = 0, kNeox = 1 };
 
+// What a launch computes: the fused op, or one half of the unfused two-kernel
+// chain the fused op replaces (RMSNorm alone, then RoPE alone, each in place).
+enum Op : int { kOpFused = 0, kOpNorm = 1, kOpRope = 2 };
+
 // Kernel parameters, passed by value as a __grid_constant__.
 struct Params {
     char *q;                      // head (0,0) of q
@@ -123,8 +127,9 @@ __device__ __forceinline__ long long load_position(const void *positions, long l
 }
 
 // T: storage type (bf16/half); P: position type (int / long long);
-// D: head_dim; MODE: pairing; UMAX: max warp passes per item (loads in flight).
-template <class T, class P, int D, int MODE, int UMAX>
+// D: head_dim; MODE: pairing; UMAX: max warp passes per item (loads in flight);
+// OP: fused (the product) or one step of the unfused baseline.
+template <class T, class P, int D, int MODE, int UMAX, int OP = kOpFused>
 __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__ Params p) {
     constexpr int LPH = D / 16;         // lanes per head
     constexpr int HPW = kWarp / LPH;    // heads per warp pass
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     for (long long it = it_begin; it < it_end; ++it) {
         const long long t = it / p.chunks_per_token;
         const int ch = static_cast<int>(it - t * p.chunks_per_token);
-        if (t != cur_t) {
+        if (OP != kOpNorm && t != cur_t) {
             cur_t = t;
             const long long pos = load_position<P>(p.positions, t);
             if (p.cache_len > 0) {
@@ -281,28 +286,32 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
             unpack8<T>(xa[u], a);
             unpack8<T>(xb[u], b);
 
-            float ss0 = 0.f, ss1 = 0.f;
+            if (OP != kOpRope) {
+                float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                ss0 = fmaf(a[e], a[e], ss0);
-                ss1 = fmaf(b[e], b[e], ss1);
-            }
-            float ss = ss0 + ss1;
+                for (int e = 0; e < 8; ++e) {
+                    ss0 = fmaf(a[e], a[e], ss0);
+                    ss1 = fmaf(b[e], b[e], ss1);
+                }
+                float ss = ss0 + ss1;
 #pragma unroll
-            for (int off = LPH / 2; off > 0; off >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float r = rsqrtf(fmaf(ss, p.inv_d, p.eps));
+                for (int off = LPH / 2; off > 0; off >>= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float r = rsqrtf(fmaf(ss, p.inv_d, p.eps));
 
-            float wa[8], wb[8];
-            unpack8<T>(is_q ? wqa : wka, wa);
-            unpack8<T>(is_q ? wqb : wkb, wb);
+                float wa[8], wb[8];
+                unpack8<T>(is_q ? wqa : wka, wa);
+                unpack8<T>(is_q ? wqb : wkb, wb);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                a[e] = a[e] * r * wa[e];
-                b[e] = b[e] * r * wb[e];
+                for (int e = 0; e < 8; ++e) {
+                    a[e] = a[e] * r * wa[e];
+                    b[e] = b[e] * r * wb[e];
+                }
             }
 
-            if (MODE == kInterleaved) {
+            if (OP == kOpNorm) {
+                // no rotation in the norm-only step
+            } else if (MODE == kInterleaved) {
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const float a0 = a[2 * m], a1 = a[2 * m + 1];

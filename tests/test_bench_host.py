@@ -86,9 +86,10 @@ def test_profiled_traffic_requires_matching_sources(tmp_path, monkeypatch):
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "qk_rmsnorm_rope_gb300").symlink_to(os.path.join(ROOT, "qk_rmsnorm_rope_gb300"))
-    f = prof / f"{bench.KERNEL_NAME}_dit.txt"
+    f = prof / "qknr_bulk_kernel_dit.txt"
     f.write_text(f"source_sha256: {bench.kernel_source_hash()}\ntraffic_bytes_per_launch: 123\n")
-    assert bench.profiled_traffic("dit") == 123.0
+    assert bench.profiled_traffic("qknr_bulk_kernel", "dit") == 123.0
     f.write_text("source_sha256: 00\ntraffic_bytes_per_launch: 123\n")
-    assert bench.profiled_traffic("dit") is None
-    assert bench.profiled_traffic("gqa") is None
+    assert bench.profiled_traffic("qknr_bulk_kernel", "dit") is None
+    assert bench.profiled_traffic("qknr_bulk_kernel", "gqa") is None
+    assert bench.profiled_traffic("qknr_fused_kernel", "dit") is None

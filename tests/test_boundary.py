@@ -95,14 +95,20 @@ def test_can_use_rejects():
     assert qknr.qknr_can_use(64, 2, 0, 0) == 1
 
 
-def test_set_work_map_validation():
-    assert qknr.qknr_set_work_map(5, 0, 0, -1) == 2
-    assert qknr.qknr_set_work_map(0, 96, 0, -1) == 2
-    assert qknr.qknr_set_work_map(0, 0, -1, -1) == 2
-    assert qknr.qknr_set_work_map(0, 0, 0, 2) == 2
-    assert "use_pdl" in qknr.qknr_last_error()
-    assert qknr.qknr_set_work_map(2, 128, 3, 0) == 0
-    assert qknr.qknr_set_work_map(0, 0, 0, -1) == 0
+def test_set_tuning_validation():
+    K = qknr.TUNE_KEYS
+    bad = [(K["kernel"], 3), (K["passes"], 5), (K["threads"], 96), (K["ctas_per_sm"], -1),
+           (K["pdl"], 2), (K["consumers"], 17), (K["stages"], 33), (K["tile_bytes"], 100), (99, 0)]
+    for key, value in bad:
+        assert qknr.qknr_set_tuning(key, value) == 2, (key, value)
+    assert "tuning key" in qknr.qknr_last_error()
+    qknr.set_tuning(kernel=1, passes=2, threads=128, ctas_per_sm=3, pdl=0, consumers=4, stages=8,
+                    tile_bytes=4096)
+    assert qknr.get_tuning("kernel") == 1 and qknr.get_tuning("stages") == 8
+    assert qknr.get_tuning("pdl") == 0
+    qknr.set_tuning(reset=True)
+    assert qknr.get_tuning("kernel") == 0 and qknr.get_tuning("pdl") == -1
+    assert qknr.get_tuning("tile_bytes") == 0
 
 
 def test_apply_rejects_cpu_tensors():
@@ -136,9 +142,10 @@ import qk_rmsnorm_rope_gb300 as q
 rc = q.qknr_apply(16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 1e-6, 0, None)
 print(rc, q.qknr_last_error())
 rc2 = q.qknr_apply_checked(16, 16, 16, 16, 16, 4, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 1e-6, 0, None)
-out = (ctypes.c_int64 * 8)()
+out = (ctypes.c_int64 * 12)()
 rc3 = q.qknr_query_work_map(8, 1, 1, 128, 128, 0, 0, out)
-print(rc2, rc3)
+rc4 = q.qknr_sync(None)
+print(rc2, rc3, rc4)
 """
 
 
@@ -150,4 +157,4 @@ def test_calls_before_init_are_refused():
     assert r.returncode == 0, r.stderr
     first, second = r.stdout.strip().splitlines()[-2:]
     assert first.startswith("1 ") and "qknr_init" in first
-    assert second.split() == ["1", "1"]
+    assert second.split() == ["1", "1", "1"]

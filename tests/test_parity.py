@@ -35,9 +35,10 @@ def qknr():
     import qk_rmsnorm_rope_gb300 as q
     torch.cuda.set_device(0)
     q.init(0)
-    q.qknr_set_work_map(0, 0, 0, -1)
+    q.set_tuning(reset=True)
     yield q
-    q.qknr_set_work_map(0, 0, 0, -1)
+    q.set_tuning(reset=True)
+    q.sync()   # no kernel wait ran out during the module
 
 
 def _expected(cpu, w):
@@ -142,12 +143,19 @@ def _make(D, R, neox, pos, T, n_qo, n_kv, dtype="bf16", seed=0, cache_len=300, b
                               seed=seed)
 
 
+@pytest.mark.parametrize("kernel", ["bulk", "register"])
 @pytest.mark.parametrize("D,R,neox,pos,T", GRID,
                          ids=[f"D{g[0]}-R{g[1]}-{'neox' if g[2] else 'inter'}-{g[3]}-T{g[4]}"
                               for g in GRID])
-def test_shape_grid(qknr, D, R, neox, pos, T):
+def test_shape_grid(qknr, D, R, neox, pos, T, kernel):
+    """Both kernels over the grid; the bulk kernel applies where rope_dim % 8 == 0
+    (elsewhere that case runs the register kernel)."""
     w = _make(D, R, neox, pos, T, 4, 2, dtype="bf16" if (D + R + T) % 2 == 0 else "fp16")
-    _check_workload(qknr, w)
+    qknr.set_tuning(reset=True, kernel=2 if (kernel == "bulk" and R % 8 == 0) else 1)
+    try:
+        _check_workload(qknr, w)
+    finally:
+        qknr.set_tuning(reset=True)
 
 
 @pytest.mark.parametrize("n_qo,n_kv", [(1, 1), (8, 1), (32, 8), (5, 3), (1, 7), (64, 64)])
@@ -157,29 +165,72 @@ def test_gqa_head_counts(qknr, n_qo, n_kv, D):
     _check_workload(qknr, w)
 
 
-@pytest.mark.parametrize("ppi,threads,ctas", [(1, 64, 1), (2, 128, 0), (3, 256, 2), (4, 512, 0),
-                                              (4, 64, 0), (1, 256, 0)])
-def test_work_maps_agree_bit_for_bit(qknr, ppi, threads, ctas):
-    """Per-head results do not depend on the work map: every forced map gives
-    the same bits as the automatic one, and all match the oracle."""
-    for name, T in (("mha_neox", 97), ("fused_qkv", 41), ("tiny", 16)):
+TUNINGS = [
+    dict(kernel=1, passes=1, threads=64, ctas_per_sm=1),
+    dict(kernel=1, passes=2, threads=128),
+    dict(kernel=1, passes=3, threads=256, ctas_per_sm=2),
+    dict(kernel=1, passes=4, threads=512),
+    dict(kernel=1, passes=4, threads=64, pdl=0),
+    dict(kernel=2),
+    dict(kernel=2, consumers=1, stages=1),
+    dict(kernel=2, consumers=3, stages=7),
+    dict(kernel=2, consumers=16),
+    dict(kernel=2, tile_bytes=512),
+    dict(kernel=2, tile_bytes=1536, consumers=2, stages=4),
+    dict(kernel=2, ctas_per_sm=2),
+    dict(kernel=2, pdl=0, consumers=4, stages=4),
+]
+
+
+@pytest.mark.parametrize("tuning", TUNINGS, ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_tunings_agree_bit_for_bit(qknr, tuning):
+    """Per-head results do not depend on the kernel or its launch tuning: every
+    forced setting gives the same bits as the automatic one, and all match the
+    oracle. Covers several items/tiles per token, one-stage rings, ragged ring
+    depths and two CTAs per SM."""
+    for name, T in (("mha_neox", 97), ("fused_qkv", 41), ("tiny", 16), ("gqa", 50)):
         base = workloads.get(name)
         w = workloads.scaled(base, T, cache_len=min(base.cache_len, 4096))
         cpu = workloads.make_inputs(w)
         ref = workloads.to_device(cpu, w, "cuda")
-        qknr.qknr_set_work_map(0, 0, 0, -1)
+        qknr.set_tuning(reset=True)
         _run_gpu(qknr, ref, w)
         dev = workloads.to_device(cpu, w, "cuda")
-        assert qknr.qknr_set_work_map(ppi, threads, ctas, 0) == 0
+        qknr.set_tuning(reset=True, **tuning)
         try:
             _run_gpu(qknr, dev, w)
         finally:
-            qknr.qknr_set_work_map(0, 0, 0, -1)
+            qknr.set_tuning(reset=True)
         assert torch.equal(dev["q"].view(torch.int16), ref["q"].view(torch.int16)), name
         assert torch.equal(dev["k"].view(torch.int16), ref["k"].view(torch.int16)), name
         eq, ek = _expected(cpu, w)
         _assert_close(dev["q"].double().cpu().numpy(), eq, w.torch_dtype, name)
         _assert_close(dev["k"].double().cpu().numpy(), ek, w.torch_dtype, name)
+
+
+def test_kernel_choice(qknr):
+    """The automatic choice is the register kernel; the bulk kernel runs when
+    asked for, and forcing it where it does not apply is refused before any
+    launch."""
+    bf = qknr.QKNR_BF16
+    assert qknr.work_map(4608, 24, 24, 128, 128, False, bf)["kernel"] == "register"
+    assert qknr.work_map(100, 4, 2, 128, 6, False, bf)["kernel"] == "register"
+    qknr.set_tuning(kernel=2)
+    m = qknr.work_map(4608, 24, 24, 128, 128, False, bf)
+    qknr.set_tuning(reset=True)
+    assert m["kernel"] == "bulk"
+    assert m["unroll_or_stages"] % m["consumers"] == 0 and m["smem_bytes"] <= 232448
+    w = _make(128, 6, False, "i32", 9, 2, 2)
+    dev = workloads.make_inputs(w, device="cuda")
+    before = dev["q"].clone()
+    qknr.set_tuning(kernel=2)
+    try:
+        with pytest.raises(qknr.QknrError) as e:
+            _run_gpu(qknr, dev, w)
+        assert e.value.code == 3
+    finally:
+        qknr.set_tuning(reset=True)
+    assert torch.equal(dev["q"], before)
 
 
 def test_separate_strides_and_padded_heads(qknr):
@@ -271,7 +322,16 @@ def test_empty_and_errors_leave_inputs_untouched(qknr):
     assert torch.equal(dev["q"], before_q) and torch.equal(dev["k"], before_k)
 
 
-def test_checked_variant(qknr):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_checked_variant(qknr, kernel):
+    qknr.set_tuning(reset=True, kernel=kernel)
+    try:
+        _checked_variant(qknr)
+    finally:
+        qknr.set_tuning(reset=True)
+
+
+def _checked_variant(qknr):
     w = _make(128, 128, False, "i64", 70, 4, 2, cache_len=64, seed=4)
     cpu = workloads.make_inputs(w)
     # all in range: same bits as the unchecked call
@@ -317,4 +377,61 @@ def test_streams_and_repeat_determinism(qknr):
         qknr.apply(b["q"], b["k"], b["q_w"], b["k_w"], b["cos_sin_cache"], b["positions"],
                    is_neox=True, eps=w.eps)
     s.synchronize()
+    assert torch.equal(a["q"], b["q"]) and torch.equal(a["k"], b["k"])
+
+
+def _pair_norms(o, R, neox):
+    """Length of the rotation pair each element belongs to (|o| past rope_dim)."""
+    pn = np.abs(o).copy()
+    half = R // 2
+    if neox:
+        a, b = o[..., :half], o[..., half:R]
+        n = np.sqrt(a * a + b * b)
+        pn[..., :half] = n
+        pn[..., half:R] = n
+    else:
+        a, b = o[..., 0:R:2], o[..., 1:R:2]
+        n = np.sqrt(a * a + b * b)
+        pn[..., 0:R:2] = n
+        pn[..., 1:R:2] = n
+    return pn
+
+
+@pytest.mark.parametrize("name,T", REDUCED, ids=[r[0] for r in REDUCED])
+def test_unfused_baseline(qknr, name, T):
+    """The unfused two-kernel chain (RMSNorm kernel, then RoPE kernel) against
+    the oracle. Its stored intermediate adds one rounding before the rotation,
+    bounded by u * |(n_a, n_b)| per rotated element (u = 2^-8 bf16, 2^-11
+    fp16), so the bound is 2u * pair length + the fused bound."""
+    base = workloads.get(name)
+    w = workloads.scaled(base, T, cache_len=min(base.cache_len, 8192))
+    cpu = workloads.make_inputs(w)
+    eq, ek = _expected(cpu, w)
+    dev = workloads.to_device(cpu, w, "cuda")
+    qknr.apply_unfused(dev["q"], dev["k"], dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
+                       dev["positions"], is_neox=w.is_neox, eps=w.eps)
+    torch.cuda.synchronize()
+    u = 2.0 ** -8 if w.torch_dtype == torch.bfloat16 else 2.0 ** -11
+    for got, exp in ((dev["q"], eq), (dev["k"], ek)):
+        g = got.double().cpu().numpy()
+        tol = 2 * u * _pair_norms(exp, w.rope_dim, w.is_neox) + oracle.tolerance(exp, w.torch_dtype)
+        assert np.all(np.abs(g - exp) <= tol), float(np.max(np.abs(g - exp) / tol))
+    if w.fused_total_heads:
+        lo = w.n_qo + w.n_kv
+        assert torch.equal(dev["buffer"][:, lo:, :].cpu().view(torch.int16),
+                           cpu["buffer"][:, lo:, :].view(torch.int16))
+
+
+def test_unfused_norm_step_is_the_fused_op_at_position_zero(qknr):
+    """With every position 0 the RoPE step is the identity, so the unfused
+    chain must give exactly the fused op's bits."""
+    w = _make(128, 64, True, "i32", 77, 6, 2, seed=12)
+    cpu = workloads.make_inputs(w)
+    cpu["positions"].zero_()
+    a = workloads.to_device(cpu, w, "cuda")
+    b = workloads.to_device(cpu, w, "cuda")
+    _run_gpu(qknr, a, w)
+    qknr.apply_unfused(b["q"], b["k"], b["q_w"], b["k_w"], b["cos_sin_cache"], b["positions"],
+                       is_neox=True, eps=w.eps)
+    torch.cuda.synchronize()
     assert torch.equal(a["q"], b["q"]) and torch.equal(a["k"], b["k"])

@@ -1,0 +1,64 @@
+"""The PyTorch custom-op registration (torch.ops.qknr.fused_inplace_qknorm_rope).
+
+CPU: the schema declares q and k as mutated and the op returns nothing; the
+shape gate agrees with the C ABI's. GPU: the op gives the same bits as the
+direct call, eagerly and under torch.compile (aot_eager backend, one graph),
+where the mutation must be visible to the code after the op."""
+import os
+import sys
+
+import pytest
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+import workloads  # noqa: E402
+from qk_rmsnorm_rope_gb300 import torch_op  # noqa: E402
+
+
+def test_schema_declares_mutation():
+    schema = str(torch.ops.qknr.fused_inplace_qknorm_rope.default._schema)
+    assert "Tensor(a0!) q" in schema and "Tensor(a1!) k" in schema
+    assert schema.endswith("-> ()")
+
+
+def test_can_use_gate():
+    assert torch_op.can_use_fused_inplace_qknorm_rope(128, 64, True, torch.float16)
+    assert torch_op.can_use_fused_inplace_qknorm_rope(256, 128, False, torch.bfloat16)
+    assert not torch_op.can_use_fused_inplace_qknorm_rope(96, 64, False, torch.bfloat16)
+    assert not torch_op.can_use_fused_inplace_qknorm_rope(128, 64, False, torch.float32)
+
+
+@pytest.mark.gpu
+def test_op_matches_direct_call_eager_and_compiled():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import qk_rmsnorm_rope_gb300 as q
+    torch.cuda.set_device(0)
+    q.init(0)
+    w = workloads.scaled(workloads.get("gqa"), 64, cache_len=1024)
+    cpu = workloads.make_inputs(w)
+    ref = workloads.to_device(cpu, w, "cuda")
+    q.apply(ref["q"], ref["k"], ref["q_w"], ref["k_w"], ref["cos_sin_cache"], ref["positions"],
+            is_neox=w.is_neox, eps=w.eps)
+    eager = workloads.to_device(cpu, w, "cuda")
+    torch.ops.qknr.fused_inplace_qknorm_rope(eager["q"], eager["k"], eager["q_w"], eager["k_w"],
+                                             eager["cos_sin_cache"], eager["positions"],
+                                             w.is_neox, w.eps)
+
+    def step(qq, kk, qw, kw, cache, pos):
+        qq = qq * 1.0          # a fresh tensor that the op then mutates inside the graph
+        kk = kk * 1.0
+        torch.ops.qknr.fused_inplace_qknorm_rope(qq, kk, qw, kw, cache, pos, True, w.eps)
+        return qq + 0.0, kk + 0.0
+
+    compiled = torch.compile(step, backend="aot_eager", fullgraph=True)
+    src = workloads.to_device(cpu, w, "cuda")
+    cq, ck = compiled(src["q"], src["k"], src["q_w"], src["k_w"], src["cos_sin_cache"],
+                      src["positions"])
+    torch.cuda.synchronize()
+    for d in (eager,):
+        assert torch.equal(d["q"], ref["q"]) and torch.equal(d["k"], ref["k"])
+    assert torch.equal(cq, ref["q"]) and torch.equal(ck, ref["k"])
+    # the compiled function worked on copies: its inputs keep their values
+    assert torch.equal(src["q"].cpu(), cpu["q"])
