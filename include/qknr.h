@@ -199,9 +199,9 @@ int qknr_sync(void *stream);
 #define QKNR_TUNE_THREADS 3     /* register kernel: threads per CTA, 64/128/256/512 (0 auto = 256) */
 #define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy; bulk: 1) */
 #define QKNR_TUNE_PDL 5         /* programmatic dependent launch: -1 auto (on), 0 off, 1 on */
-#define QKNR_TUNE_CONSUMERS 6   /* bulk kernel: consumer warps per CTA, 1..16 (0 auto = 8) */
-#define QKNR_TUNE_STAGES 7      /* bulk kernel: ring depth, 1..32 (0 auto: what fits); rounded down to a
-                                   multiple of the consumer count */
+#define QKNR_TUNE_CONSUMERS 6   /* bulk kernel: consumer warps per CTA, 1..16 (0 auto: one per warp
+                                   pass of a tile, 4..16) */
+#define QKNR_TUNE_STAGES 7      /* bulk kernel: ring depth, 1..32 (0 auto: what fits) */
 #define QKNR_TUNE_TILE_BYTES 8  /* bulk kernel: max bytes of heads per tile (0 auto = 24576) */
 
 /*

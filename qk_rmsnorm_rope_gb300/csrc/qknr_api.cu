@@ -260,8 +260,8 @@ bool bulk_applies(const Call &c) { return (c.rope_dim % 8) == 0 && aligned(c.cac
 
 // Bulk kernel: tiles are (token, chunk of heads) of at most `tile` bytes of
 // heads; one producer warp and `consumers` consumer warps per CTA; the ring
-// depth is the largest multiple of the consumer count that fits the shared
-// memory of the CTAs resident per SM (default one CTA per SM).
+// is as deep as the shared memory of the CTAs resident per SM allows (default
+// one CTA per SM), at most kMaxStages.
 int plan_bulk(DeviceState &st, const Call &c, WorkMap *wm) {
     const int d_idx = head_dim_index(c.head_dim);
     const int heads = c.n_qo + c.n_kv;
@@ -281,13 +281,15 @@ int plan_bulk(DeviceState &st, const Call &c, WorkMap *wm) {
     const int smem_cap = std::min(kMaxBulkSmem, (228 * 1024) / ctas - 1024);
     const int fit = (smem_cap - qknr::bulk_stage_offset(kMaxStages)) / wm->stage_bytes;
     if (fit < 1) return fail(QKNR_ERR_UNSUPPORTED, "a %d-byte tile does not fit shared memory", wm->stage_bytes);
+    // all consumer warps share each tile; by default one warp per warp pass of
+    // a tile (at least 4, at most 16)
+    const int passes = (wm->heads_per_chunk + (qknr::kWarp / (c.head_dim / 16)) - 1) /
+                       (qknr::kWarp / (c.head_dim / 16));
     int consumers = tune(QKNR_TUNE_CONSUMERS);
-    if (consumers <= 0) consumers = 8;
+    if (consumers <= 0) consumers = std::min(16, std::max(4, passes));
     int stages = tune(QKNR_TUNE_STAGES);
     if (stages <= 0) stages = kMaxStages;
     stages = std::min(stages, fit);
-    if (consumers > stages) consumers = stages;
-    stages = stages / consumers * consumers;  // each stage belongs to one consumer warp
     wm->stages = stages;
     wm->consumers = consumers;
     wm->threads = qknr::kWarp * (1 + consumers);

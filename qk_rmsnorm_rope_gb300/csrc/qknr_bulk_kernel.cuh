@@ -17,11 +17,12 @@
 //    stage's full mbarrier with the byte count and issues the copies. In the
 //    checked mode a tile whose position is outside the cache is not copied: it
 //    is flagged, counted, and its stage is released at once.
-//  * consumer warps take the CTA's tiles round robin (the ring depth is a
-//    multiple of the consumer count, so each stage belongs to one consumer and
-//    its mbarrier phases are awaited in order), wait on the full mbarrier, compute from shared memory with the register kernel's lane
-//    mapping (two 16-byte vectors per lane, no pairing shuffles) and store
-//    128-bit results straight to global memory, then release the stage.
+//  * all consumer warps work on every tile, in order: each takes every NC-th
+//    warp pass of the tile, two passes at a time with independent dependency
+//    chains, computing from shared memory with the register kernel's lane
+//    mapping (two 16-byte vectors per lane, no pairing shuffles) and storing
+//    128-bit results straight to global memory; the stage is free again once
+//    all NC consumers have arrived on its empty mbarrier.
 //  * tiles are split across CTAs in balanced contiguous ranges; the grid is
 //    persistent (one wave).
 //  * every mbarrier wait is bounded by %globaltimer. A wait that runs out sets
@@ -144,6 +145,64 @@ __device__ __forceinline__ float4 lds_f4(const float *p) {
     return *reinterpret_cast<const float4 *>(p);
 }
 
+// One head slot of a warp pass: the lane's two vectors xa, xb (raw storage)
+// are replaced by the op's output (raw storage). Every lane of the warp must
+// call it (the sum of squares is reduced across the head's lanes); lanes
+// without a head pass zeros and do not store.
+template <class T, int MODE, int LPH>
+__device__ __forceinline__ void fused_head(uint4 &xa, uint4 &xb, const uint4 &wpa, const uint4 &wpb,
+                                           const float (&c8)[8], const float (&s8)[8], bool split,
+                                           bool rot_lane, int half, float inv_d, float eps) {
+    float a[8], b[8];
+    unpack8<T>(xa, a);
+    unpack8<T>(xb, b);
+    float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        ss0 = fmaf(a[e], a[e], ss0);
+        ss1 = fmaf(b[e], b[e], ss1);
+    }
+    float ss = ss0 + ss1;
+#pragma unroll
+    for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float r = rsqrtf(fmaf(ss, inv_d, eps));
+    float wa[8], wb[8];
+    unpack8<T>(wpa, wa);
+    unpack8<T>(wpb, wb);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        a[e] = a[e] * r * wa[e];
+        b[e] = b[e] * r * wb[e];
+    }
+    if (MODE == kInterleaved) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float a0 = a[2 * m], a1 = a[2 * m + 1];
+            a[2 * m] = a0 * c8[m] - a1 * s8[m];
+            a[2 * m + 1] = a1 * c8[m] + a0 * s8[m];
+            const float b0 = b[2 * m], b1 = b[2 * m + 1];
+            b[2 * m] = b0 * c8[4 + m] - b1 * s8[4 + m];
+            b[2 * m + 1] = b1 * c8[4 + m] + b0 * s8[4 + m];
+        }
+    } else if (split) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float x0 = a[e], x1 = b[e];
+            a[e] = x0 * c8[e] - x1 * s8[e];
+            b[e] = x1 * c8[e] + x0 * s8[e];
+        }
+    } else if (rot_lane) {
+        switch (half) {
+            case 1: rotate_small_neox<1>(a, c8, s8); break;
+            case 2: rotate_small_neox<2>(a, c8, s8); break;
+            case 3: rotate_small_neox<3>(a, c8, s8); break;
+            default: rotate_small_neox<4>(a, c8, s8); break;
+        }
+    }
+    xa = pack8<T>(a);
+    xb = pack8<T>(b);
+}
+
 template <class T, class P, int D, int MODE>
 __global__ void __launch_bounds__(544, 1) qknr_bulk_kernel(const __grid_constant__ BulkParams p) {
     constexpr int LPH = D / 16;
@@ -174,7 +233,7 @@ __global__ void __launch_bounds__(544, 1) qknr_bulk_kernel(const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(full + s), 1);
-            mbar_init(smem_u32(empty + s), 1);
+            mbar_init(smem_u32(empty + s), static_cast<uint32_t>(n_consumers));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -280,12 +339,15 @@ __global__ void __launch_bounds__(544, 1) qknr_bulk_kernel(const __grid_constant
         const uint4 wqa = __ldg(p.q_w + va), wqb = __ldg(p.q_w + vb);
         const uint4 wka = __ldg(p.k_w + va), wkb = __ldg(p.k_w + vb);
 
-        for (int i = cw; i < n_local; i += n_consumers) {
+        // Every consumer warp takes part in every tile, in tile order: warp cw
+        // handles passes cw, cw + NC, ... of the tile, two at a time with
+        // independent chains, then arrives on the stage's empty barrier (which
+        // counts all NC consumers). A warp waits for tile i only after it has
+        // itself seen tile i - S arrive, and tile i + S cannot arrive before
+        // this warp released tile i, so the parity it awaits is never stale.
+        for (int i = 0; i < n_local; ++i) {
             const int s = i % S;
             const uint32_t round = static_cast<uint32_t>(i / S);
-            // Stage s only ever holds this warp's tiles (the host makes the
-            // ring depth a multiple of the consumer count), so the phase seen
-            // here is never more than one round ahead of the one awaited.
             if (!mbar_wait_bounded_warp(smem_u32(full + s), round & 1u)) {
                 if (lane == 0) atomicOr(p.status + 2, kWatchdogBit);
                 break;
@@ -296,13 +358,14 @@ __global__ void __launch_bounds__(544, 1) qknr_bulk_kernel(const __grid_constant
                 const int c = static_cast<int>(tile - t * p.chunks_per_token);
                 const int h0 = c * p.heads_per_chunk;
                 const int h1 = min(H, h0 + p.heads_per_chunk);
+                const int npass = (h1 - h0 + HPW - 1) / HPW;
                 const unsigned char *st = stages + static_cast<size_t>(s) * p.stage_bytes;
                 const float *row = reinterpret_cast<const float *>(st + (h1 - h0) * 2 * D);
 
                 float c8[8], s8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) { c8[e] = 1.f; s8[e] = 0.f; }
-                if (rot_lane) {
+                if (rot_lane && cw < npass) {
                     if (MODE == kInterleaved) {
                         // R % 8 == 0 here: a vector rotates entirely or not at all
                         if (8 * va < R) {
@@ -330,68 +393,36 @@ __global__ void __launch_bounds__(544, 1) qknr_bulk_kernel(const __grid_constant
                     }
                 }
 
-                for (int hb = h0; hb < h1; hb += HPW) {
-                    const int h = hb + g;
-                    const bool ok = h < h1;
-                    const bool is_q = h < p.n_qo;
-                    uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
-                    if (ok) {
-                        const unsigned char *hp = st + (h - h0) * 2 * D;
-                        xa = lds16(hp + 16 * va);
-                        xb = lds16(hp + 16 * vb);
-                    }
-                    float a[8], b[8];
-                    unpack8<T>(xa, a);
-                    unpack8<T>(xb, b);
-                    float ss0 = 0.f, ss1 = 0.f;
+                for (int pp = cw; pp < npass; pp += 2 * n_consumers) {
+                    uint4 xa[2], xb[2];
+                    int hh[2];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        ss0 = fmaf(a[e], a[e], ss0);
-                        ss1 = fmaf(b[e], b[e], ss1);
-                    }
-                    float ss = ss0 + ss1;
-#pragma unroll
-                    for (int off = LPH / 2; off > 0; off >>= 1)
-                        ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                    const float r = rsqrtf(fmaf(ss, p.inv_d, p.eps));
-                    float wa[8], wb[8];
-                    unpack8<T>(is_q ? wqa : wka, wa);
-                    unpack8<T>(is_q ? wqb : wkb, wb);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        a[e] = a[e] * r * wa[e];
-                        b[e] = b[e] * r * wb[e];
-                    }
-                    if (MODE == kInterleaved) {
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const float a0 = a[2 * m], a1 = a[2 * m + 1];
-                            a[2 * m] = a0 * c8[m] - a1 * s8[m];
-                            a[2 * m + 1] = a1 * c8[m] + a0 * s8[m];
-                            const float b0 = b[2 * m], b1 = b[2 * m + 1];
-                            b[2 * m] = b0 * c8[4 + m] - b1 * s8[4 + m];
-                            b[2 * m + 1] = b1 * c8[4 + m] + b0 * s8[4 + m];
-                        }
-                    } else if (split) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float x0 = a[e], x1 = b[e];
-                            a[e] = x0 * c8[e] - x1 * s8[e];
-                            b[e] = x1 * c8[e] + x0 * s8[e];
-                        }
-                    } else if (rot_lane) {
-                        switch (half) {
-                            case 1: rotate_small_neox<1>(a, c8, s8); break;
-                            case 2: rotate_small_neox<2>(a, c8, s8); break;
-                            case 3: rotate_small_neox<3>(a, c8, s8); break;
-                            default: rotate_small_neox<4>(a, c8, s8); break;
+                    for (int u = 0; u < 2; ++u) {
+                        const int h = h0 + (pp + u * n_consumers) * HPW + g;
+                        hh[u] = h;
+                        xa[u] = make_uint4(0u, 0u, 0u, 0u);
+                        xb[u] = xa[u];
+                        if (h < h1) {
+                            const unsigned char *hp = st + (h - h0) * 2 * D;
+                            xa[u] = lds16(hp + 16 * va);
+                            xb[u] = lds16(hp + 16 * vb);
                         }
                     }
-                    if (ok) {
-                        char *dstp = is_q ? p.q + t * p.q_stride_b + h * p.head_stride_b
-                                          : p.k + t * p.k_stride_b + (h - p.n_qo) * p.head_stride_b;
-                        __stcs(reinterpret_cast<uint4 *>(dstp) + va, pack8<T>(a));
-                        __stcs(reinterpret_cast<uint4 *>(dstp) + vb, pack8<T>(b));
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const bool is_q = hh[u] < p.n_qo;
+                        fused_head<T, MODE, LPH>(xa[u], xb[u], is_q ? wqa : wka, is_q ? wqb : wkb, c8, s8,
+                                                 split, rot_lane, half, p.inv_d, p.eps);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int h = hh[u];
+                        if (h < h1) {
+                            char *dstp = h < p.n_qo ? p.q + t * p.q_stride_b + h * p.head_stride_b
+                                                    : p.k + t * p.k_stride_b + (h - p.n_qo) * p.head_stride_b;
+                            __stcs(reinterpret_cast<uint4 *>(dstp) + va, xa[u]);
+                            __stcs(reinterpret_cast<uint4 *>(dstp) + vb, xb[u]);
+                        }
                     }
                 }
             }
