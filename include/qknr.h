@@ -191,17 +191,20 @@ int qknr_sync(void *stream);
 #define QKNR_KERNEL_AUTO 0
 #define QKNR_KERNEL_REGISTER 1 /* loads straight into registers; every accepted shape */
 #define QKNR_KERNEL_BULK 2     /* cp.async.bulk ring in shared memory; rope_dim % 8 == 0, 16-byte aligned table */
+#define QKNR_KERNEL_ASYNC 3    /* per-warp cp.async pipeline; same requirements as QKNR_KERNEL_BULK */
 
 /* tuning keys for qknr_set_tuning / qknr_get_tuning */
 #define QKNR_TUNE_RESET 0       /* qknr_set_tuning(QKNR_TUNE_RESET, 0): every key back to automatic */
-#define QKNR_TUNE_KERNEL 1      /* 0 auto (the register kernel), 1 register, 2 bulk */
+#define QKNR_TUNE_KERNEL 1      /* 0 auto (the register kernel), 1 register, 2 bulk, 3 async */
 #define QKNR_TUNE_PASSES 2      /* register kernel: warp passes per item, 1..4 (0 auto = 4) */
-#define QKNR_TUNE_THREADS 3     /* register kernel: threads per CTA, 64/128/256/512 (0 auto = 256) */
+#define QKNR_TUNE_THREADS 3     /* register / async kernel: threads per CTA, 64/128/256/512 (0 auto =
+                                   256; the async kernel takes at most 256) */
 #define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy; bulk: 1) */
 #define QKNR_TUNE_PDL 5         /* programmatic dependent launch: -1 auto (on), 0 off, 1 on */
 #define QKNR_TUNE_CONSUMERS 6   /* bulk kernel: consumer warps per CTA, 1..16 (0 auto: one per warp
                                    pass of a tile, 4..16) */
-#define QKNR_TUNE_STAGES 7      /* bulk kernel: ring depth, 1..32 (0 auto: what fits) */
+#define QKNR_TUNE_STAGES 7      /* bulk kernel: ring depth, 1..32; async kernel: per-warp ring depth,
+                                   2..8 (0 auto: what fits) */
 #define QKNR_TUNE_TILE_BYTES 8  /* bulk kernel: max bytes of heads per tile (0 auto = 24576) */
 
 /*
@@ -221,7 +224,7 @@ int qknr_get_tuning(int key, int *value);
  *  0 kernel (QKNR_KERNEL_REGISTER / QKNR_KERNEL_BULK)  1 grid CTAs  2 threads per CTA
  *  3 work items (warp items / tiles)  4 items per token  5 resident CTAs per SM
  *  6 PDL on  7 passes per token (register) / heads per tile (bulk)
- *  8 unroll class (register) / ring stages (bulk)  9 consumer warps (bulk)
+ *  8 unroll class (register) / ring stages (bulk, async)  9 consumer warps (bulk)
  * 10 dynamic shared memory bytes  11 bytes per ring stage
  */
 int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,

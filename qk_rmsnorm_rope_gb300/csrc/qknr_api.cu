@@ -11,9 +11,12 @@
 //   bulk kernel      qknr_bulk_kernel   (qknr_bulk_kernel.cuh): cp.async.bulk
 //                    copies into a shared-memory ring; needs rope_dim % 8 == 0
 //                    and a 16-byte aligned cos|sin table.
+//   async kernel     qknr_async_kernel  (qknr_async_kernel.cuh): a per-warp
+//                    cp.async pipeline; same requirements as the bulk kernel.
 // The automatic choice is the register kernel (measured faster on GB300 so far);
 // the bulk kernel runs when QKNR_TUNE_KERNEL asks for it.
 #include "../../include/qknr.h"
+#include "qknr_async_kernel.cuh"
 #include "qknr_bulk_kernel.cuh"
 #include "qknr_dispatch.h"
 #include "qknr_kernel.cuh"
@@ -69,9 +72,9 @@ std::once_flag g_env_once;
 int tune_check(int key, int value) {
     switch (key) {
         case QKNR_TUNE_KERNEL:
-            return (value >= 0 && value <= 2)
+            return (value >= 0 && value <= 3)
                        ? QKNR_OK
-                       : fail(QKNR_ERR_INVALID_ARG, "kernel must be 0 (auto), 1 (register) or 2 (bulk)");
+                       : fail(QKNR_ERR_INVALID_ARG, "kernel must be 0 (auto), 1 (register), 2 (bulk) or 3 (async)");
         case QKNR_TUNE_PASSES:
             return (value >= 0 && value <= qknr::kUnrollClass[qknr::kNumUnroll - 1])
                        ? QKNR_OK
@@ -149,6 +152,8 @@ struct DeviceState {
     std::atomic<bool> bulk_attr[2][2][qknr::kNumHeadDim][2];
     // resident CTAs per SM of the unfused-baseline kernels, by (dtype, op-1, pos64, d_idx, mode)
     std::atomic<int> unfused_occ[2][2][2][qknr::kNumHeadDim][2];
+    // async kernels whose dynamic shared-memory limit was raised, by (dtype, pos64, d_idx, mode)
+    std::atomic<bool> async_attr[2][2][qknr::kNumHeadDim][2];
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -318,16 +323,74 @@ int plan_bulk(DeviceState &st, const Call &c, WorkMap *wm) {
     return QKNR_OK;
 }
 
+// Async kernel: warps stream (token, pass) units through a private ring of S
+// stages (pass data 1 KB + cos|sin row + flag). S and the CTAs per SM are
+// chosen so that the rings of all resident warps fit the SM's shared memory.
+int plan_async(DeviceState &st, const Call &c, WorkMap *wm) {
+    const int d_idx = head_dim_index(c.head_dim);
+    const int hpw = qknr::kWarp / (c.head_dim / 16);
+    wm->kind = QKNR_KERNEL_ASYNC;
+    wm->passes_per_token = (c.n_qo + c.n_kv + hpw - 1) / hpw;
+    wm->chunks_per_token = wm->passes_per_token;
+    wm->items = c.num_tokens * wm->passes_per_token;
+    wm->stage_bytes = 1024 + 4 * c.rope_dim + 16;
+    int threads = tune(QKNR_TUNE_THREADS);
+    if (threads_index(threads) < 0 || threads > 256) threads = 256;
+    wm->threads = threads;
+    const int warps = threads / qknr::kWarp;
+
+    const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
+    const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
+    const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
+    wm->kernel = dt ? qknr::async_kernel_fp16(pos64, d_idx, mode) : qknr::async_kernel_bf16(pos64, d_idx, mode);
+    if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no async kernel for this shape");
+    std::atomic<bool> &attr = st.async_attr[dt][pos64][d_idx][mode];
+    if (!attr.load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(wm->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxBulkSmem);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        attr.store(true, std::memory_order_release);
+    }
+    // CTAs per SM allowed by registers alone
+    int occ_regs = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_regs, wm->kernel, threads, 0);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(async)");
+    if (occ_regs <= 0) return fail(QKNR_ERR_CUDA, "async kernel cannot be resident with %d threads", threads);
+    const int force = tune(QKNR_TUNE_CTAS_PER_SM);
+    int ctas = force > 0 ? std::min(force, occ_regs) : occ_regs;
+    int stages = tune(QKNR_TUNE_STAGES);
+    const int per_sm = 228 * 1024 - 4096;
+    for (;;) {
+        const int fit = per_sm / ctas / (warps * wm->stage_bytes);
+        int s = stages > 0 ? std::min(stages, fit) : fit;
+        s = std::min(s, qknr::kAsyncMaxStages);
+        if (s >= 2 || ctas == 1) {
+            wm->stages = std::max(1, s);
+            break;
+        }
+        --ctas;
+    }
+    if (wm->stages < 2) return fail(QKNR_ERR_UNSUPPORTED, "async kernel: a %d-byte stage does not fit twice", wm->stage_bytes);
+    wm->smem_bytes = warps * wm->stages * wm->stage_bytes;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wm->kernel, threads, wm->smem_bytes);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(async)");
+    if (occ <= 0) return fail(QKNR_ERR_CUDA, "async kernel cannot be resident (%d bytes of shared memory)", wm->smem_bytes);
+    wm->ctas_per_sm = std::min(occ, ctas);
+    const long long needed = (wm->items + warps - 1) / warps;
+    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(wm->ctas_per_sm) * st.sm_count)));
+    return QKNR_OK;
+}
+
 int plan(DeviceState &st, const Call &c, WorkMap *wm) {
     const int kind = tune(QKNR_TUNE_KERNEL);
     int rc;
-    if (kind != QKNR_KERNEL_BULK) {
-        rc = plan_register(st, c, wm);
-    } else {
+    if (kind == QKNR_KERNEL_BULK || kind == QKNR_KERNEL_ASYNC) {
         if (!bulk_applies(c))
             return fail(QKNR_ERR_UNSUPPORTED,
-                        "the bulk kernel needs rope_dim %% 8 == 0 and a 16-byte aligned cos|sin table");
-        rc = plan_bulk(st, c, wm);
+                        "the bulk and async kernels need rope_dim %% 8 == 0 and a 16-byte aligned cos|sin table");
+        rc = kind == QKNR_KERNEL_BULK ? plan_bulk(st, c, wm) : plan_async(st, c, wm);
+    } else {
+        rc = plan_register(st, c, wm);
     }
     if (rc) return rc;
     const int pdl = tune(QKNR_TUNE_PDL);
@@ -444,7 +507,33 @@ int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStr
     cfg.attrs = attr;
     cfg.numAttrs = wm.pdl ? 1 : 0;
     cudaError_t e;
-    if (wm.kind == QKNR_KERNEL_BULK) {
+    if (wm.kind == QKNR_KERNEL_ASYNC) {
+        qknr::AsyncParams prm = {};
+        prm.q = static_cast<char *>(c.q);
+        prm.k = static_cast<char *>(c.k);
+        prm.q_w = static_cast<const uint4 *>(c.q_w);
+        prm.k_w = static_cast<const uint4 *>(c.k_w);
+        prm.cache = c.cache;
+        prm.positions = c.positions;
+        prm.status = status;
+        prm.q_stride_b = c.q_stride * 2;
+        prm.k_stride_b = c.k_stride * 2;
+        prm.head_stride_b = c.head_stride * 2;
+        prm.num_tokens = c.num_tokens;
+        prm.num_passes = wm.items;
+        prm.cache_len = c.cache_len;
+        prm.n_qo = c.n_qo;
+        prm.n_kv = c.n_kv;
+        prm.rope_dim = c.rope_dim;
+        prm.passes_per_token = wm.passes_per_token;
+        prm.stages = wm.stages;
+        prm.stage_bytes = wm.stage_bytes;
+        prm.eps = c.eps;
+        prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
+        cfg.dynamicSmemBytes = static_cast<size_t>(wm.smem_bytes);
+        void *args[] = {&prm};
+        e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
+    } else if (wm.kind == QKNR_KERNEL_BULK) {
         BulkParams prm = {};
         prm.q = static_cast<char *>(c.q);
         prm.k = static_cast<char *>(c.k);
@@ -823,7 +912,7 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     out[5] = wm.ctas_per_sm;
     out[6] = wm.pdl;
     out[7] = wm.kind == QKNR_KERNEL_BULK ? wm.heads_per_chunk : wm.passes_per_token;
-    out[8] = wm.kind == QKNR_KERNEL_BULK ? wm.stages : qknr::kUnrollClass[wm.u_idx];
+    out[8] = wm.kind == QKNR_KERNEL_REGISTER ? qknr::kUnrollClass[wm.u_idx] : wm.stages;
     out[9] = wm.kind == QKNR_KERNEL_BULK ? wm.consumers : 0;
     out[10] = wm.smem_bytes;
     out[11] = wm.stage_bytes;

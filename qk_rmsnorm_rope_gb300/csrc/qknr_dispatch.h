@@ -20,6 +20,10 @@ const void *kernel_fp16(int pos64, int d_idx, int mode, int u_idx);
 const void *bulk_kernel_bf16(int pos64, int d_idx, int mode);
 const void *bulk_kernel_fp16(int pos64, int d_idx, int mode);
 
+// Per-warp cp.async pipeline kernel entry for (position type, head_dim class, mode).
+const void *async_kernel_bf16(int pos64, int d_idx, int mode);
+const void *async_kernel_fp16(int pos64, int d_idx, int mode);
+
 // One step of the unfused two-kernel baseline (op = kOpNorm or kOpRope), the
 // register kernel with 4 passes per item. Norm-only ignores pos64 and mode.
 const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode);

@@ -1,5 +1,6 @@
 // qknr_inst_bf16.cu -- explicit instantiations of the fused kernels (register and bulk-copy ring) for bf16 storage.
 #include "qknr_dispatch.h"
+#include "qknr_async_kernel.cuh"
 #include "qknr_bulk_kernel.cuh"
 #include "qknr_kernel.cuh"
 
@@ -64,7 +65,27 @@ const void *unfused_by_op(int op, int pos64, int mode) {
                          : reinterpret_cast<const void *>(&qknr_fused_kernel<__nv_bfloat16, int, D, kInterleaved, 4, kOpRope>);
 }
 
+template <class P, int D>
+const void *async_by_mode(int mode) {
+    return mode == kNeox ? reinterpret_cast<const void *>(&qknr_async_kernel<__nv_bfloat16, P, D, kNeox>)
+                         : reinterpret_cast<const void *>(&qknr_async_kernel<__nv_bfloat16, P, D, kInterleaved>);
+}
+
+template <class P>
+const void *async_by_head_dim(int d_idx, int mode) {
+    switch (d_idx) {
+        case 0: return async_by_mode<P, 64>(mode);
+        case 1: return async_by_mode<P, 128>(mode);
+        case 2: return async_by_mode<P, 256>(mode);
+        default: return nullptr;
+    }
+}
+
 }  // namespace
+
+const void *async_kernel_bf16(int pos64, int d_idx, int mode) {
+    return pos64 ? async_by_head_dim<long long>(d_idx, mode) : async_by_head_dim<int>(d_idx, mode);
+}
 
 const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode) {
     switch (d_idx) {

@@ -143,15 +143,16 @@ def _make(D, R, neox, pos, T, n_qo, n_kv, dtype="bf16", seed=0, cache_len=300, b
                               seed=seed)
 
 
-@pytest.mark.parametrize("kernel", ["bulk", "register"])
+@pytest.mark.parametrize("kernel", ["register", "bulk", "async"])
 @pytest.mark.parametrize("D,R,neox,pos,T", GRID,
                          ids=[f"D{g[0]}-R{g[1]}-{'neox' if g[2] else 'inter'}-{g[3]}-T{g[4]}"
                               for g in GRID])
 def test_shape_grid(qknr, D, R, neox, pos, T, kernel):
-    """Both kernels over the grid; the bulk kernel applies where rope_dim % 8 == 0
-    (elsewhere that case runs the register kernel)."""
+    """Every kernel over the grid; the bulk and async kernels apply where
+    rope_dim % 8 == 0 (elsewhere that case runs the register kernel)."""
     w = _make(D, R, neox, pos, T, 4, 2, dtype="bf16" if (D + R + T) % 2 == 0 else "fp16")
-    qknr.set_tuning(reset=True, kernel=2 if (kernel == "bulk" and R % 8 == 0) else 1)
+    kind = {"register": 1, "bulk": 2, "async": 3}[kernel]
+    qknr.set_tuning(reset=True, kernel=kind if R % 8 == 0 else 1)
     try:
         _check_workload(qknr, w)
     finally:
@@ -179,6 +180,11 @@ TUNINGS = [
     dict(kernel=2, tile_bytes=1536, consumers=2, stages=4),
     dict(kernel=2, ctas_per_sm=2),
     dict(kernel=2, pdl=0, consumers=4, stages=4),
+    dict(kernel=3),
+    dict(kernel=3, stages=2),
+    dict(kernel=3, stages=3, threads=64),
+    dict(kernel=3, stages=8, threads=128, ctas_per_sm=1),
+    dict(kernel=3, pdl=0),
 ]
 
 
@@ -322,7 +328,7 @@ def test_empty_and_errors_leave_inputs_untouched(qknr):
     assert torch.equal(dev["q"], before_q) and torch.equal(dev["k"], before_k)
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_checked_variant(qknr, kernel):
     qknr.set_tuning(reset=True, kernel=kernel)
     try:
