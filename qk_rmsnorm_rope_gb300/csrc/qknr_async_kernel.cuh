@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(256, 3) qknr_async_kernel(const __grid_constan
                 xb = lds16(st + 512 + 16 * lane);
             }
             const bool is_q = h < p.n_qo;
-            fused_head<T, MODE, LPH>(xa, xb, is_q ? wqa : wka, is_q ? wqb : wkb, c8, s8, split, rot_lane,
+            qknr_head<T, MODE, LPH>(xa, xb, is_q ? wqa : wka, is_q ? wqb : wkb, c8, s8, split, rot_lane,
                                      half, p.inv_d, p.eps);
             if (h < H) {
                 char *dst = is_q ? p.q + t * p.q_stride_b + static_cast<long long>(h) * p.head_stride_b

@@ -145,64 +145,6 @@ __device__ __forceinline__ float4 lds_f4(const float *p) {
     return *reinterpret_cast<const float4 *>(p);
 }
 
-// One head slot of a warp pass: the lane's two vectors xa, xb (raw storage)
-// are replaced by the op's output (raw storage). Every lane of the warp must
-// call it (the sum of squares is reduced across the head's lanes); lanes
-// without a head pass zeros and do not store.
-template <class T, int MODE, int LPH>
-__device__ __forceinline__ void fused_head(uint4 &xa, uint4 &xb, const uint4 &wpa, const uint4 &wpb,
-                                           const float (&c8)[8], const float (&s8)[8], bool split,
-                                           bool rot_lane, int half, float inv_d, float eps) {
-    float a[8], b[8];
-    unpack8<T>(xa, a);
-    unpack8<T>(xb, b);
-    float ss0 = 0.f, ss1 = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        ss0 = fmaf(a[e], a[e], ss0);
-        ss1 = fmaf(b[e], b[e], ss1);
-    }
-    float ss = ss0 + ss1;
-#pragma unroll
-    for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float r = rsqrtf(fmaf(ss, inv_d, eps));
-    float wa[8], wb[8];
-    unpack8<T>(wpa, wa);
-    unpack8<T>(wpb, wb);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        a[e] = a[e] * r * wa[e];
-        b[e] = b[e] * r * wb[e];
-    }
-    if (MODE == kInterleaved) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float a0 = a[2 * m], a1 = a[2 * m + 1];
-            a[2 * m] = a0 * c8[m] - a1 * s8[m];
-            a[2 * m + 1] = a1 * c8[m] + a0 * s8[m];
-            const float b0 = b[2 * m], b1 = b[2 * m + 1];
-            b[2 * m] = b0 * c8[4 + m] - b1 * s8[4 + m];
-            b[2 * m + 1] = b1 * c8[4 + m] + b0 * s8[4 + m];
-        }
-    } else if (split) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float x0 = a[e], x1 = b[e];
-            a[e] = x0 * c8[e] - x1 * s8[e];
-            b[e] = x1 * c8[e] + x0 * s8[e];
-        }
-    } else if (rot_lane) {
-        switch (half) {
-            case 1: rotate_small_neox<1>(a, c8, s8); break;
-            case 2: rotate_small_neox<2>(a, c8, s8); break;
-            case 3: rotate_small_neox<3>(a, c8, s8); break;
-            default: rotate_small_neox<4>(a, c8, s8); break;
-        }
-    }
-    xa = pack8<T>(a);
-    xb = pack8<T>(b);
-}
-
 template <class T, class P, int D, int MODE>
 __global__ void __launch_bounds__(544, 1) qknr_bulk_kernel(const __grid_constant__ BulkParams p) {
     constexpr int LPH = D / 16;
@@ -411,7 +353,7 @@ __global__ void __launch_bounds__(544, 1) qknr_bulk_kernel(const __grid_constant
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const bool is_q = hh[u] < p.n_qo;
-                        fused_head<T, MODE, LPH>(xa[u], xb[u], is_q ? wqa : wka, is_q ? wqb : wkb, c8, s8,
+                        qknr_head<T, MODE, LPH>(xa[u], xb[u], is_q ? wqa : wka, is_q ? wqb : wkb, c8, s8,
                                                  split, rot_lane, half, p.inv_d, p.eps);
                     }
 #pragma unroll

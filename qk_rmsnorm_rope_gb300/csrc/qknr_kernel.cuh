@@ -30,15 +30,11 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "qknr_math.cuh"
+
 namespace qknr {
 
 constexpr int kWarp = 32;
-
-enum Mode : int { kInterleaved = 0, kNeox = 1 };
-
-// What a launch computes: the fused op, or one half of the unfused two-kernel
-// chain the fused op replaces (RMSNorm alone, then RoPE alone, each in place).
-enum Op : int { kOpFused = 0, kOpNorm = 1, kOpRope = 2 };
 
 // Kernel parameters, passed by value as a __grid_constant__.
 struct Params {
@@ -62,64 +58,6 @@ struct Params {
     float eps;
     float inv_d;                  // 1 / head_dim (exact: head_dim is a power of two)
 };
-
-template <class T>
-struct Cvt;
-
-template <>
-struct Cvt<__nv_bfloat16> {
-    // bf16 -> fp32 is exact: the 16 bits become the high half of a float.
-    static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
-    static __device__ __forceinline__ float hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-    static __device__ __forceinline__ uint32_t pack(float a, float b) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // round to nearest even; a -> low half
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-};
-
-template <>
-struct Cvt<__half> {
-    static __device__ __forceinline__ float lo(uint32_t u) {
-        return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu)));
-    }
-    static __device__ __forceinline__ float hi(uint32_t u) {
-        return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16)));
-    }
-    static __device__ __forceinline__ uint32_t pack(float a, float b) {
-        __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-};
-
-template <class T>
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
-    f[0] = Cvt<T>::lo(v.x); f[1] = Cvt<T>::hi(v.x);
-    f[2] = Cvt<T>::lo(v.y); f[3] = Cvt<T>::hi(v.y);
-    f[4] = Cvt<T>::lo(v.z); f[5] = Cvt<T>::hi(v.z);
-    f[6] = Cvt<T>::lo(v.w); f[7] = Cvt<T>::hi(v.w);
-}
-
-template <class T>
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-    uint4 v;
-    v.x = Cvt<T>::pack(f[0], f[1]);
-    v.y = Cvt<T>::pack(f[2], f[3]);
-    v.z = Cvt<T>::pack(f[4], f[5]);
-    v.w = Cvt<T>::pack(f[6], f[7]);
-    return v;
-}
-
-// NeoX with rope_dim <= 8: every rotated dim is in vector 0, pairs (e, e+HALF).
-template <int HALF>
-__device__ __forceinline__ void rotate_small_neox(float (&a)[8], const float (&c)[8],
-                                                  const float (&s)[8]) {
-#pragma unroll
-    for (int e = 0; e < HALF; ++e) {
-        const float x0 = a[e], x1 = a[e + HALF];
-        a[e] = x0 * c[e] - x1 * s[e];
-        a[e + HALF] = x1 * c[e] + x0 * s[e];
-    }
-}
 
 template <class P>
 __device__ __forceinline__ long long load_position(const void *positions, long long t) {
@@ -282,64 +220,11 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
             if (pb + u >= pe) break;    // warp-uniform
             const int h = (pb + u) * HPW + g;
             const bool is_q = h < p.n_qo;
-            float a[8], b[8];
-            unpack8<T>(xa[u], a);
-            unpack8<T>(xb[u], b);
-
-            if (OP != kOpRope) {
-                float ss0 = 0.f, ss1 = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    ss0 = fmaf(a[e], a[e], ss0);
-                    ss1 = fmaf(b[e], b[e], ss1);
-                }
-                float ss = ss0 + ss1;
-#pragma unroll
-                for (int off = LPH / 2; off > 0; off >>= 1)
-                    ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                const float r = rsqrtf(fmaf(ss, p.inv_d, p.eps));
-
-                float wa[8], wb[8];
-                unpack8<T>(is_q ? wqa : wka, wa);
-                unpack8<T>(is_q ? wqb : wkb, wb);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    a[e] = a[e] * r * wa[e];
-                    b[e] = b[e] * r * wb[e];
-                }
-            }
-
-            if (OP == kOpNorm) {
-                // no rotation in the norm-only step
-            } else if (MODE == kInterleaved) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float a0 = a[2 * m], a1 = a[2 * m + 1];
-                    a[2 * m] = a0 * c[m] - a1 * s[m];
-                    a[2 * m + 1] = a1 * c[m] + a0 * s[m];
-                    const float b0 = b[2 * m], b1 = b[2 * m + 1];
-                    b[2 * m] = b0 * c[4 + m] - b1 * s[4 + m];
-                    b[2 * m + 1] = b1 * c[4 + m] + b0 * s[4 + m];
-                }
-            } else if (split) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x0 = a[e], x1 = b[e];
-                    a[e] = x0 * c[e] - x1 * s[e];
-                    b[e] = x1 * c[e] + x0 * s[e];
-                }
-            } else if (rot_lane) {
-                switch (half) {
-                    case 1: rotate_small_neox<1>(a, c, s); break;
-                    case 2: rotate_small_neox<2>(a, c, s); break;
-                    case 3: rotate_small_neox<3>(a, c, s); break;
-                    default: rotate_small_neox<4>(a, c, s); break;
-                }
-            }
-
+            qknr_head<T, MODE, LPH, OP>(xa[u], xb[u], is_q ? wqa : wka, is_q ? wqb : wkb, c, s, split,
+                                        rot_lane, half, p.inv_d, p.eps);
             if (dst[u] != nullptr) {
-                __stcs(reinterpret_cast<uint4 *>(dst[u]) + va, pack8<T>(a));
-                __stcs(reinterpret_cast<uint4 *>(dst[u]) + vb, pack8<T>(b));
+                __stcs(reinterpret_cast<uint4 *>(dst[u]) + va, xa[u]);
+                __stcs(reinterpret_cast<uint4 *>(dst[u]) + vb, xb[u]);
             }
         }
     }
