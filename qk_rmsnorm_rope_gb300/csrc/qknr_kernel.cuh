@@ -125,13 +125,48 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     float c[8], s[8];
     long long cur_t = -1;
     bool tok_ok = true;
+    const long long num_tokens = p.num_items / p.chunks_per_token;
+    // positions of tokens pos_base .. pos_base + 31, one per lane
+    long long pos_base = it_begin < it_end ? it_begin / p.chunks_per_token : 0;
+    long long my_pos = 0;
+    if (OP != kOpNorm && pos_base + lane < num_tokens)
+        my_pos = load_position<P>(p.positions, pos_base + lane);
 
     for (long long it = it_begin; it < it_end; ++it) {
         const long long t = it / p.chunks_per_token;
         const int ch = static_cast<int>(it - t * p.chunks_per_token);
+        const int pb = static_cast<int>(static_cast<long long>(ch) * p.passes_per_token / p.chunks_per_token);
+        const int pe = static_cast<int>(static_cast<long long>(ch + 1) * p.passes_per_token / p.chunks_per_token);
+
+        uint4 xa[UMAX], xb[UMAX];
+        char *dst[UMAX];
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u) {
+            const int h = (pb + u) * HPW + g;
+            const bool ok = (pb + u < pe) && (h < H);
+            char *base = (h < p.n_qo)
+                ? p.q + t * p.q_stride_b + static_cast<long long>(h) * p.head_stride_b
+                : p.k + t * p.k_stride_b + static_cast<long long>(h - p.n_qo) * p.head_stride_b;
+            dst[u] = ok ? base : nullptr;
+            if (ok) {
+                xa[u] = __ldcs(reinterpret_cast<const uint4 *>(base) + va);
+                xb[u] = __ldcs(reinterpret_cast<const uint4 *>(base) + vb);
+            } else {
+                xa[u] = make_uint4(0u, 0u, 0u, 0u);
+                xb[u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+
+        // The q/k loads above do not depend on the position; the cos/sin loads
+        // below go out while they are in flight (the position itself was
+        // read ahead, 32 tokens at a time).
         if (OP != kOpNorm && t != cur_t) {
             cur_t = t;
-            const long long pos = load_position<P>(p.positions, t);
+            if (t >= pos_base + kWarp || t < pos_base) {   // next batch of 32 positions
+                pos_base = t;
+                my_pos = (t + lane < num_tokens) ? load_position<P>(p.positions, t + lane) : 0;
+            }
+            const long long pos = __shfl_sync(0xffffffffu, my_pos, static_cast<int>(t - pos_base));
             if (p.cache_len > 0) {
                 tok_ok = pos >= 0 && pos < p.cache_len;
                 if (!tok_ok && ch == 0 && lane == 0) {
@@ -192,28 +227,6 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
             }
         }
         if (!tok_ok) continue;          // warp-uniform: t is the same for the whole warp
-
-        const int pb = static_cast<int>(static_cast<long long>(ch) * p.passes_per_token / p.chunks_per_token);
-        const int pe = static_cast<int>(static_cast<long long>(ch + 1) * p.passes_per_token / p.chunks_per_token);
-
-        uint4 xa[UMAX], xb[UMAX];
-        char *dst[UMAX];
-#pragma unroll
-        for (int u = 0; u < UMAX; ++u) {
-            const int h = (pb + u) * HPW + g;
-            const bool ok = (pb + u < pe) && (h < H);
-            char *base = (h < p.n_qo)
-                ? p.q + t * p.q_stride_b + static_cast<long long>(h) * p.head_stride_b
-                : p.k + t * p.k_stride_b + static_cast<long long>(h - p.n_qo) * p.head_stride_b;
-            dst[u] = ok ? base : nullptr;
-            if (ok) {
-                xa[u] = __ldcs(reinterpret_cast<const uint4 *>(base) + va);
-                xb[u] = __ldcs(reinterpret_cast<const uint4 *>(base) + vb);
-            } else {
-                xa[u] = make_uint4(0u, 0u, 0u, 0u);
-                xb[u] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
 
 #pragma unroll
         for (int u = 0; u < UMAX; ++u) {
