@@ -206,12 +206,14 @@ int qknr_sync(void *stream);
 #define QKNR_TUNE_STAGES 7      /* bulk kernel: ring depth, 1..32; async kernel: per-warp ring depth,
                                    2..8 (0 auto: what fits) */
 #define QKNR_TUNE_TILE_BYTES 8  /* bulk kernel: max bytes of heads per tile (0 auto = 24576) */
+#define QKNR_TUNE_ORDER 9       /* register kernel item order: 0 auto, 1 a contiguous range per warp,
+                                   2 interleaved (warp w takes items w, w + W, ...) */
 
 /*
  * Process-wide launch tuning, for benchmarks and tests; results do not depend
  * on it (every setting gives the same bits). Invalid values return
  * QKNR_ERR_INVALID_ARG and change nothing. The environment variable
- * QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=1,pdl=1,consumers=8,stages=16,tile=24576"
+ * QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=1,pdl=1,consumers=8,stages=16,tile=24576,order=2"
  * sets the same keys at first use.
  */
 int qknr_set_tuning(int key, int value);

@@ -39,7 +39,7 @@ STATUS_NAMES = {
 QKNR_KERNEL_AUTO, QKNR_KERNEL_REGISTER, QKNR_KERNEL_BULK, QKNR_KERNEL_ASYNC = 0, 1, 2, 3
 # QKNR_TUNE_* keys (include/qknr.h)
 TUNE_KEYS = {"reset": 0, "kernel": 1, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5,
-             "consumers": 6, "stages": 7, "tile_bytes": 8}
+             "consumers": 6, "stages": 7, "tile_bytes": 8, "order": 9}
 WORK_MAP_FIELDS = ["kernel", "grid", "threads", "items", "items_per_token", "ctas_per_sm", "pdl",
                    "passes_or_heads", "unroll_or_stages", "consumers", "smem_bytes", "stage_bytes"]
 

@@ -63,10 +63,10 @@ int fail_cuda(cudaError_t e, const char *what) {
 }
 
 // ------------------------------------------------------------------ tuning
-constexpr int kNumTuneKeys = 9;   // keys 1..8 (QKNR_TUNE_*); slot 0 unused
+constexpr int kNumTuneKeys = 10;  // keys 1..9 (QKNR_TUNE_*); slot 0 unused
 // the value that means "automatic" for each key
-constexpr int kTuneAuto[kNumTuneKeys] = {0, 0, 0, 0, 0, -1, 0, 0, 0};
-std::atomic<int> g_tune[kNumTuneKeys] = {{0}, {0}, {0}, {0}, {0}, {-1}, {0}, {0}, {0}};
+constexpr int kTuneAuto[kNumTuneKeys] = {0, 0, 0, 0, 0, -1, 0, 0, 0, 0};
+std::atomic<int> g_tune[kNumTuneKeys] = {{0}, {0}, {0}, {0}, {0}, {-1}, {0}, {0}, {0}, {0}};
 std::once_flag g_env_once;
 
 int tune_check(int key, int value) {
@@ -97,6 +97,10 @@ int tune_check(int key, int value) {
             return (value >= 0 && value <= kMaxStages)
                        ? QKNR_OK
                        : fail(QKNR_ERR_INVALID_ARG, "stages must be in [0, %d]", kMaxStages);
+        case QKNR_TUNE_ORDER:
+            return (value >= 0 && value <= 2)
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "order must be 0 (auto), 1 (contiguous) or 2 (interleaved)");
         case QKNR_TUNE_TILE_BYTES:
             return (value == 0 || (value >= 512 && value <= 196608))
                        ? QKNR_OK
@@ -116,7 +120,8 @@ void read_env_tuning() {
     } names[] = {{"kernel", QKNR_TUNE_KERNEL},   {"passes", QKNR_TUNE_PASSES},
                  {"threads", QKNR_TUNE_THREADS}, {"ctas", QKNR_TUNE_CTAS_PER_SM},
                  {"pdl", QKNR_TUNE_PDL},         {"consumers", QKNR_TUNE_CONSUMERS},
-                 {"stages", QKNR_TUNE_STAGES},   {"tile", QKNR_TUNE_TILE_BYTES}};
+                 {"stages", QKNR_TUNE_STAGES},   {"tile", QKNR_TUNE_TILE_BYTES},
+                 {"order", QKNR_TUNE_ORDER}};
     std::string spec(s);
     size_t pos = 0;
     while (pos < spec.size()) {
@@ -206,6 +211,7 @@ struct WorkMap {
     int chunks_per_token = 0;
     int passes_per_token = 0, max_passes = 0, u_idx = 0;  // register kernel
     int heads_per_chunk = 0, stages = 0, consumers = 0;   // bulk kernel
+    int interleave = 0;                                   // register kernel item order
     int stage_bytes = 0, smem_bytes = 0;
     const void *kernel = nullptr;
 };
@@ -258,6 +264,7 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     const long long warps_per_cta = threads / qknr::kWarp;
     const long long needed = (wm->items + warps_per_cta - 1) / warps_per_cta;
     wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(occ) * st.sm_count)));
+    wm->interleave = tune(QKNR_TUNE_ORDER) == 2 ? 1 : 0;
     return QKNR_OK;
 }
 
@@ -580,6 +587,7 @@ int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStr
         prm.chunks_per_token = wm.chunks_per_token;
         prm.passes_per_token = wm.passes_per_token;
         prm.cache_vec = (c.rope_dim % 8 == 0) && aligned(c.cache, 16);
+        prm.interleave = wm.interleave;
         prm.eps = c.eps;
         prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
         cfg.dynamicSmemBytes = 0;

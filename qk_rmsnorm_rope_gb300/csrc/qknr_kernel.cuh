@@ -55,6 +55,7 @@ struct Params {
     int chunks_per_token;         // items per token
     int passes_per_token;         // ceil((n_qo + n_kv) / heads_per_pass)
     int cache_vec;                // 1: cos/sin rows may be read as float4
+    int interleave;               // 1: warp w takes items w, w + W, ... (W warps); 0: a contiguous range
     float eps;
     float inv_d;                  // 1 / head_dim (exact: head_dim is a power of two)
 };
@@ -115,8 +116,12 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long warp_id = gtid / kWarp;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) / kWarp;
-    const long long it_begin = warp_id * p.num_items / nwarps;
-    const long long it_end = (warp_id + 1) * p.num_items / nwarps;
+    // Items of this warp: a balanced contiguous range, or every nwarps-th item
+    // (then all warps sweep the tensors together, a compact window of memory
+    // at any moment, which suits DRAM better).
+    const long long it_begin = p.interleave ? warp_id : warp_id * p.num_items / nwarps;
+    const long long it_end = p.interleave ? p.num_items : (warp_id + 1) * p.num_items / nwarps;
+    const long long it_step = p.interleave ? nwarps : 1;
 
     // cos and (sign-free) sin per owned element. Interleaved: c[m]/s[m] serve
     // pair m of vector a (m < 4) and pair m-4 of vector b (m >= 4). NeoX split:
@@ -125,14 +130,22 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     float c[8], s[8];
     long long cur_t = -1;
     bool tok_ok = true;
-    const long long num_tokens = p.num_items / p.chunks_per_token;
-    // positions of tokens pos_base .. pos_base + 31, one per lane
-    long long pos_base = it_begin < it_end ? it_begin / p.chunks_per_token : 0;
+    // Positions read ahead, 32 items at a time: lane j holds the position of
+    // the token of the batch's j-th item; jb is the current item's index in
+    // the batch.
     long long my_pos = 0;
-    if (OP != kOpNorm && pos_base + lane < num_tokens)
-        my_pos = load_position<P>(p.positions, pos_base + lane);
+    int jb = 0;
+    if (OP != kOpNorm) {
+        const long long it_j = it_begin + lane * it_step;
+        if (it_j < it_end) my_pos = load_position<P>(p.positions, it_j / p.chunks_per_token);
+    }
 
-    for (long long it = it_begin; it < it_end; ++it) {
+    for (long long it = it_begin; it < it_end; it += it_step, ++jb) {
+        if (OP != kOpNorm && jb == kWarp) {   // next batch of 32 items' positions
+            jb = 0;
+            const long long it_j = it + lane * it_step;
+            my_pos = it_j < it_end ? load_position<P>(p.positions, it_j / p.chunks_per_token) : 0;
+        }
         const long long t = it / p.chunks_per_token;
         const int ch = static_cast<int>(it - t * p.chunks_per_token);
         const int pb = static_cast<int>(static_cast<long long>(ch) * p.passes_per_token / p.chunks_per_token);
@@ -162,11 +175,7 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
         // read ahead, 32 tokens at a time).
         if (OP != kOpNorm && t != cur_t) {
             cur_t = t;
-            if (t >= pos_base + kWarp || t < pos_base) {   // next batch of 32 positions
-                pos_base = t;
-                my_pos = (t + lane < num_tokens) ? load_position<P>(p.positions, t + lane) : 0;
-            }
-            const long long pos = __shfl_sync(0xffffffffu, my_pos, static_cast<int>(t - pos_base));
+            const long long pos = __shfl_sync(0xffffffffu, my_pos, jb);
             if (p.cache_len > 0) {
                 tok_ok = pos >= 0 && pos < p.cache_len;
                 if (!tok_ok && ch == 0 && lane == 0) {
