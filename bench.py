@@ -39,7 +39,8 @@ import workloads  # noqa: E402
 METRIC = "fused QK-RMSNorm+RoPE effective HBM GB/s (% of GB300 peak) and heads/sec"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_NAMES = {"bulk": "qknr_bulk_kernel", "register": "qknr_fused_kernel"}
+KERNEL_NAMES = {"bulk": "qknr_bulk_kernel", "register": "qknr_fused_kernel",
+                "async": "qknr_async_kernel", "lean": "qknr_lean_kernel"}
 
 
 # ------------------------------------------------------------------ environment

@@ -192,10 +192,11 @@ int qknr_sync(void *stream);
 #define QKNR_KERNEL_REGISTER 1 /* loads straight into registers; every accepted shape */
 #define QKNR_KERNEL_BULK 2     /* cp.async.bulk ring in shared memory; rope_dim % 8 == 0, 16-byte aligned table */
 #define QKNR_KERNEL_ASYNC 3    /* per-warp cp.async pipeline; same requirements as QKNR_KERNEL_BULK */
+#define QKNR_KERNEL_LEAN 4     /* register kernel with weights and cos|sin row in shared memory */
 
 /* tuning keys for qknr_set_tuning / qknr_get_tuning */
 #define QKNR_TUNE_RESET 0       /* qknr_set_tuning(QKNR_TUNE_RESET, 0): every key back to automatic */
-#define QKNR_TUNE_KERNEL 1      /* 0 auto (the register kernel), 1 register, 2 bulk, 3 async */
+#define QKNR_TUNE_KERNEL 1      /* 0 auto (the register kernel), 1 register, 2 bulk, 3 async, 4 lean */
 #define QKNR_TUNE_PASSES 2      /* register kernel: warp passes per item, 1..4 (0 auto = 4) */
 #define QKNR_TUNE_THREADS 3     /* register / async kernel: threads per CTA, 64/128/256/512 (0 auto =
                                    256; the async kernel takes at most 256) */

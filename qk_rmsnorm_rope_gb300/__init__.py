@@ -36,7 +36,7 @@ STATUS_NAMES = {
     6: "QKNR_ERR_POSITION_OOB", 7: "QKNR_ERR_WATCHDOG",
 }
 
-QKNR_KERNEL_AUTO, QKNR_KERNEL_REGISTER, QKNR_KERNEL_BULK, QKNR_KERNEL_ASYNC = 0, 1, 2, 3
+QKNR_KERNEL_AUTO, QKNR_KERNEL_REGISTER, QKNR_KERNEL_BULK, QKNR_KERNEL_ASYNC, QKNR_KERNEL_LEAN = 0, 1, 2, 3, 4
 # QKNR_TUNE_* keys (include/qknr.h)
 TUNE_KEYS = {"reset": 0, "kernel": 1, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5,
              "consumers": 6, "stages": 7, "tile_bytes": 8, "order": 9}
@@ -339,5 +339,5 @@ def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int
     _check(qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox), dtype,
                                out))
     d = dict(zip(WORK_MAP_FIELDS, [int(v) for v in out]))
-    d["kernel"] = {1: "register", 2: "bulk", 3: "async"}.get(d["kernel"], d["kernel"])
+    d["kernel"] = {1: "register", 2: "bulk", 3: "async", 4: "lean"}.get(d["kernel"], d["kernel"])
     return d

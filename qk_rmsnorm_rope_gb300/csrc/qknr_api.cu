@@ -72,9 +72,10 @@ std::once_flag g_env_once;
 int tune_check(int key, int value) {
     switch (key) {
         case QKNR_TUNE_KERNEL:
-            return (value >= 0 && value <= 3)
+            return (value >= 0 && value <= 4)
                        ? QKNR_OK
-                       : fail(QKNR_ERR_INVALID_ARG, "kernel must be 0 (auto), 1 (register), 2 (bulk) or 3 (async)");
+                       : fail(QKNR_ERR_INVALID_ARG,
+                              "kernel must be 0 (auto), 1 (register), 2 (bulk), 3 (async) or 4 (lean)");
         case QKNR_TUNE_PASSES:
             return (value >= 0 && value <= qknr::kUnrollClass[qknr::kNumUnroll - 1])
                        ? QKNR_OK
@@ -159,6 +160,8 @@ struct DeviceState {
     std::atomic<int> unfused_occ[2][2][2][qknr::kNumHeadDim][2];
     // async kernels whose dynamic shared-memory limit was raised, by (dtype, pos64, d_idx, mode)
     std::atomic<bool> async_attr[2][2][qknr::kNumHeadDim][2];
+    // resident CTAs per SM of the lean kernel, by (dtype, pos64, d_idx, mode, threads class)
+    std::atomic<int> lean_occ[2][2][qknr::kNumHeadDim][2][4];
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -388,6 +391,42 @@ int plan_async(DeviceState &st, const Call &c, WorkMap *wm) {
     return QKNR_OK;
 }
 
+// Lean kernel: the register kernel's items (4 passes) with weights and the
+// cos|sin row in shared memory; at most 256 threads per CTA.
+int plan_lean(DeviceState &st, const Call &c, WorkMap *wm) {
+    const int d_idx = head_dim_index(c.head_dim);
+    const int hpw = qknr::kWarp / (c.head_dim / 16);
+    wm->kind = QKNR_KERNEL_LEAN;
+    wm->passes_per_token = (c.n_qo + c.n_kv + hpw - 1) / hpw;
+    wm->chunks_per_token = (wm->passes_per_token + 3) / 4;
+    wm->max_passes = (wm->passes_per_token + wm->chunks_per_token - 1) / wm->chunks_per_token;
+    wm->u_idx = 1;
+    wm->items = c.num_tokens * wm->chunks_per_token;
+    int threads = tune(QKNR_TUNE_THREADS);
+    if (threads_index(threads) < 0 || threads > 256) threads = 256;
+    wm->threads = threads;
+    const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
+    const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
+    const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
+    wm->kernel = dt ? qknr::lean_kernel_fp16(pos64, d_idx, mode) : qknr::lean_kernel_bf16(pos64, d_idx, mode);
+    if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no lean kernel for this shape");
+    std::atomic<int> &slot = st.lean_occ[dt][pos64][d_idx][mode][threads_index(threads)];
+    int occ = slot.load(std::memory_order_relaxed);
+    if (occ == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wm->kernel, threads, 0);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(lean)");
+        if (occ <= 0) return fail(QKNR_ERR_CUDA, "lean kernel cannot be resident with %d threads", threads);
+        slot.store(occ, std::memory_order_relaxed);
+    }
+    const int force = tune(QKNR_TUNE_CTAS_PER_SM);
+    if (force > 0) occ = std::min(occ, force);
+    wm->ctas_per_sm = occ;
+    const long long warps_per_cta = threads / qknr::kWarp;
+    const long long needed = (wm->items + warps_per_cta - 1) / warps_per_cta;
+    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(occ) * st.sm_count)));
+    return QKNR_OK;
+}
+
 int plan(DeviceState &st, const Call &c, WorkMap *wm) {
     const int kind = tune(QKNR_TUNE_KERNEL);
     int rc;
@@ -396,6 +435,8 @@ int plan(DeviceState &st, const Call &c, WorkMap *wm) {
             return fail(QKNR_ERR_UNSUPPORTED,
                         "the bulk and async kernels need rope_dim %% 8 == 0 and a 16-byte aligned cos|sin table");
         rc = kind == QKNR_KERNEL_BULK ? plan_bulk(st, c, wm) : plan_async(st, c, wm);
+    } else if (kind == QKNR_KERNEL_LEAN) {
+        rc = plan_lean(st, c, wm);
     } else {
         rc = plan_register(st, c, wm);
     }
@@ -920,7 +961,8 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     out[5] = wm.ctas_per_sm;
     out[6] = wm.pdl;
     out[7] = wm.kind == QKNR_KERNEL_BULK ? wm.heads_per_chunk : wm.passes_per_token;
-    out[8] = wm.kind == QKNR_KERNEL_REGISTER ? qknr::kUnrollClass[wm.u_idx] : wm.stages;
+    out[8] = (wm.kind == QKNR_KERNEL_REGISTER || wm.kind == QKNR_KERNEL_LEAN) ? qknr::kUnrollClass[wm.u_idx]
+                                                                            : wm.stages;
     out[9] = wm.kind == QKNR_KERNEL_BULK ? wm.consumers : 0;
     out[10] = wm.smem_bytes;
     out[11] = wm.stage_bytes;

@@ -24,6 +24,10 @@ const void *bulk_kernel_fp16(int pos64, int d_idx, int mode);
 const void *async_kernel_bf16(int pos64, int d_idx, int mode);
 const void *async_kernel_fp16(int pos64, int d_idx, int mode);
 
+// Register kernel with per-token state in shared memory, for (position type, head_dim class, mode).
+const void *lean_kernel_bf16(int pos64, int d_idx, int mode);
+const void *lean_kernel_fp16(int pos64, int d_idx, int mode);
+
 // One step of the unfused two-kernel baseline (op = kOpNorm or kOpRope), the
 // register kernel with 4 passes per item. Norm-only ignores pos64 and mode.
 const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode);

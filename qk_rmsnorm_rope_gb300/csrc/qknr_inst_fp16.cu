@@ -3,6 +3,7 @@
 #include "qknr_async_kernel.cuh"
 #include "qknr_bulk_kernel.cuh"
 #include "qknr_kernel.cuh"
+#include "qknr_lean_kernel.cuh"
 
 namespace qknr {
 namespace {
@@ -81,7 +82,27 @@ const void *async_by_head_dim(int d_idx, int mode) {
     }
 }
 
+template <class P, int D>
+const void *lean_by_mode(int mode) {
+    return mode == kNeox ? reinterpret_cast<const void *>(&qknr_lean_kernel<__half, P, D, kNeox>)
+                         : reinterpret_cast<const void *>(&qknr_lean_kernel<__half, P, D, kInterleaved>);
+}
+
+template <class P>
+const void *lean_by_head_dim(int d_idx, int mode) {
+    switch (d_idx) {
+        case 0: return lean_by_mode<P, 64>(mode);
+        case 1: return lean_by_mode<P, 128>(mode);
+        case 2: return lean_by_mode<P, 256>(mode);
+        default: return nullptr;
+    }
+}
+
 }  // namespace
+
+const void *lean_kernel_fp16(int pos64, int d_idx, int mode) {
+    return pos64 ? lean_by_head_dim<long long>(d_idx, mode) : lean_by_head_dim<int>(d_idx, mode);
+}
 
 const void *async_kernel_fp16(int pos64, int d_idx, int mode) {
     return pos64 ? async_by_head_dim<long long>(d_idx, mode) : async_by_head_dim<int>(d_idx, mode);

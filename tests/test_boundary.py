@@ -97,7 +97,7 @@ def test_can_use_rejects():
 
 def test_set_tuning_validation():
     K = qknr.TUNE_KEYS
-    bad = [(K["kernel"], 4), (K["passes"], 5), (K["threads"], 96), (K["ctas_per_sm"], -1),
+    bad = [(K["kernel"], 5), (K["passes"], 5), (K["threads"], 96), (K["ctas_per_sm"], -1),
            (K["pdl"], 2), (K["consumers"], 17), (K["stages"], 33), (K["tile_bytes"], 100), (K["order"], 3), (99, 0)]
     for key, value in bad:
         assert qknr.qknr_set_tuning(key, value) == 2, (key, value)

@@ -143,7 +143,7 @@ def _make(D, R, neox, pos, T, n_qo, n_kv, dtype="bf16", seed=0, cache_len=300, b
                               seed=seed)
 
 
-@pytest.mark.parametrize("kernel", ["register", "bulk", "async"])
+@pytest.mark.parametrize("kernel", ["register", "bulk", "async", "lean"])
 @pytest.mark.parametrize("D,R,neox,pos,T", GRID,
                          ids=[f"D{g[0]}-R{g[1]}-{'neox' if g[2] else 'inter'}-{g[3]}-T{g[4]}"
                               for g in GRID])
@@ -151,8 +151,8 @@ def test_shape_grid(qknr, D, R, neox, pos, T, kernel):
     """Every kernel over the grid; the bulk and async kernels apply where
     rope_dim % 8 == 0 (elsewhere that case runs the register kernel)."""
     w = _make(D, R, neox, pos, T, 4, 2, dtype="bf16" if (D + R + T) % 2 == 0 else "fp16")
-    kind = {"register": 1, "bulk": 2, "async": 3}[kernel]
-    qknr.set_tuning(reset=True, kernel=kind if R % 8 == 0 else 1)
+    kind = {"register": 1, "bulk": 2, "async": 3, "lean": 4}[kernel]
+    qknr.set_tuning(reset=True, kernel=kind if (R % 8 == 0 or kind in (1, 4)) else 1)
     try:
         _check_workload(qknr, w)
     finally:
@@ -188,6 +188,9 @@ TUNINGS = [
     dict(kernel=3, stages=3, threads=64),
     dict(kernel=3, stages=8, threads=128, ctas_per_sm=1),
     dict(kernel=3, pdl=0),
+    dict(kernel=4),
+    dict(kernel=4, threads=64, ctas_per_sm=2),
+    dict(kernel=4, threads=128, pdl=0),
 ]
 
 
@@ -331,7 +334,7 @@ def test_empty_and_errors_leave_inputs_untouched(qknr):
     assert torch.equal(dev["q"], before_q) and torch.equal(dev["k"], before_k)
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 def test_checked_variant(qknr, kernel):
     qknr.set_tuning(reset=True, kernel=kernel)
     try:
