@@ -140,16 +140,28 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
         if (it_j < it_end) my_pos = load_position<P>(p.positions, it_j / p.chunks_per_token);
     }
 
+    // (token, chunk) of the current item, advanced incrementally: no 64-bit
+    // division per item (each one costs dozens of instructions, and the
+    // kernel is close to instruction-issue bound)
+    const int chunks = p.chunks_per_token;
+    long long t = it_begin / chunks;
+    int ch = static_cast<int>(it_begin - t * chunks);
+    const long long step_t = it_step / chunks;
+    const int step_c = static_cast<int>(it_step - step_t * chunks);
+
     for (long long it = it_begin; it < it_end; it += it_step, ++jb) {
         if (OP != kOpNorm && jb == kWarp) {   // next batch of 32 items' positions
             jb = 0;
             const long long it_j = it + lane * it_step;
-            my_pos = it_j < it_end ? load_position<P>(p.positions, it_j / p.chunks_per_token) : 0;
+            my_pos = it_j < it_end ? load_position<P>(p.positions, it_j / chunks) : 0;
         }
-        const long long t = it / p.chunks_per_token;
-        const int ch = static_cast<int>(it - t * p.chunks_per_token);
-        const int pb = static_cast<int>(static_cast<long long>(ch) * p.passes_per_token / p.chunks_per_token);
-        const int pe = static_cast<int>(static_cast<long long>(ch + 1) * p.passes_per_token / p.chunks_per_token);
+        if (it != it_begin) {
+            t += step_t;
+            ch += step_c;
+            if (ch >= chunks) { ch -= chunks; ++t; }
+        }
+        const int pb = chunks == 1 ? 0 : (ch * p.passes_per_token) / chunks;
+        const int pe = chunks == 1 ? p.passes_per_token : ((ch + 1) * p.passes_per_token) / chunks;
 
         uint4 xa[UMAX], xb[UMAX];
         char *dst[UMAX];
