@@ -163,15 +163,17 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
         const int pb = chunks == 1 ? 0 : (ch * p.passes_per_token) / chunks;
         const int pe = chunks == 1 ? p.passes_per_token : ((ch + 1) * p.passes_per_token) / chunks;
 
+        // this token's rows; k's is shifted back by n_qo heads so that head h
+        // (q heads first, then k heads) is row + h * head_stride for both
+        char *const q_row = p.q + t * p.q_stride_b;
+        char *const k_row = p.k + t * p.k_stride_b - static_cast<long long>(p.n_qo) * p.head_stride_b;
         uint4 xa[UMAX], xb[UMAX];
         char *dst[UMAX];
 #pragma unroll
         for (int u = 0; u < UMAX; ++u) {
             const int h = (pb + u) * HPW + g;
             const bool ok = (pb + u < pe) && (h < H);
-            char *base = (h < p.n_qo)
-                ? p.q + t * p.q_stride_b + static_cast<long long>(h) * p.head_stride_b
-                : p.k + t * p.k_stride_b + static_cast<long long>(h - p.n_qo) * p.head_stride_b;
+            char *base = (h < p.n_qo ? q_row : k_row) + static_cast<long long>(h) * p.head_stride_b;
             dst[u] = ok ? base : nullptr;
             if (ok) {
                 xa[u] = __ldcs(reinterpret_cast<const uint4 *>(base) + va);
