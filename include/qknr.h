@@ -207,8 +207,8 @@ int qknr_sync(void *stream);
 #define QKNR_TUNE_STAGES 7      /* bulk kernel: ring depth, 1..32; async kernel: per-warp ring depth,
                                    2..8 (0 auto: what fits) */
 #define QKNR_TUNE_TILE_BYTES 8  /* bulk kernel: max bytes of heads per tile (0 auto = 24576) */
-#define QKNR_TUNE_ORDER 9       /* register kernel item order: 0 auto, 1 a contiguous range per warp,
-                                   2 interleaved (warp w takes items w, w + W, ...) */
+#define QKNR_TUNE_ORDER 9       /* register kernel item order: 0 auto (= 2), 1 a contiguous range per
+                                   warp, 2 interleaved (warp w takes items w, w + W, ...) */
 
 /*
  * Process-wide launch tuning, for benchmarks and tests; results do not depend

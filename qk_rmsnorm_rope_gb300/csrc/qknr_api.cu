@@ -267,7 +267,7 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     const long long warps_per_cta = threads / qknr::kWarp;
     const long long needed = (wm->items + warps_per_cta - 1) / warps_per_cta;
     wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(occ) * st.sm_count)));
-    wm->interleave = tune(QKNR_TUNE_ORDER) == 2 ? 1 : 0;
+    wm->interleave = tune(QKNR_TUNE_ORDER) == 1 ? 0 : 1;   // interleaved unless asked otherwise
     return QKNR_OK;
 }
 

@@ -116,9 +116,9 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long warp_id = gtid / kWarp;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) / kWarp;
-    // Items of this warp: a balanced contiguous range, or every nwarps-th item
-    // (then all warps sweep the tensors together, a compact window of memory
-    // at any moment, which suits DRAM better).
+    // Items of this warp: every nwarps-th item (the default: all warps sweep
+    // the tensors together, a compact window of memory at any moment, measured
+    // faster on GB300), or a balanced contiguous range.
     const long long it_begin = p.interleave ? warp_id : warp_id * p.num_items / nwarps;
     const long long it_end = p.interleave ? p.num_items : (warp_id + 1) * p.num_items / nwarps;
     const long long it_step = p.interleave ? nwarps : 1;

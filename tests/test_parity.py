@@ -172,7 +172,7 @@ TUNINGS = [
     dict(kernel=1, passes=3, threads=256, ctas_per_sm=2),
     dict(kernel=1, passes=4, threads=512),
     dict(kernel=1, passes=4, threads=64, pdl=0),
-    dict(kernel=1, order=2),
+    dict(kernel=1, order=1),
     dict(kernel=1, order=2, passes=1, threads=64, ctas_per_sm=1),
     dict(kernel=1, order=2, passes=3, threads=512),
     dict(kernel=2),
