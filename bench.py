@@ -215,6 +215,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     qk_bytes = 2 * (w.n_qo + w.n_kv) * w.num_tokens * w.head_dim
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     n_rep = max(1, math.ceil(4 * l2 / qk_bytes)) if qk_bytes < 4 * l2 else 1
+    l2_resident = n_rep > 64          # decode-sized inputs: 64 replicas, mostly in L2
+    n_rep = min(n_rep, 64)
     reps = [workloads.to_device(cpu, w, device) for _ in range(n_rep)]
     entry = "qknr_apply_unfused" if args.variant == "unfused" else "qknr_apply"
     launches_per_step = 2 if args.variant == "unfused" else 1
@@ -270,7 +272,9 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
         "data": "synthetic",
         "config": {"workload": w.name, "shape": workloads.describe(w),
                    "storage_dtype": w.dtype, "bytes_per_step": algo, "heads_per_step": heads,
-                   "l2": (f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.0f} MB >= 4x L2)"
+                   "l2": (f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.1f} MB, L2-resident: "
+                          "a latency measurement)" if l2_resident else
+                          f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.0f} MB >= 4x L2)"
                           if n_rep > 1 else "inputs larger than 4x L2"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "work_map": wm},
@@ -423,6 +427,8 @@ def main(argv: Optional[List[str]] = None) -> int:
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload with this many tokens instead (e.g. 1 for decode latency)")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
                     help="unfused: time the two-kernel RMSNorm-then-RoPE chain instead")
     args = ap.parse_args(argv)
@@ -432,6 +438,8 @@ def main(argv: Optional[List[str]] = None) -> int:
     if world != args.gpus and world > 1:
         print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
     w = workloads.get(args.workload)
+    if args.tokens > 0:
+        w = workloads.scaled(w, args.tokens)
     if args.impl == "reference":
         line = run_reference(args, w, rank, world)
     else:

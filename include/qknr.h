@@ -82,7 +82,8 @@ int qknr_version(void);
 /*
  * Shape gate, the counterpart of the deep-dive's can_use check (§5.2) for
  * this library's own kernels. Returns 1 if (head_dim, rope_dim, is_neox,
- * dtype) is in the accepted set, else 0. Accepted: head_dim in {64, 128, 256};
+ * dtype) is in the accepted set, else 0. Accepted: head_dim in {64, 96, 128,
+ * 192, 256} (96 and 192 with the register kernel only);
  * rope_dim even with 0 < rope_dim <= head_dim; interleaved pairing takes
  * every such rope_dim; NeoX pairing takes rope_dim % 16 == 0 or rope_dim in
  * {2, 4, 6, 8}. This contains the page's set (head_dim/32 elements per lane,
@@ -197,7 +198,8 @@ int qknr_sync(void *stream);
 /* tuning keys for qknr_set_tuning / qknr_get_tuning */
 #define QKNR_TUNE_RESET 0       /* qknr_set_tuning(QKNR_TUNE_RESET, 0): every key back to automatic */
 #define QKNR_TUNE_KERNEL 1      /* 0 auto (the register kernel), 1 register, 2 bulk, 3 async, 4 lean */
-#define QKNR_TUNE_PASSES 2      /* register kernel: warp passes per item, 1..4 (0 auto = 4) */
+#define QKNR_TUNE_PASSES 2      /* register kernel: warp passes per item, 1..4 (0 auto: 4, or 1 when
+                                   the whole call has at most 16 warp passes per SM) */
 #define QKNR_TUNE_THREADS 3     /* register / async kernel: threads per CTA, 64/128/256/512 (0 auto =
                                    256; the async kernel takes at most 256) */
 #define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy; bulk: 1) */

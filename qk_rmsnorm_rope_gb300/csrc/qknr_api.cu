@@ -243,7 +243,12 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     wm->kind = QKNR_KERNEL_REGISTER;
     wm->passes_per_token = (heads + hpw - 1) / hpw;
     int ppi = tune(QKNR_TUNE_PASSES);
-    if (ppi <= 0) ppi = qknr::kUnrollClass[qknr::kNumUnroll - 1];
+    if (ppi <= 0) {
+        // a problem too small to give every SM several warps (decode-sized
+        // batches) spreads its passes over as many warps as it can
+        const long long passes = c.num_tokens * wm->passes_per_token;
+        ppi = passes <= 16LL * st.sm_count ? 1 : qknr::kUnrollClass[qknr::kNumUnroll - 1];
+    }
     wm->chunks_per_token = (wm->passes_per_token + ppi - 1) / ppi;
     wm->max_passes = (wm->passes_per_token + wm->chunks_per_token - 1) / wm->chunks_per_token;
     wm->u_idx = wm->max_passes <= 2 ? 0 : 1;
@@ -501,7 +506,7 @@ int validate(const Call &c) {
         return fail(QKNR_ERR_INVALID_ARG, "head counts n_qo=%d n_kv=%d must be >= 1", c.n_qo, c.n_kv);
     if (!shape_ok(c.head_dim, c.rope_dim, c.is_neox))
         return fail(QKNR_ERR_UNSUPPORTED,
-                    "unsupported head_dim=%d rope_dim=%d is_neox=%d (head_dim in {64,128,256}; rope_dim even, "
+                    "unsupported head_dim=%d rope_dim=%d is_neox=%d (head_dim in {64,96,128,192,256}; rope_dim even, "
                     "0 < rope_dim <= head_dim; NeoX needs rope_dim %% 16 == 0 or rope_dim <= 8)",
                     c.head_dim, c.rope_dim, c.is_neox);
     if (!std::isfinite(c.eps) || c.eps < 0.f) return fail(QKNR_ERR_INVALID_ARG, "eps must be a finite value >= 0");

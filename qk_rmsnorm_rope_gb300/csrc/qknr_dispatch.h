@@ -8,8 +8,8 @@ constexpr int kNumUnroll = 2;
 constexpr int kUnrollClass[kNumUnroll] = {2, 4};
 
 // head_dim classes
-constexpr int kNumHeadDim = 3;
-constexpr int kHeadDims[kNumHeadDim] = {64, 128, 256};
+constexpr int kNumHeadDim = 5;
+constexpr int kHeadDims[kNumHeadDim] = {64, 96, 128, 192, 256};  // 96 and 192: register kernel only
 
 // Kernel entry for (position type, head_dim class, mode, unroll class), or
 // nullptr. Defined in qknr_inst_bf16.cu / qknr_inst_fp16.cu.

@@ -31,8 +31,10 @@ template <class P>
 const void *by_head_dim(int d_idx, int mode, int u_idx) {
     switch (d_idx) {
         case 0: return by_mode<P, 64>(mode, u_idx);
-        case 1: return by_mode<P, 128>(mode, u_idx);
-        case 2: return by_mode<P, 256>(mode, u_idx);
+        case 1: return by_mode<P, 96>(mode, u_idx);
+        case 2: return by_mode<P, 128>(mode, u_idx);
+        case 3: return by_mode<P, 192>(mode, u_idx);
+        case 4: return by_mode<P, 256>(mode, u_idx);
         default: return nullptr;
     }
 }
@@ -45,10 +47,10 @@ const void *bulk_by_mode(int mode) {
 
 template <class P>
 const void *bulk_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {
+    switch (d_idx) {   // head_dim 96 / 192: register kernel only
         case 0: return bulk_by_mode<P, 64>(mode);
-        case 1: return bulk_by_mode<P, 128>(mode);
-        case 2: return bulk_by_mode<P, 256>(mode);
+        case 2: return bulk_by_mode<P, 128>(mode);
+        case 4: return bulk_by_mode<P, 256>(mode);
         default: return nullptr;
     }
 }
@@ -74,10 +76,10 @@ const void *async_by_mode(int mode) {
 
 template <class P>
 const void *async_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {
+    switch (d_idx) {   // head_dim 96 / 192: register kernel only
         case 0: return async_by_mode<P, 64>(mode);
-        case 1: return async_by_mode<P, 128>(mode);
-        case 2: return async_by_mode<P, 256>(mode);
+        case 2: return async_by_mode<P, 128>(mode);
+        case 4: return async_by_mode<P, 256>(mode);
         default: return nullptr;
     }
 }
@@ -90,10 +92,10 @@ const void *lean_by_mode(int mode) {
 
 template <class P>
 const void *lean_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {
+    switch (d_idx) {   // head_dim 96 / 192: register kernel only
         case 0: return lean_by_mode<P, 64>(mode);
-        case 1: return lean_by_mode<P, 128>(mode);
-        case 2: return lean_by_mode<P, 256>(mode);
+        case 2: return lean_by_mode<P, 128>(mode);
+        case 4: return lean_by_mode<P, 256>(mode);
         default: return nullptr;
     }
 }
@@ -111,8 +113,10 @@ const void *async_kernel_bf16(int pos64, int d_idx, int mode) {
 const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode) {
     switch (d_idx) {
         case 0: return unfused_by_op<64>(op, pos64, mode);
-        case 1: return unfused_by_op<128>(op, pos64, mode);
-        case 2: return unfused_by_op<256>(op, pos64, mode);
+        case 1: return unfused_by_op<96>(op, pos64, mode);
+        case 2: return unfused_by_op<128>(op, pos64, mode);
+        case 3: return unfused_by_op<192>(op, pos64, mode);
+        case 4: return unfused_by_op<256>(op, pos64, mode);
         default: return nullptr;
     }
 }

@@ -70,9 +70,13 @@ __device__ __forceinline__ long long load_position(const void *positions, long l
 // OP: fused (the product) or one step of the unfused baseline.
 template <class T, class P, int D, int MODE, int UMAX, int OP = kOpFused>
 __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__ Params p) {
-    constexpr int LPH = D / 16;         // lanes per head
+    // A head's data takes NVH lanes (two 16-byte vectors each); its lane group
+    // is LPH lanes, NVH rounded up to a power of two (head_dim 96 and 192 leave
+    // 2 and 4 lanes of the group idle: no loads, no stores, zero in the sum).
+    constexpr int NVH = D / 16;
+    constexpr int LPH = NVH <= 1 ? 1 : NVH <= 2 ? 2 : NVH <= 4 ? 4 : NVH <= 8 ? 8 : NVH <= 16 ? 16 : 32;
     constexpr int HPW = kWarp / LPH;    // heads per warp pass
-    static_assert(D % 16 == 0 && LPH >= 1 && LPH <= kWarp && (LPH & (LPH - 1)) == 0, "head_dim");
+    static_assert(D % 16 == 0 && NVH >= 1 && NVH <= kWarp, "head_dim");
 
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 900)
     // Programmatic dependent launch: do not touch memory before the previous
@@ -106,12 +110,19 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
         }
     } else {
         va = l;
-        vb = l + LPH;
+        vb = l + NVH;
         rot_lane = (MODE == kNeox) ? (l == 0) : (8 * va < R);
     }
+    const bool active = l < NVH;
+    if (!active) {
+        va = 0;
+        vb = 0;
+        rot_lane = false;
+    }
 
-    const uint4 wqa = __ldg(p.q_w + va), wqb = __ldg(p.q_w + vb);
-    const uint4 wka = __ldg(p.k_w + va), wkb = __ldg(p.k_w + vb);
+    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 wqa = active ? __ldg(p.q_w + va) : zero4, wqb = active ? __ldg(p.q_w + vb) : zero4;
+    const uint4 wka = active ? __ldg(p.k_w + va) : zero4, wkb = active ? __ldg(p.k_w + vb) : zero4;
 
     const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long warp_id = gtid / kWarp;
@@ -172,7 +183,7 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
 #pragma unroll
         for (int u = 0; u < UMAX; ++u) {
             const int h = (pb + u) * HPW + g;
-            const bool ok = (pb + u < pe) && (h < H);
+            const bool ok = (pb + u < pe) && (h < H) && active;
             char *base = (h < p.n_qo ? q_row : k_row) + static_cast<long long>(h) * p.head_stride_b;
             dst[u] = ok ? base : nullptr;
             if (ok) {

@@ -84,7 +84,9 @@ def test_can_use_contains_the_pages_set():
 
 
 def test_can_use_rejects():
-    assert qknr.qknr_can_use(96, 64, 0, 0) == 0          # head_dim outside {64,128,256}
+    assert qknr.qknr_can_use(80, 64, 0, 0) == 0          # head_dim outside {64,96,128,192,256}
+    assert qknr.qknr_can_use(96, 64, 1, 0) == 1          # head_dim 96 (register kernel)
+    assert qknr.qknr_can_use(192, 96, 1, 0) == 1
     assert qknr.qknr_can_use(128, 0, 0, 0) == 0          # rope_dim 0
     assert qknr.qknr_can_use(128, 130, 0, 0) == 0        # rope_dim > head_dim
     assert qknr.qknr_can_use(128, 63, 0, 0) == 0         # odd rope_dim

@@ -129,7 +129,7 @@ def _rope_dims(D, neox):
 
 
 GRID = [(D, R, neox, pos, T)
-        for D in (64, 128, 256)
+        for D in (64, 96, 128, 192, 256)
         for neox in (False, True)
         for R in _rope_dims(D, neox)
         for pos in ("i32", "i64")
@@ -152,7 +152,9 @@ def test_shape_grid(qknr, D, R, neox, pos, T, kernel):
     rope_dim % 8 == 0 (elsewhere that case runs the register kernel)."""
     w = _make(D, R, neox, pos, T, 4, 2, dtype="bf16" if (D + R + T) % 2 == 0 else "fp16")
     kind = {"register": 1, "bulk": 2, "async": 3, "lean": 4}[kernel]
-    qknr.set_tuning(reset=True, kernel=kind if (R % 8 == 0 or kind in (1, 4)) else 1)
+    if D in (96, 192) or (R % 8 and kind in (2, 3)):
+        kind = 1    # cases only the register kernel takes
+    qknr.set_tuning(reset=True, kernel=kind)
     try:
         _check_workload(qknr, w)
     finally:
@@ -160,7 +162,7 @@ def test_shape_grid(qknr, D, R, neox, pos, T, kernel):
 
 
 @pytest.mark.parametrize("n_qo,n_kv", [(1, 1), (8, 1), (32, 8), (5, 3), (1, 7), (64, 64)])
-@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("D", [64, 96, 128, 192, 256])
 def test_gqa_head_counts(qknr, n_qo, n_kv, D):
     w = _make(D, D // 2, True, "i64", 33, n_qo, n_kv, dtype="fp16", seed=n_qo * 100 + n_kv)
     _check_workload(qknr, w)
