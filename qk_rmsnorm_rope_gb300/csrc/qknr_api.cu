@@ -193,6 +193,14 @@ bool shape_ok(int head_dim, int rope_dim, int is_neox) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Heads one warp pass covers: a head's lane group is head_dim/16 lanes rounded
+// up to a power of two (the kernels' padding for head_dim 96 and 192).
+int heads_per_pass(int head_dim) {
+    int lph = 1;
+    while (lph < head_dim / 16) lph *= 2;
+    return qknr::kWarp / lph;
+}
+
 // ------------------------------------------------------------------ one call
 struct Call {
     void *q = nullptr, *k = nullptr;
@@ -237,8 +245,7 @@ int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u
 // largest unroll class (8 x 16-byte loads in flight per lane).
 int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     const int d_idx = head_dim_index(c.head_dim);
-    const int lph = c.head_dim / 16;
-    const int hpw = qknr::kWarp / lph;
+    const int hpw = heads_per_pass(c.head_dim);
     const int heads = c.n_qo + c.n_kv;
     wm->kind = QKNR_KERNEL_REGISTER;
     wm->passes_per_token = (heads + hpw - 1) / hpw;
@@ -303,8 +310,7 @@ int plan_bulk(DeviceState &st, const Call &c, WorkMap *wm) {
     if (fit < 1) return fail(QKNR_ERR_UNSUPPORTED, "a %d-byte tile does not fit shared memory", wm->stage_bytes);
     // all consumer warps share each tile; by default one warp per warp pass of
     // a tile (at least 4, at most 16)
-    const int passes = (wm->heads_per_chunk + (qknr::kWarp / (c.head_dim / 16)) - 1) /
-                       (qknr::kWarp / (c.head_dim / 16));
+    const int passes = (wm->heads_per_chunk + heads_per_pass(c.head_dim) - 1) / heads_per_pass(c.head_dim);
     int consumers = tune(QKNR_TUNE_CONSUMERS);
     if (consumers <= 0) consumers = std::min(16, std::max(4, passes));
     int stages = tune(QKNR_TUNE_STAGES);
@@ -343,7 +349,7 @@ int plan_bulk(DeviceState &st, const Call &c, WorkMap *wm) {
 // chosen so that the rings of all resident warps fit the SM's shared memory.
 int plan_async(DeviceState &st, const Call &c, WorkMap *wm) {
     const int d_idx = head_dim_index(c.head_dim);
-    const int hpw = qknr::kWarp / (c.head_dim / 16);
+    const int hpw = heads_per_pass(c.head_dim);
     wm->kind = QKNR_KERNEL_ASYNC;
     wm->passes_per_token = (c.n_qo + c.n_kv + hpw - 1) / hpw;
     wm->chunks_per_token = wm->passes_per_token;
@@ -400,7 +406,7 @@ int plan_async(DeviceState &st, const Call &c, WorkMap *wm) {
 // cos|sin row in shared memory; at most 256 threads per CTA.
 int plan_lean(DeviceState &st, const Call &c, WorkMap *wm) {
     const int d_idx = head_dim_index(c.head_dim);
-    const int hpw = qknr::kWarp / (c.head_dim / 16);
+    const int hpw = heads_per_pass(c.head_dim);
     wm->kind = QKNR_KERNEL_LEAN;
     wm->passes_per_token = (c.n_qo + c.n_kv + hpw - 1) / hpw;
     wm->chunks_per_token = (wm->passes_per_token + 3) / 4;
@@ -455,7 +461,7 @@ int plan(DeviceState &st, const Call &c, WorkMap *wm) {
 // per item, 256 threads) with the norm-only or rope-only instantiation.
 int plan_unfused(DeviceState &st, const Call &c, int op, WorkMap *wm) {
     const int d_idx = head_dim_index(c.head_dim);
-    const int hpw = qknr::kWarp / (c.head_dim / 16);
+    const int hpw = heads_per_pass(c.head_dim);
     wm->kind = QKNR_KERNEL_REGISTER;
     wm->passes_per_token = (c.n_qo + c.n_kv + hpw - 1) / hpw;
     wm->chunks_per_token = (wm->passes_per_token + 3) / 4;

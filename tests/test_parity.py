@@ -449,3 +449,28 @@ def test_unfused_norm_step_is_the_fused_op_at_position_zero(qknr):
                        is_neox=True, eps=w.eps)
     torch.cuda.synchronize()
     assert torch.equal(a["q"], b["q"]) and torch.equal(a["k"], b["k"])
+
+
+def test_planned_passes_cover_every_head(qknr):
+    """The host's passes per token must match the kernels' lane groups: a head
+    takes head_dim/16 lanes rounded up to a power of two, so a pass covers
+    32 / that many heads (head_dim 96 and 192 pad their groups)."""
+    for D in (64, 96, 128, 192, 256):
+        group = 1
+        while group < D // 16:
+            group *= 2
+        per_pass = 32 // group
+        for n_qo, n_kv in ((1, 1), (8, 1), (4, 2), (1, 7), (24, 24), (32, 8), (13, 5)):
+            H = n_qo + n_kv
+            for kernel in (1, 4) if D in (96, 192) else (1, 2, 3, 4):
+                if D in (96, 192) and kernel != 1:
+                    continue
+                qknr.set_tuning(reset=True, kernel=kernel)
+                try:
+                    m = qknr.work_map(33, n_qo, n_kv, D, D // 2, True, qknr.QKNR_FP16)
+                finally:
+                    qknr.set_tuning(reset=True)
+                if m["kernel"] == "bulk":
+                    continue      # tiles count heads, not passes
+                passes = m["passes_or_heads"]
+                assert (passes - 1) * per_pass < H <= passes * per_pass, (D, n_qo, n_kv, kernel, passes)
