@@ -322,7 +322,7 @@ def test_empty_and_errors_leave_inputs_untouched(qknr):
     # stride not a multiple of 8 elements
     assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 128, 64, 0, 260, 256, 128, 1e-6, 0, s) == 4
     # unsupported shapes
-    assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 96, 64, 0, 256, 256, 128, 1e-6, 0, s) == 3
+    assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 80, 64, 0, 256, 256, 128, 1e-6, 0, s) == 3
     assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 128, 24, 1, 256, 256, 128, 1e-6, 0, s) == 3
     # invalid arguments
     assert qknr.qknr_apply(qp, kp, *common, -1, 2, 2, 128, 64, 0, 256, 256, 128, 1e-6, 0, s) == 2
