@@ -82,13 +82,23 @@ def measured_peaks() -> Dict:
         return {}
 
 
-def kernel_source_hash() -> str:
+# device-code files each kernel is built from (a profile's counters stay valid
+# while these are unchanged)
+KERNEL_SOURCES = {
+    "qknr_fused_kernel": ["qknr_math.cuh", "qknr_kernel.cuh"],
+    "qknr_bulk_kernel": ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_bulk_kernel.cuh"],
+    "qknr_async_kernel": ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_bulk_kernel.cuh",
+                          "qknr_async_kernel.cuh"],
+    "qknr_lean_kernel": ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_lean_kernel.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str = "qknr_fused_kernel") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "qk_rmsnorm_rope_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
@@ -106,7 +116,7 @@ def profiled_traffic(kernel: str, workload: str) -> Optional[float]:
         if ":" in ln:
             k, v = ln.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("source_sha256") != kernel_source_hash():
+    if kernel not in KERNEL_SOURCES or fields.get("source_sha256") != kernel_source_hash(kernel):
         return None
     try:
         return float(fields["traffic_bytes_per_launch"])

@@ -87,9 +87,11 @@ def test_profiled_traffic_requires_matching_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "qk_rmsnorm_rope_gb300").symlink_to(os.path.join(ROOT, "qk_rmsnorm_rope_gb300"))
     f = prof / "qknr_bulk_kernel_dit.txt"
-    f.write_text(f"source_sha256: {bench.kernel_source_hash()}\ntraffic_bytes_per_launch: 123\n")
+    f.write_text(f"source_sha256: {bench.kernel_source_hash('qknr_bulk_kernel')}\n"
+                 "traffic_bytes_per_launch: 123\n")
     assert bench.profiled_traffic("qknr_bulk_kernel", "dit") == 123.0
     f.write_text("source_sha256: 00\ntraffic_bytes_per_launch: 123\n")
     assert bench.profiled_traffic("qknr_bulk_kernel", "dit") is None
     assert bench.profiled_traffic("qknr_bulk_kernel", "gqa") is None
     assert bench.profiled_traffic("qknr_fused_kernel", "dit") is None
+    assert bench.kernel_source_hash("qknr_fused_kernel") != bench.kernel_source_hash("qknr_bulk_kernel")
