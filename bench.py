@@ -363,7 +363,7 @@ def cpu_baseline(w, cpu, budget_s: float = 10.0) -> Dict:
     block = min(T, 512)
     done_tok, t_used = 0, 0.0
     start = 0
-    while t_used < budget_s and done_tok < 64 * T:
+    while t_used < budget_s and done_tok < 1024 * T:
         idx = torch.arange(start, start + block) % T
         sub = _sample_inputs(cpu, idx)
         t0 = time.perf_counter()
