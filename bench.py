@@ -427,6 +427,43 @@ def run_reference(args, w: workloads.Workload, rank: int, world: int) -> Optiona
     }
 
 
+def run_ceiling(args, w: workloads.Workload) -> Dict:
+    """Context line: torch's own in-place elementwise kernel (x.mul_(1)) and
+    out-of-place copy on bf16 buffers moving exactly this workload's
+    algorithmic bytes per step, rotated over >= 4x L2 like the op's inputs:
+    what a plain streaming read-modify-write reaches on this GPU."""
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    algo = workloads.algorithmic_bytes(w)
+    n = max(1, algo // 4)                       # bf16 elements: 2 B read + 2 B written each
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    reps = max(1, math.ceil(4 * l2 / (2 * n))) if 2 * n < 4 * l2 else 1
+    reps = min(reps, 64)
+    xs = [torch.zeros(n, dtype=torch.bfloat16, device=device) for _ in range(reps)]
+    ys = [torch.zeros(n, dtype=torch.bfloat16, device=device) for _ in range(reps)]
+
+    def timed(fn):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(args.steps):
+            fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / args.steps
+
+    t_inplace = timed(lambda i: xs[i % reps].mul_(1.0))
+    t_copy = timed(lambda i: ys[i % reps].copy_(xs[i % reps]))
+    return {"ceiling": "torch elementwise kernels at this workload's byte count",
+            "workload": w.name, "bytes_per_step": 4 * n, "replicas": reps,
+            "inplace_mul_gbs": round(4 * n / t_inplace / 1e9, 1),
+            "copy_gbs": round(4 * n / t_copy / 1e9, 1),
+            "steps": args.steps, "warmup": args.warmup}
+
+
 def main(argv: Optional[List[str]] = None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,6 +476,9 @@ def main(argv: Optional[List[str]] = None) -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run the workload with this many tokens instead (e.g. 1 for decode latency)")
+    ap.add_argument("--ceiling", action="store_true",
+                    help="print torch's in-place elementwise and copy throughput at this "
+                         "workload's byte count instead (context, not the op)")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
                     help="unfused: time the two-kernel RMSNorm-then-RoPE chain instead")
     args = ap.parse_args(argv)
@@ -450,7 +490,9 @@ def main(argv: Optional[List[str]] = None) -> int:
     w = workloads.get(args.workload)
     if args.tokens > 0:
         w = workloads.scaled(w, args.tokens)
-    if args.impl == "reference":
+    if args.ceiling:
+        line = run_ceiling(args, w) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, w, rank, world)
     else:
         line = run_ours(args, w, rank, world, local)
