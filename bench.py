@@ -274,7 +274,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     if args.variant == "unfused":
         kernel = "qknr_fused_kernel<..., kOpNorm> + qknr_fused_kernel<..., kOpRope>"
         wm = {"kernel": "register (norm step, rope step)"}
-    traffic = profiled_traffic(kernel, w.name) if args.variant == "fused" else None
+    full_size = w.num_tokens == workloads.get(w.name).num_tokens
+    traffic = profiled_traffic(kernel, w.name) if (args.variant == "fused" and full_size) else None
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
