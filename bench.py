@@ -308,6 +308,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
 
 
 def run_e2e(q, cpu, w, device, stream, steps: int, dist, entry: str = "qknr_apply") -> Dict:
+    if entry == "qknr_apply":
+        return run_e2e_host(q, cpu, w, device, stream, steps, dist)
     dev = workloads.to_device(cpu, w, device)
     call = PreparedCall(q, dev, w, stream.cuda_stream, entry)
     if w.fused_total_heads:
@@ -344,6 +346,65 @@ def run_e2e(q, cpu, w, device, stream, steps: int, dist, entry: str = "qknr_appl
     return {"value": round(world * algo * steps / secs / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "path": "pinned host -> qknr_apply (C ABI) -> pinned host, one stream"}
+
+
+def run_e2e_host(q, cpu, w, device, stream, steps: int, dist) -> Dict:
+    """End to end through qknr_apply_host: every step, q, k and positions start
+    in pinned host memory and the results end there. The headline runs the
+    direct mode (the kernel reads and writes the pinned buffers in place over
+    NVLink-C2C, both directions at once); the staged mode (chunked copies to
+    device buffers, overlapped with the kernels) is timed beside it. Each step
+    transforms the host q/k in place (the values stay bounded: every step
+    re-normalises them)."""
+    dev = workloads.to_device(cpu, w, device)
+    if w.fused_total_heads:
+        hb = cpu["buffer"].clone().pin_memory()
+        h_q, h_k = hb[:, :w.n_qo, :], hb[:, w.n_qo:w.n_qo + w.n_kv, :]
+    else:
+        h_q, h_k = cpu["q"].clone().pin_memory(), cpu["k"].clone().pin_memory()
+    h_pos = cpu["positions"].clone().pin_memory()
+    d_q, d_k, d_pos = dev["q"], dev["k"], dev["positions"]
+    T, n_qo, D = d_q.shape
+    n_kv = d_k.shape[1]
+    hs = d_q.stride(1) if n_qo > 1 else d_k.stride(1)
+    fn = q.lib.qknr_apply_host
+    heads_b = 2 * D * (n_qo + n_kv) * T
+    h2d = heads_b + h_pos.numel() * h_pos.element_size()
+    d2h = heads_b
+    world = dist.get_world_size() if dist is not None else 1
+    algo = workloads.algorithmic_bytes(w)
+    values = {}
+    for mode in (q.QKNR_HOST_DIRECT, q.QKNR_HOST_STAGED):
+        args = (h_q.data_ptr(), h_k.data_ptr(), dev["q_w"].data_ptr(), dev["k_w"].data_ptr(),
+                dev["cos_sin_cache"].data_ptr(), h_pos.data_ptr(), d_q.data_ptr(), d_k.data_ptr(),
+                d_pos.data_ptr(), T, n_qo, n_kv, D, w.rope_dim, int(w.is_neox), d_q.stride(0),
+                d_k.stride(0), hs, w.eps, q.dtype_code(d_q.dtype, d_pos.dtype), 0, mode,
+                stream.cuda_stream)
+
+        def step():
+            rc = fn(*args)
+            if rc != 0:
+                raise q.QknrError(rc, q.qknr_last_error())
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        barrier(dist)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            step()
+        torch.cuda.synchronize()
+        secs = time.perf_counter() - t0   # host wall clock: what the caller waits for
+        secs = max_over_ranks(dist, secs, device)
+        values[mode] = round(world * algo * steps / secs / 1e9, 2)
+    return {"value": values[q.QKNR_HOST_DIRECT], "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "path": ("pinned host q, k, positions -> qknr_apply_host (C ABI), direct mode: one kernel "
+                     "reads and writes the pinned host buffers in place over NVLink-C2C"),
+            "staged_value": values[q.QKNR_HOST_STAGED],
+            "staged_path": ("qknr_apply_host staged mode: chunked host-to-device copies, kernels and "
+                            "device-to-host copies overlapping on two copy streams and the caller's "
+                            "stream")}
 
 
 # ------------------------------------------------------------------ CPU oracle

@@ -179,6 +179,55 @@ int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_
                                int64_t k_stride, int64_t head_stride, float eps, int dtype,
                                void *stream);
 
+/* qknr_apply_host flags */
+#define QKNR_HOST_AUTO 0   /* direct when every host buffer is device-mapped, else staged */
+#define QKNR_HOST_STAGED 1 /* always copy through the device staging buffers */
+#define QKNR_HOST_DIRECT 2 /* always direct; QKNR_ERR_INVALID_ARG if a buffer is not device-mapped */
+
+/*
+ * The op on q, k and positions held in HOST memory, for callers whose
+ * activations live on the host (offload, or a host-side pipeline): the
+ * results are written back into h_q and h_k. Same operation and results as
+ * qknr_apply (deep-dive §3 contract); the host transfer is this library's
+ * addition.
+ *
+ * h_q, h_k, h_positions: host buffers, laid out by the same sizes and strides
+ *   as for qknr_apply. Only the heads' bytes are read and written: bytes
+ *   between heads and between rows (the V part of a fused QKV buffer) are
+ *   left as they are.
+ * q_w, k_w, cos_sin_cache: device memory, as for qknr_apply.
+ * d_q, d_k, d_positions: caller-owned device buffers with the same layout,
+ *   used only by the staged mode (may be NULL when the call runs direct).
+ *
+ * Direct mode: when the host buffers are pinned memory mapped into the
+ * device's address space (cudaHostAlloc, cudaHostRegister, torch's
+ * pin_memory on a unified-addressing system) or managed memory, checked with
+ * cudaPointerGetAttributes at both ends of each buffer, one kernel reads and
+ * writes them in place over the host link (NVLink-C2C on GB300), both
+ * directions at once.
+ * Staged mode: the tokens are cut into chunks of chunk_tokens (0: automatic,
+ *   up to 8 chunks of at least 4 MB); chunk i is copied into the staging
+ *   buffers, transformed there and copied back, and the copies of one chunk
+ *   overlap the kernel and the copies of its neighbours (two library streams,
+ *   made by the first staged call on a device, plus `stream`). Pageable host
+ *   memory works here (the copies then go through the driver's staging).
+ * flags: QKNR_HOST_AUTO, QKNR_HOST_STAGED or QKNR_HOST_DIRECT.
+ *
+ * Asynchronous like qknr_apply: the work is ordered after everything
+ * enqueued on `stream` before the call, and everything enqueued on `stream`
+ * after it waits for the last result to reach the host. Synchronise `stream`
+ * before reading h_q and h_k. Staged calls on one device are serialised on
+ * the host (they share the library streams). Errors as qknr_apply, plus
+ * QKNR_ERR_INVALID_ARG for a null host pointer, chunk_tokens < 0, an unknown
+ * flag, or QKNR_HOST_DIRECT with a buffer the device cannot address.
+ */
+int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
+                    const float *cos_sin_cache, const void *h_positions, void *d_q, void *d_k,
+                    void *d_positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim,
+                    int rope_dim, int is_neox, int64_t q_stride, int64_t k_stride,
+                    int64_t head_stride, float eps, int dtype, int64_t chunk_tokens, int flags,
+                    void *stream);
+
 /*
  * Reports whether any earlier call on the current device had a kernel wait
  * run out (the bulk kernel bounds every wait at about one second; it never

@@ -17,13 +17,14 @@ import os
 from typing import Dict, Optional
 
 __all__ = [
-    "QKNR_BF16", "QKNR_FP16", "QKNR_POS_I64", "QknrError", "library_path",
+    "QKNR_BF16", "QKNR_FP16", "QKNR_POS_I64", "QKNR_HOST_AUTO", "QKNR_HOST_STAGED",
+    "QKNR_HOST_DIRECT", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
     "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-    "qknr_sync",
+    "qknr_apply_host", "qknr_sync",
     "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map", "TUNE_KEYS",
-    "init", "apply", "apply_checked", "apply_unfused", "can_use", "dtype_code", "work_map", "set_tuning",
-    "get_tuning", "sync",
+    "init", "apply", "apply_checked", "apply_unfused", "apply_host", "can_use", "dtype_code",
+    "work_map", "set_tuning", "get_tuning", "sync",
 ]
 
 QKNR_BF16 = 0x000
@@ -37,6 +38,8 @@ STATUS_NAMES = {
 }
 
 QKNR_KERNEL_AUTO, QKNR_KERNEL_REGISTER, QKNR_KERNEL_BULK, QKNR_KERNEL_ASYNC, QKNR_KERNEL_LEAN = 0, 1, 2, 3, 4
+QKNR_HOST_AUTO, QKNR_HOST_STAGED, QKNR_HOST_DIRECT = 0, 1, 2
+HOST_MODES = {"auto": QKNR_HOST_AUTO, "staged": QKNR_HOST_STAGED, "direct": QKNR_HOST_DIRECT}
 # QKNR_TUNE_* keys (include/qknr.h)
 TUNE_KEYS = {"reset": 0, "kernel": 1, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5,
              "consumers": 6, "stages": 7, "tile_bytes": 8, "order": 9}
@@ -77,6 +80,8 @@ def _load() -> ctypes.CDLL:
                                        i64, i64, i64, f32, i32, vp]
     lib.qknr_apply_checked_noalloc.argtypes = lib.qknr_apply_checked.argtypes
     lib.qknr_apply_unfused.argtypes = lib.qknr_apply.argtypes
+    lib.qknr_apply_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
+                                    i64, i64, i64, f32, i32, i64, i32, vp]
     lib.qknr_sync.argtypes = [vp]
     lib.qknr_set_tuning.argtypes = [i32, i32]
     lib.qknr_get_tuning.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
@@ -84,7 +89,7 @@ def _load() -> ctypes.CDLL:
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
                  "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-                 "qknr_sync",
+                 "qknr_apply_host", "qknr_sync",
                  "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
@@ -167,6 +172,15 @@ def qknr_apply_unfused(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_q
                                          k_stride, head_stride, eps, dtype, stream)
 
 
+def qknr_apply_host(h_q, h_k, q_w, k_w, cos_sin_cache, h_positions, d_q, d_k, d_positions,
+                    num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, q_stride, k_stride,
+                    head_stride, eps, dtype, chunk_tokens, flags, stream) -> int:
+    return _get_lib().qknr_apply_host(h_q, h_k, q_w, k_w, cos_sin_cache, h_positions, d_q, d_k,
+                                      d_positions, num_tokens, n_qo, n_kv, head_dim, rope_dim,
+                                      int(is_neox), q_stride, k_stride, head_stride, eps, dtype,
+                                      chunk_tokens, flags, stream)
+
+
 def qknr_sync(stream) -> int:
     return _get_lib().qknr_sync(stream)
 
@@ -214,7 +228,8 @@ def can_use(head_dim: int, rope_dim: int, is_neox: bool, dtype=None) -> bool:
     return bool(qknr_can_use(head_dim, rope_dim, int(is_neox), code))
 
 
-def _marshal(q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim):
+def _marshal(q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim,
+             same_device=True):
     import torch
     if q.dim() != 3 or k.dim() != 3:
         raise QknrError(2, "q and k must be [num_tokens, heads, head_dim] (reshape 4-D inputs)")
@@ -239,7 +254,8 @@ def _marshal(q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_d
         raise QknrError(2, "q, k, q_w and k_w must share one dtype")
     if q_w.shape != (D,) or k_w.shape != (D,) or not (q_w.is_contiguous() and k_w.is_contiguous()):
         raise QknrError(2, "q_w and k_w must be contiguous [head_dim]")
-    devs = {t.device for t in (q, k, q_w, k_w, cos_sin_cache, positions)}
+    devs = {t.device for t in ((q, k, q_w, k_w, cos_sin_cache, positions) if same_device
+                               else (q_w, k_w, cos_sin_cache))}
     if len(devs) != 1 or next(iter(devs)).type != "cuda":
         raise QknrError(2, "all tensors must be on one CUDA device")
     if n_qo > 1 and n_kv > 1 and q.stride(1) != k.stride(1):
@@ -304,6 +320,49 @@ def apply_unfused(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, ep
         _check(qknr_apply_unfused(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
                                   cos_sin_cache.data_ptr(), positions.data_ptr(), T, n_qo, n_kv, D,
                                   R, int(bool(is_neox)), qs, ks, hs, float(eps), code, stream))
+
+
+def apply_host(h_q, h_k, q_w, k_w, cos_sin_cache, h_positions, d_q=None, d_k=None,
+               d_positions=None, *, is_neox: bool, eps: float = 1e-6, head_dim: int = 0,
+               rope_dim: int = 0, chunk_tokens: int = 0, mode: str = "auto", stream=None) -> None:
+    """The op on host tensors h_q, h_k, h_positions, written back into h_q and
+    h_k (see qknr_apply_host). q_w, k_w and cos_sin_cache are device tensors.
+    ``mode``: "direct" (the kernel works on pinned, device-mapped host memory
+    in place), "staged" (chunked copies through the device tensors d_q, d_k,
+    d_positions of the same shapes and strides) or "auto" (direct when
+    possible). Asynchronous on ``stream`` (default: torch's current stream on
+    q_w's device): synchronise it before reading h_q and h_k."""
+    import torch
+    if mode not in HOST_MODES:
+        raise QknrError(2, f"mode must be one of {sorted(HOST_MODES)}")
+    for name, h in (("q", h_q), ("k", h_k), ("positions", h_positions)):
+        if h.device.type != "cpu":
+            raise QknrError(2, f"h_{name} must be a host (CPU) tensor")
+    staged = d_q is not None
+    if staged:
+        for name, h, d in (("q", h_q, d_q), ("k", h_k, d_k), ("positions", h_positions, d_positions)):
+            if d is None or h.shape != d.shape or h.stride() != d.stride() or h.dtype != d.dtype:
+                raise QknrError(2, f"d_{name} must match h_{name} in shape, stride and dtype")
+        shape_of = (d_q, d_k, d_positions)
+    else:
+        if mode == "staged":
+            raise QknrError(2, "mode 'staged' needs the device tensors d_q, d_k, d_positions")
+        # the layout checks of _marshal, on host stand-ins with the same geometry
+        shape_of = tuple(torch.empty_strided(h.shape, h.stride(), dtype=h.dtype, device="meta")
+                         for h in (h_q, h_k, h_positions))
+    T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(
+        *shape_of[:2], q_w, k_w, cos_sin_cache, shape_of[2], is_neox, head_dim, rope_dim,
+        same_device=staged)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_w.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    ptr = (lambda t: t.data_ptr() if t is not None else 0)
+    with torch.cuda.device(q_w.device):
+        _check(qknr_apply_host(h_q.data_ptr(), h_k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
+                               cos_sin_cache.data_ptr(), h_positions.data_ptr(), ptr(d_q), ptr(d_k),
+                               ptr(d_positions), T, n_qo, n_kv, D, R, int(bool(is_neox)), qs, ks, hs,
+                               float(eps), code, int(chunk_tokens), HOST_MODES[mode], stream))
 
 
 def set_tuning(**kw) -> None:

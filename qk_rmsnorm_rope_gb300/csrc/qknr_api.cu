@@ -31,6 +31,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <functional>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 
@@ -162,6 +163,13 @@ struct DeviceState {
     std::atomic<bool> async_attr[2][2][qknr::kNumHeadDim][2];
     // resident CTAs per SM of the lean kernel, by (dtype, pos64, d_idx, mode, threads class)
     std::atomic<int> lean_occ[2][2][qknr::kNumHeadDim][2][4];
+    // host-buffer pipeline (qknr_apply_host): a host-to-device and a
+    // device-to-host copy stream and the events that order them against the
+    // caller's stream; made by the first such call on this device
+    std::mutex host_mu;
+    bool host_ready = false;
+    cudaStream_t host_in = nullptr, host_out = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_in = nullptr, ev_kernel = nullptr, ev_out = nullptr;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -763,6 +771,200 @@ int apply_checked_noalloc_impl(const Call &c, void *stream) {
     return run_checked(slot.state, wm, c, static_cast<cudaStream_t>(stream), host_words);
 }
 
+// ---------------------------------------------------------------------------
+// Host buffers (qknr_apply_host).
+//
+// q, k and positions start and end in host memory. When the GPU can address
+// that memory (mapped pinned or managed memory), one launch works on it in
+// place: the loads and stores cross the host link, both directions at once.
+// Otherwise the buffers are staged through the caller's device buffers: the
+// tokens are cut into
+// chunks; chunk i's heads and positions go host -> device on host_in, the
+// kernel runs on the caller's stream once they have landed, and the results
+// go device -> host on host_out once the kernel is done. The two copy
+// directions and the kernels of neighbouring chunks overlap, so a call takes
+// about as long as its slower copy direction plus one chunk.
+constexpr int kHostMaxChunks = 8;                    // automatic chunking: at most this many chunks
+constexpr long long kHostMinChunkBytes = 4LL << 20;  // ... of at least this many head bytes each way
+
+void host_pipe_release(DeviceState &st) {
+    if (st.host_in) cudaStreamDestroy(st.host_in);
+    if (st.host_out) cudaStreamDestroy(st.host_out);
+    for (cudaEvent_t *ev : {&st.ev_start, &st.ev_in, &st.ev_kernel, &st.ev_out}) {
+        if (*ev) cudaEventDestroy(*ev);
+        *ev = nullptr;
+    }
+    st.host_in = st.host_out = nullptr;
+    st.host_ready = false;
+}
+
+// With st.host_mu held and the device current.
+int host_pipe_setup(DeviceState &st) {
+    if (st.host_ready) return QKNR_OK;
+    cudaError_t e = cudaStreamCreateWithFlags(&st.host_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&st.host_out, cudaStreamNonBlocking);
+    for (cudaEvent_t *ev : {&st.ev_start, &st.ev_in, &st.ev_kernel, &st.ev_out})
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        host_pipe_release(st);
+        return fail_cuda(e, "host pipeline streams and events");
+    }
+    st.host_ready = true;
+    return QKNR_OK;
+}
+
+// Copy the heads of n_tok token rows between two buffers of one layout (n
+// heads of head_dim elements, head_stride_b apart; rows stride_b apart).
+// Only head bytes move: a row's heads form one span when they are adjacent,
+// otherwise each head is copied on its own.
+cudaError_t copy_heads(char *dst, const char *src, long long n_tok, long long stride_b, int n,
+                       long long head_stride_b, int head_dim, cudaMemcpyKind kind, cudaStream_t s) {
+    const size_t head_b = 2 * static_cast<size_t>(head_dim);
+    const bool span = n == 1 || head_stride_b == static_cast<long long>(head_b);
+    const size_t width = span ? n * head_b : head_b;
+    const int pieces = span ? 1 : n;
+    for (int h = 0; h < pieces; ++h) {
+        const size_t off = static_cast<size_t>(h) * static_cast<size_t>(head_stride_b);
+        cudaError_t e;
+        if (n_tok == 1 || static_cast<size_t>(stride_b) == width)
+            e = cudaMemcpyAsync(dst + off, src + off, static_cast<size_t>(n_tok) * width, kind, s);
+        else
+            e = cudaMemcpy2DAsync(dst + off, static_cast<size_t>(stride_b), src + off, static_cast<size_t>(stride_b),
+                                  width, static_cast<size_t>(n_tok), kind, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// The device address of host memory the GPU can reach directly (mapped
+// pinned memory or managed memory), checked at both ends of its extent;
+// nullptr for anything else (pageable or device memory, or an extent that
+// leaves the allocation).
+void *device_view(const void *p, long long extent) {
+    cudaPointerAttributes a = {};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // a failed query stays the last error otherwise
+        return nullptr;
+    }
+    if ((a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeManaged) || !a.devicePointer) return nullptr;
+    if (extent > 1) {
+        cudaPointerAttributes b = {};
+        const char *last = static_cast<const char *>(p) + (extent - 1);
+        if (cudaPointerGetAttributes(&b, last) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        if (b.type != a.type || !b.devicePointer ||
+            static_cast<const char *>(b.devicePointer) - static_cast<const char *>(a.devicePointer) != extent - 1)
+            return nullptr;
+    }
+    return a.devicePointer;
+}
+
+int apply_host_impl(const Call &dc, void *h_q, void *h_k, const void *h_pos, long long chunk_tokens, int flags,
+                    void *stream) {
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    if (!h_q || !h_k || !h_pos) return fail(QKNR_ERR_INVALID_ARG, "null host pointer");
+    if (flags != QKNR_HOST_AUTO && flags != QKNR_HOST_STAGED && flags != QKNR_HOST_DIRECT)
+        return fail(QKNR_ERR_INVALID_ARG, "flags %d is not QKNR_HOST_AUTO/STAGED/DIRECT", flags);
+    if (chunk_tokens < 0) return fail(QKNR_ERR_INVALID_ARG, "chunk_tokens %lld < 0", chunk_tokens);
+    Call hc = dc;  // the host buffers: the same layout
+    hc.q = h_q;
+    hc.k = h_k;
+    hc.positions = h_pos;
+    int rc = validate(hc);
+    if (rc) return rc;
+    const long long T = dc.num_tokens;
+    const long long hs_b = dc.head_stride * 2, qs_b = dc.q_stride * 2, ks_b = dc.k_stride * 2;
+    const long long pos_b = (dc.dtype & QKNR_POS_I64) ? 8 : 4;
+    if (T == 0) return QKNR_OK;
+
+    if (flags != QKNR_HOST_STAGED) {
+        // direct: the kernel reads and writes the host buffers over the host link
+        void *vq = device_view(h_q, (T - 1) * qs_b + row_bytes(dc.n_qo, hs_b, dc.head_dim));
+        void *vk = device_view(h_k, (T - 1) * ks_b + row_bytes(dc.n_kv, hs_b, dc.head_dim));
+        void *vp = device_view(h_pos, T * pos_b);
+        if (vq && vk && vp) {
+            Call c = dc;
+            c.q = vq;
+            c.k = vk;
+            c.positions = vp;
+            rc = validate(c);
+            if (rc) return rc;
+            WorkMap wm;
+            rc = plan(*st, c, &wm);
+            if (rc) return rc;
+            return launch(wm, c, st->status, static_cast<cudaStream_t>(stream));
+        }
+        if (flags == QKNR_HOST_DIRECT)
+            return fail(QKNR_ERR_INVALID_ARG,
+                        "QKNR_HOST_DIRECT: h_q, h_k and h_positions must be mapped pinned or managed memory");
+    }
+    rc = validate(dc);  // staged: the device staging buffers
+    if (rc) return rc;
+    long long chunk = chunk_tokens;
+    if (chunk == 0) {
+        const long long tok_b = 2LL * dc.head_dim * (dc.n_qo + dc.n_kv);
+        chunk = std::max((T + kHostMaxChunks - 1) / kHostMaxChunks, (kHostMinChunkBytes + tok_b - 1) / tok_b);
+    }
+    chunk = std::min(chunk, T);
+
+    std::lock_guard<std::mutex> lock(st->host_mu);
+    rc = host_pipe_setup(*st);
+    if (rc) return rc;
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    // everything before this call on the caller's stream comes first
+    cudaError_t e = cudaEventRecord(st->ev_start, user);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st->host_in, st->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st->host_out, st->ev_start, 0);
+    if (e != cudaSuccess) return fail_cuda(e, "host pipeline start");
+
+    const char *what = nullptr;
+    for (long long t0 = 0; t0 < T && !rc && e == cudaSuccess; t0 += chunk) {
+        const long long n = std::min(chunk, T - t0);
+        char *dq = static_cast<char *>(dc.q) + t0 * qs_b, *dk = static_cast<char *>(dc.k) + t0 * ks_b;
+        char *hq = static_cast<char *>(h_q) + t0 * qs_b, *hk = static_cast<char *>(h_k) + t0 * ks_b;
+        char *dpos = static_cast<char *>(const_cast<void *>(dc.positions)) + t0 * pos_b;
+        const char *hpos = static_cast<const char *>(h_pos) + t0 * pos_b;
+        what = "host-to-device copy";
+        e = copy_heads(dq, hq, n, qs_b, dc.n_qo, hs_b, dc.head_dim, cudaMemcpyHostToDevice, st->host_in);
+        if (e == cudaSuccess)
+            e = copy_heads(dk, hk, n, ks_b, dc.n_kv, hs_b, dc.head_dim, cudaMemcpyHostToDevice, st->host_in);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dpos, hpos, static_cast<size_t>(n * pos_b), cudaMemcpyHostToDevice, st->host_in);
+        if (e == cudaSuccess) e = cudaEventRecord(st->ev_in, st->host_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(user, st->ev_in, 0);
+        if (e != cudaSuccess) break;
+        Call cc = dc;
+        cc.q = dq;
+        cc.k = dk;
+        cc.positions = dpos;
+        cc.num_tokens = n;
+        WorkMap wm;
+        rc = plan(*st, cc, &wm);
+        if (rc) break;
+        wm.pdl = 0;  // each chunk's kernel waits for its copies, not only for the kernel before it
+        rc = launch(wm, cc, st->status, user);
+        if (rc) break;
+        what = "device-to-host copy";
+        e = cudaEventRecord(st->ev_kernel, user);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st->host_out, st->ev_kernel, 0);
+        if (e == cudaSuccess)
+            e = copy_heads(hq, dq, n, qs_b, dc.n_qo, hs_b, dc.head_dim, cudaMemcpyDeviceToHost, st->host_out);
+        if (e == cudaSuccess)
+            e = copy_heads(hk, dk, n, ks_b, dc.n_kv, hs_b, dc.head_dim, cudaMemcpyDeviceToHost, st->host_out);
+    }
+    // the caller's stream continues once the last result is on the host (also
+    // after an error, so that nothing later on it overtakes what was enqueued)
+    cudaError_t e2 = cudaEventRecord(st->ev_out, st->host_out);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(user, st->ev_out, 0);
+    if (rc) return rc;
+    if (e != cudaSuccess) return fail_cuda(e, what);
+    if (e2 != cudaSuccess) return fail_cuda(e2, "host pipeline end");
+    return QKNR_OK;
+}
+
 Call make_call(void *q, void *k, const void *q_w, const void *k_w, const float *cache, long long cache_len,
                const void *positions, long long num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
                int is_neox, long long q_stride, long long k_stride, long long head_stride, float eps,
@@ -857,6 +1059,8 @@ int qknr_shutdown(void) {
             rc = fail(QKNR_ERR_CUDA, "cudaFreeHost(status) failed");
         st.status = nullptr;
         st.status_host = nullptr;
+        std::lock_guard<std::mutex> host_lock(st.host_mu);
+        host_pipe_release(st);
     }
     if (prev >= 0) cudaSetDevice(prev);
     return rc;
@@ -909,6 +1113,16 @@ int qknr_apply_unfused(void *q, void *k, const void *q_w, const void *k_w, const
     rc = launch(norm, c, st->status, s);
     if (!rc) rc = launch(rope, c, st->status, s);
     return rc;
+}
+
+int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w, const float *cos_sin_cache,
+                    const void *h_positions, void *d_q, void *d_k, void *d_positions, int64_t num_tokens,
+                    int n_qo, int n_kv, int head_dim, int rope_dim, int is_neox, int64_t q_stride,
+                    int64_t k_stride, int64_t head_stride, float eps, int dtype, int64_t chunk_tokens,
+                    int flags, void *stream) {
+    return apply_host_impl(make_call(d_q, d_k, q_w, k_w, cos_sin_cache, 0, d_positions, num_tokens, n_qo, n_kv,
+                                     head_dim, rope_dim, is_neox, q_stride, k_stride, head_stride, eps, dtype),
+                           h_q, h_k, h_positions, chunk_tokens, flags, stream);
 }
 
 int qknr_sync(void *stream) {

@@ -53,6 +53,8 @@ def test_constants_match_header():
     assert c["QKNR_BF16"] == qknr.QKNR_BF16
     assert c["QKNR_FP16"] == qknr.QKNR_FP16
     assert c["QKNR_POS_I64"] == qknr.QKNR_POS_I64
+    for name in ("QKNR_HOST_AUTO", "QKNR_HOST_STAGED", "QKNR_HOST_DIRECT"):
+        assert c[name] == getattr(qknr, name)
     for code, name in qknr.STATUS_NAMES.items():
         assert c[name] == code
 
@@ -147,7 +149,9 @@ rc2 = q.qknr_apply_checked(16, 16, 16, 16, 16, 4, 16, 1, 1, 1, 128, 128, 0, 128,
 out = (ctypes.c_int64 * 12)()
 rc3 = q.qknr_query_work_map(8, 1, 1, 128, 128, 0, 0, out)
 rc4 = q.qknr_sync(None)
-print(rc2, rc3, rc4)
+rc5 = q.qknr_apply_host(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 1e-6, 0,
+                        0, 0, None)
+print(rc2, rc3, rc4, rc5)
 """
 
 
@@ -159,4 +163,4 @@ def test_calls_before_init_are_refused():
     assert r.returncode == 0, r.stderr
     first, second = r.stdout.strip().splitlines()[-2:]
     assert first.startswith("1 ") and "qknr_init" in first
-    assert second.split() == ["1", "1", "1"]
+    assert second.split() == ["1", "1", "1", "1"]
