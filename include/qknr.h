@@ -179,6 +179,24 @@ int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_
                                int64_t k_stride, int64_t head_stride, float eps, int dtype,
                                void *stream);
 
+/*
+ * qknr_apply for q and k whose heads are laid out with different strides
+ * (for example q inside a fused QKV buffer and k in a padded cache layout):
+ * q's heads are q_head_stride elements apart, k's k_head_stride. The
+ * deep-dive's contract (§3, §4.7) has one shared head stride; this entry
+ * point lifts that restriction. Same results, bit for bit, as qknr_apply on
+ * the same values. With equal strides, or one head on a side, it is
+ * qknr_apply's single launch; otherwise two launches of the register kernel
+ * on `stream`, q's heads then k's. Arguments, ownership and errors as
+ * qknr_apply (each side's stride is checked on its own; a negative stride is
+ * QKNR_ERR_INVALID_ARG). Asynchronous on `stream`.
+ */
+int qknr_apply_strided(void *q, void *k, const void *q_w, const void *k_w,
+                       const float *cos_sin_cache, const void *positions, int64_t num_tokens,
+                       int n_qo, int n_kv, int head_dim, int rope_dim, int is_neox,
+                       int64_t q_stride, int64_t k_stride, int64_t q_head_stride,
+                       int64_t k_head_stride, float eps, int dtype, void *stream);
+
 /* qknr_apply_host flags */
 #define QKNR_HOST_AUTO 0   /* direct when every host buffer is device-mapped, else staged */
 #define QKNR_HOST_STAGED 1 /* always copy through the device staging buffers */

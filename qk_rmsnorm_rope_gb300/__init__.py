@@ -21,7 +21,7 @@ __all__ = [
     "QKNR_HOST_DIRECT", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
     "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-    "qknr_apply_host", "qknr_sync",
+    "qknr_apply_host", "qknr_apply_strided", "qknr_sync",
     "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map", "TUNE_KEYS",
     "init", "apply", "apply_checked", "apply_unfused", "apply_host", "can_use", "dtype_code",
     "work_map", "set_tuning", "get_tuning", "sync",
@@ -82,6 +82,8 @@ def _load() -> ctypes.CDLL:
     lib.qknr_apply_unfused.argtypes = lib.qknr_apply.argtypes
     lib.qknr_apply_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
                                     i64, i64, i64, f32, i32, i64, i32, vp]
+    lib.qknr_apply_strided.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
+                                       i64, i64, i64, i64, f32, i32, vp]
     lib.qknr_sync.argtypes = [vp]
     lib.qknr_set_tuning.argtypes = [i32, i32]
     lib.qknr_get_tuning.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
@@ -89,7 +91,7 @@ def _load() -> ctypes.CDLL:
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
                  "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-                 "qknr_apply_host", "qknr_sync",
+                 "qknr_apply_host", "qknr_apply_strided", "qknr_sync",
                  "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
@@ -181,6 +183,14 @@ def qknr_apply_host(h_q, h_k, q_w, k_w, cos_sin_cache, h_positions, d_q, d_k, d_
                                       chunk_tokens, flags, stream)
 
 
+def qknr_apply_strided(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_qo, n_kv,
+                       head_dim, rope_dim, is_neox, q_stride, k_stride, q_head_stride,
+                       k_head_stride, eps, dtype, stream) -> int:
+    return _get_lib().qknr_apply_strided(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens,
+                                         n_qo, n_kv, head_dim, rope_dim, int(is_neox), q_stride,
+                                         k_stride, q_head_stride, k_head_stride, eps, dtype, stream)
+
+
 def qknr_sync(stream) -> int:
     return _get_lib().qknr_sync(stream)
 
@@ -229,7 +239,7 @@ def can_use(head_dim: int, rope_dim: int, is_neox: bool, dtype=None) -> bool:
 
 
 def _marshal(q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim,
-             same_device=True):
+             same_device=True, split_strides=False):
     import torch
     if q.dim() != 3 or k.dim() != 3:
         raise QknrError(2, "q and k must be [num_tokens, heads, head_dim] (reshape 4-D inputs)")
@@ -258,32 +268,43 @@ def _marshal(q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_d
                                else (q_w, k_w, cos_sin_cache))}
     if len(devs) != 1 or next(iter(devs)).type != "cuda":
         raise QknrError(2, "all tensors must be on one CUDA device")
-    if n_qo > 1 and n_kv > 1 and q.stride(1) != k.stride(1):
+    if n_qo > 1 and n_kv > 1 and q.stride(1) != k.stride(1) and not split_strides:
         raise QknrError(2, "q and k must share one head stride")
     head_stride = q.stride(1) if n_qo > 1 else (k.stride(1) if n_kv > 1 else D)
-    return (T, n_qo, n_kv, head_dim, rope_dim, q.stride(0), k.stride(0), head_stride,
-            dtype_code(q.dtype, positions.dtype))
+    out = (T, n_qo, n_kv, head_dim, rope_dim, q.stride(0), k.stride(0), head_stride,
+           dtype_code(q.dtype, positions.dtype))
+    if split_strides:
+        return out + (k.stride(1) if n_kv > 1 else head_stride,)
+    return out
 
 
 def apply(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float = 1e-6,
           head_dim: int = 0, rope_dim: int = 0, stream=None) -> None:
     """In-place fused QK RMSNorm + RoPE on torch CUDA tensors (returns None).
 
-    q [T, n_qo, D] and k [T, n_kv, D] (bf16/fp16, unit innermost stride, one
-    shared head stride) are overwritten. Runs on ``stream`` (a torch.cuda.Stream
-    or raw handle), default torch's current stream on q's device.
+    q [T, n_qo, D] and k [T, n_kv, D] (bf16/fp16, unit innermost stride) are
+    overwritten. Runs on ``stream`` (a torch.cuda.Stream or raw handle),
+    default torch's current stream on q's device. q and k may have different
+    head strides (qknr_apply_strided); with one shared stride this is
+    qknr_apply.
     """
     import torch
-    T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(q, k, q_w, k_w, cos_sin_cache, positions,
-                                                      is_neox, head_dim, rope_dim)
+    T, n_qo, n_kv, D, R, qs, ks, hs, code, khs = _marshal(
+        q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim, split_strides=True)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif not isinstance(stream, int):
         stream = stream.cuda_stream
     with torch.cuda.device(q.device):
-        _check(qknr_apply(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
-                          cos_sin_cache.data_ptr(), positions.data_ptr(), T, n_qo, n_kv, D, R,
-                          int(bool(is_neox)), qs, ks, hs, float(eps), code, stream))
+        if khs == hs:
+            _check(qknr_apply(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
+                              cos_sin_cache.data_ptr(), positions.data_ptr(), T, n_qo, n_kv, D, R,
+                              int(bool(is_neox)), qs, ks, hs, float(eps), code, stream))
+        else:
+            _check(qknr_apply_strided(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
+                                      cos_sin_cache.data_ptr(), positions.data_ptr(), T, n_qo,
+                                      n_kv, D, R, int(bool(is_neox)), qs, ks, hs, khs,
+                                      float(eps), code, stream))
 
 
 def apply_checked(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float = 1e-6,

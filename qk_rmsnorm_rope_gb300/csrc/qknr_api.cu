@@ -219,6 +219,7 @@ struct Call {
     long long num_tokens = 0;
     int n_qo = 0, n_kv = 0, head_dim = 0, rope_dim = 0, is_neox = 0;
     long long q_stride = 0, k_stride = 0, head_stride = 0;  // elements
+    long long k_head_stride = -1;  // elements; < 0: k's heads are head_stride apart too
     float eps = 0.f;
     int dtype = 0;
 };
@@ -526,20 +527,21 @@ int validate(const Call &c) {
     if (!std::isfinite(c.eps) || c.eps < 0.f) return fail(QKNR_ERR_INVALID_ARG, "eps must be a finite value >= 0");
     if (!c.q || !c.k || !c.q_w || !c.k_w || !c.cache || !c.positions)
         return fail(QKNR_ERR_INVALID_ARG, "null pointer argument");
+    const long long k_hs = c.k_head_stride < 0 ? c.head_stride : c.k_head_stride;
     if (c.q_stride < 0 || c.k_stride < 0 || c.head_stride < 0) return fail(QKNR_ERR_INVALID_ARG, "negative stride");
-    if ((c.n_qo > 1 || c.n_kv > 1) && c.head_stride < c.head_dim)
-        return fail(QKNR_ERR_INVALID_ARG, "head_stride %lld < head_dim %d: heads overlap", c.head_stride,
-                    c.head_dim);
+    if ((c.n_qo > 1 && c.head_stride < c.head_dim) || (c.n_kv > 1 && k_hs < c.head_dim))
+        return fail(QKNR_ERR_INVALID_ARG, "head stride %lld < head_dim %d: heads overlap",
+                    c.n_qo > 1 && c.head_stride < c.head_dim ? c.head_stride : k_hs, c.head_dim);
     if (!aligned(c.q, 16) || !aligned(c.k, 16) || !aligned(c.q_w, 16) || !aligned(c.k_w, 16))
         return fail(QKNR_ERR_MISALIGNED, "q, k, q_w and k_w must be 16-byte aligned");
-    if ((c.q_stride % 8) || (c.k_stride % 8) || (c.head_stride % 8))
-        return fail(QKNR_ERR_MISALIGNED, "q_stride, k_stride and head_stride must be multiples of 8 elements");
+    if ((c.q_stride % 8) || (c.k_stride % 8) || (c.head_stride % 8) || (k_hs % 8))
+        return fail(QKNR_ERR_MISALIGNED, "q_stride, k_stride and head strides must be multiples of 8 elements");
     if (!aligned(c.cache, 4)) return fail(QKNR_ERR_MISALIGNED, "cos_sin_cache must be 4-byte aligned");
     if (!aligned(c.positions, (dtype & QKNR_POS_I64) ? 8 : 4))
         return fail(QKNR_ERR_MISALIGNED, "positions must be aligned to their element size");
 
     const long long hs_b = c.head_stride * 2, qs_b = c.q_stride * 2, ks_b = c.k_stride * 2;
-    const long long q_row = row_bytes(c.n_qo, hs_b, c.head_dim), k_row = row_bytes(c.n_kv, hs_b, c.head_dim);
+    const long long q_row = row_bytes(c.n_qo, hs_b, c.head_dim), k_row = row_bytes(c.n_kv, k_hs * 2, c.head_dim);
     if (c.num_tokens > 1 && (qs_b < q_row || ks_b < k_row))
         return fail(QKNR_ERR_INVALID_ARG, "token stride smaller than one token's heads: rows overlap");
     if (c.num_tokens > 0) {
@@ -965,6 +967,46 @@ int apply_host_impl(const Call &dc, void *h_q, void *h_k, const void *h_pos, lon
     return QKNR_OK;
 }
 
+// q and k with their own head strides. With one stride (or one head on a
+// side, whose stride does not matter) this is qknr_apply's single launch.
+// Otherwise the register kernel runs twice on the stream: over the q heads
+// alone, then over the k heads alone, each with its own stride; the per-head
+// arithmetic is the same, so are the bits.
+int apply_strided_impl(const Call &c, void *stream) {
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    if (c.k_head_stride < 0) return fail(QKNR_ERR_INVALID_ARG, "negative stride");
+    int rc = validate(c);
+    if (rc) return rc;
+    if (c.num_tokens == 0) return QKNR_OK;
+    Call one = c;
+    if (c.n_kv == 1 || c.k_head_stride == c.head_stride) {
+        one.k_head_stride = -1;
+        return apply_impl(one, stream, false);
+    }
+    if (c.n_qo == 1) {
+        one.head_stride = c.k_head_stride;
+        one.k_head_stride = -1;
+        return apply_impl(one, stream, false);
+    }
+    Call sides[2] = {c, c};
+    sides[0].n_kv = 0;                          // q heads, head_stride apart
+    sides[0].k_head_stride = -1;
+    sides[1].n_qo = 0;                          // k heads, k_head_stride apart
+    sides[1].head_stride = c.k_head_stride;
+    sides[1].k_head_stride = -1;
+    const int pdl = tune(QKNR_TUNE_PDL);
+    for (const Call &side : sides) {
+        WorkMap wm;
+        rc = plan_register(*st, side, &wm);
+        if (rc) return rc;
+        wm.pdl = pdl < 0 ? 1 : pdl;
+        rc = launch(wm, side, st->status, static_cast<cudaStream_t>(stream));
+        if (rc) return rc;
+    }
+    return QKNR_OK;
+}
+
 Call make_call(void *q, void *k, const void *q_w, const void *k_w, const float *cache, long long cache_len,
                const void *positions, long long num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
                int is_neox, long long q_stride, long long k_stride, long long head_stride, float eps,
@@ -1123,6 +1165,16 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w, cons
     return apply_host_impl(make_call(d_q, d_k, q_w, k_w, cos_sin_cache, 0, d_positions, num_tokens, n_qo, n_kv,
                                      head_dim, rope_dim, is_neox, q_stride, k_stride, head_stride, eps, dtype),
                            h_q, h_k, h_positions, chunk_tokens, flags, stream);
+}
+
+int qknr_apply_strided(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
+                       const void *positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
+                       int is_neox, int64_t q_stride, int64_t k_stride, int64_t q_head_stride,
+                       int64_t k_head_stride, float eps, int dtype, void *stream) {
+    Call c = make_call(q, k, q_w, k_w, cos_sin_cache, 0, positions, num_tokens, n_qo, n_kv, head_dim, rope_dim,
+                       is_neox, q_stride, k_stride, q_head_stride, eps, dtype);
+    c.k_head_stride = k_head_stride;
+    return apply_strided_impl(c, stream);
 }
 
 int qknr_sync(void *stream) {

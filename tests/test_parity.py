@@ -278,6 +278,64 @@ def test_separate_strides_and_padded_heads(qknr):
     assert torch.equal(dk_big.cpu().view(torch.int16)[mk], kbig.view(torch.int16)[mk])
 
 
+STRIDED = [(6, 2, 0, 32, 128, True), (4, 4, 64, 0, 64, False), (1, 3, 0, 16, 256, False),
+           (3, 1, 8, 0, 96, True), (5, 3, 8, 24, 192, False), (24, 24, 0, 128, 128, False)]
+
+
+@pytest.mark.parametrize("n_qo,n_kv,q_pad,k_pad,D,neox", STRIDED,
+                         ids=[f"q{c[0]}+{c[2]}-k{c[1]}+{c[3]}-D{c[4]}" for c in STRIDED])
+def test_independent_head_strides(qknr, n_qo, n_kv, q_pad, k_pad, D, neox):
+    """q and k heads with their own strides (qknr_apply_strided, through the
+    raw entry point and through apply()): the same bits as qknr_apply on
+    contiguous copies, within the oracle's tolerance, padding untouched."""
+    T, R = 131, D // 2 if neox else D
+    g = np.random.default_rng(n_qo * 7 + n_kv + D)
+    qbuf = torch.from_numpy(g.standard_normal((T, n_qo, D + q_pad), dtype=np.float32)).to(torch.bfloat16)
+    kbuf = torch.from_numpy(g.standard_normal((T, n_kv, D + k_pad), dtype=np.float32)).to(torch.bfloat16)
+    qw = (1 + 0.1 * torch.from_numpy(g.standard_normal(D, dtype=np.float32))).to(torch.bfloat16)
+    kw = (1 + 0.1 * torch.from_numpy(g.standard_normal(D, dtype=np.float32))).to(torch.bfloat16)
+    cache = workloads.build_cos_sin_cache(256, R, 1e4)
+    pos = torch.from_numpy(g.integers(0, 256, T)).to(torch.int32)
+    qc, kc = qbuf[:, :, :D].contiguous(), kbuf[:, :, :D].contiguous()
+    eq, ek = oracle.apply(qc, kc, qw, kw, cache, pos, is_neox=neox, eps=1e-6)
+    ref_q, ref_k = qc.cuda(), kc.cuda()
+    dw = (qw.cuda(), kw.cuda(), cache.cuda(), pos.cuda())
+    qknr.apply(ref_q, ref_k, *dw, is_neox=neox, eps=1e-6)
+    for route in ("raw", "apply"):
+        dq_buf, dk_buf = qbuf.cuda(), kbuf.cuda()
+        dq, dk = dq_buf[:, :, :D], dk_buf[:, :, :D]
+        if route == "raw":
+            rc = qknr.qknr_apply_strided(dq.data_ptr(), dk.data_ptr(), dw[0].data_ptr(),
+                                         dw[1].data_ptr(), dw[2].data_ptr(), dw[3].data_ptr(), T,
+                                         n_qo, n_kv, D, R, int(neox), dq.stride(0), dk.stride(0),
+                                         dq.stride(1), dk.stride(1), 1e-6, qknr.QKNR_BF16, None)
+            assert rc == 0, qknr.qknr_last_error()
+        else:
+            qknr.apply(dq, dk, *dw, is_neox=neox, eps=1e-6)
+        torch.cuda.synchronize()
+        assert torch.equal(dq.cpu().view(torch.int16), ref_q.cpu().view(torch.int16)), route
+        assert torch.equal(dk.cpu().view(torch.int16), ref_k.cpu().view(torch.int16)), route
+        _assert_close(dq.double().cpu().numpy(), eq, torch.bfloat16, "q")
+        _assert_close(dk.double().cpu().numpy(), ek, torch.bfloat16, "k")
+        assert torch.equal(dq_buf[:, :, D:].cpu(), qbuf[:, :, D:])
+        assert torch.equal(dk_buf[:, :, D:].cpu(), kbuf[:, :, D:])
+
+
+def test_independent_head_strides_errors(qknr):
+    T, D = 4, 64
+    q = torch.zeros(T, 2, D, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(T, 2, D + 8, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(D, dtype=torch.bfloat16, device="cuda")
+    cache = workloads.build_cos_sin_cache(8, D, 1e4).cuda()
+    pos = torch.zeros(T, dtype=torch.int32, device="cuda")
+    args = (q.data_ptr(), k.data_ptr(), w.data_ptr(), w.data_ptr(), cache.data_ptr(),
+            pos.data_ptr(), T, 2, 2, D, D, 0, 2 * D, 2 * (D + 8))
+    for q_hs, k_hs, code in ((D, -8, 2), (D, 32, 2), (D, D + 4, 4), (D, D + 8, 0)):
+        rc = qknr.qknr_apply_strided(*args, q_hs, k_hs, 1e-6, qknr.QKNR_BF16, None)
+        assert rc == code, (q_hs, k_hs, rc, qknr.qknr_last_error())
+    torch.cuda.synchronize()
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
