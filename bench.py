@@ -238,6 +238,20 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
         calls[i % n_rep]()
     torch.cuda.synchronize()
 
+    graph = None
+    if args.graph:
+        # one graph of n_rep calls (one per replica), replayed: GPU time per
+        # call without the host's launch rate (decode-sized calls)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cs = torch.cuda.current_stream().cuda_stream
+            gcalls = [PreparedCall(q, r, w, cs, entry) for r in reps]
+            for c in gcalls:
+                c()
+        graph.replay()
+        torch.cuda.synchronize()
+        args.steps = max(1, args.steps // n_rep) * n_rep
+
     sampler = ClockSampler(smi_id(device))
     sampler.start()
     barrier(dist)
@@ -245,8 +259,12 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for i in range(args.steps):
-        calls[i % n_rep]()
+    if graph is not None:
+        for _ in range(args.steps // n_rep):
+            graph.replay()
+    else:
+        for i in range(args.steps):
+            calls[i % n_rep]()
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
@@ -288,6 +306,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
                           f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.0f} MB >= 4x L2)"
                           if n_rep > 1 else "inputs larger than 4x L2"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": (f"CUDA graph of {n_rep} calls, replayed" if args.graph
+                              else "one C-ABI call per step from Python"),
                    "work_map": wm},
         "heads_per_s": world * heads * args.steps / secs,
         "pct_of_peak": round(100.0 * achieved / peak, 2),
@@ -592,6 +612,8 @@ def main(argv: Optional[List[str]] = None) -> int:
     ap.add_argument("--ceiling", action="store_true",
                     help="print torch's in-place elementwise and copy throughput at this "
                          "workload's byte count instead (context, not the op)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of a CUDA graph of calls (GPU time per call, no host launch rate)")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
                     help="unfused: time the two-kernel RMSNorm-then-RoPE chain instead")
     args = ap.parse_args(argv)

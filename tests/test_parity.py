@@ -13,6 +13,7 @@ that hold at any size); a grid over head_dim x rope_dim x pairing x position
 type x token counts 1/9/129 (the grid the deep-dive's own unit test uses,
 "Step4"); GQA head counts; strided and padded layouts; and the edge cases.
 """
+import dataclasses
 import os
 import sys
 
@@ -334,6 +335,48 @@ def test_independent_head_strides_errors(qknr):
         rc = qknr.qknr_apply_strided(*args, q_hs, k_hs, 1e-6, qknr.QKNR_BF16, None)
         assert rc == code, (q_hs, k_hs, rc, qknr.qknr_last_error())
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("pdl", [-1, 0])
+def test_cuda_graph_capture_and_replay(qknr, pdl):
+    """Calls captured into a CUDA graph (two calls on different buffers, with
+    programmatic dependent launch on or off) replay to the same bits as eager
+    calls, on new values written into the captured buffers."""
+    base = workloads.get("gqa")
+    ws = [workloads.scaled(base, 70, cache_len=4096), workloads.scaled(workloads.get("dit"), 33)]
+    qknr.set_tuning(pdl=pdl)
+    try:
+        devs = [workloads.to_device(workloads.make_inputs(w), w, "cuda") for w in ws]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for w, d in zip(ws, devs):   # warm-up outside capture (plans and occupancy cached)
+                qknr.apply(d["q"], d["k"], d["q_w"], d["k_w"], d["cos_sin_cache"], d["positions"],
+                           is_neox=w.is_neox, eps=w.eps)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for w, d in zip(ws, devs):
+                qknr.apply(d["q"], d["k"], d["q_w"], d["k_w"], d["cos_sin_cache"], d["positions"],
+                           is_neox=w.is_neox, eps=w.eps)
+        for seed in (11, 12):
+            fresh = [workloads.make_inputs(dataclasses.replace(w, seed=seed)) for w in ws]
+            refs = []
+            for w, d, f in zip(ws, devs, fresh):
+                d["q"].copy_(f["q"])
+                d["k"].copy_(f["k"])
+                r = workloads.to_device(f, w, "cuda")
+                qknr.apply(r["q"], r["k"], d["q_w"], d["k_w"], d["cos_sin_cache"], d["positions"],
+                           is_neox=w.is_neox, eps=w.eps)
+                refs.append(r)
+            graph.replay()
+            torch.cuda.synchronize()
+            for d, r in zip(devs, refs):
+                assert torch.equal(d["q"].view(torch.int16), r["q"].view(torch.int16))
+                assert torch.equal(d["k"].view(torch.int16), r["k"].view(torch.int16))
+    finally:
+        qknr.set_tuning(reset=True)
 
 
 def test_extreme_values(qknr):
