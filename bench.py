@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import time
@@ -93,12 +94,27 @@ KERNEL_SOURCES = {
 }
 
 
-def kernel_source_hash(kernel: str = "qknr_fused_kernel") -> str:
+def code_tokens(text: str) -> str:
+    """C/C++ source without comments and with whitespace collapsed: what the
+    compiler sees (the kernel sources hold no comment markers inside string
+    literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(kernel: str = "qknr_fused_kernel", read=None) -> str:
+    """sha256 over the code (comments and layout ignored) of the files the
+    kernel is built from; ``read(name)`` may supply another version's text."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "qk_rmsnorm_rope_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        if read is None:
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+        else:
+            text = read(name)
+        h.update(name.encode() + b"\0" + code_tokens(text).encode())
     return h.hexdigest()
 
 

@@ -5,7 +5,7 @@
 // launch, int32 or int64 positions, grid sized from occupancy x SM count, the
 // CUDA launch error checked), restated for this library's kernels.
 //
-// Two kernels compute the op (identical arithmetic and lane mapping):
+// Four kernels compute the op (identical arithmetic and lane mapping):
 //   register kernel  qknr_fused_kernel  (qknr_kernel.cuh): loads straight into
 //                    registers; any accepted shape and alignment.
 //   bulk kernel      qknr_bulk_kernel   (qknr_bulk_kernel.cuh): cp.async.bulk
@@ -13,8 +13,14 @@
 //                    and a 16-byte aligned cos|sin table.
 //   async kernel     qknr_async_kernel  (qknr_async_kernel.cuh): a per-warp
 //                    cp.async pipeline; same requirements as the bulk kernel.
-// The automatic choice is the register kernel (measured faster on GB300 so far);
-// the bulk kernel runs when QKNR_TUNE_KERNEL asks for it.
+//   lean kernel      qknr_lean_kernel   (qknr_lean_kernel.cuh): the register
+//                    kernel with weights and the cos|sin row in shared memory.
+// The automatic choice is the register kernel (measured fastest on GB300); the
+// others run when QKNR_TUNE_KERNEL asks for them.
+//
+// Entry points beyond the op itself: the position-checked variants (one with
+// no allocation), the unfused two-kernel baseline, the host-buffer variant
+// (direct or staged) and the variant with separate q and k head strides.
 #include "../../include/qknr.h"
 #include "qknr_async_kernel.cuh"
 #include "qknr_bulk_kernel.cuh"

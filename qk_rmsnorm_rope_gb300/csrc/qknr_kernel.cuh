@@ -16,10 +16,12 @@
 //    i.e. both halves of eight rotation pairs; lanes past the rotated span own
 //    two tail vectors from the two halves of the tail. The only shuffles are
 //    the log2(D/16)-step segmented sum of squares.
-//  * A warp item is (token, chunk of passes). Items are split across warps in
-//    balanced contiguous ranges, so a warp walks consecutive chunks of the same
-//    token and keeps that token's cos/sin values in registers across all its
-//    heads; the position and the cache row are read once per token per warp.
+//  * A warp item is (token, chunk of up to UMAX passes). By default warp w of
+//    W takes items w, w + W, w + 2W, ...: all warps sweep the tensors together,
+//    a compact window of memory at any moment. A contiguous range of items per
+//    warp is the other order. A warp keeps the current token's cos/sin values
+//    in registers and reloads them only when its token changes; positions are
+//    read 32 items ahead, so the cos/sin loads never wait for one.
 //  * Each item issues all its loads (up to UMAX passes x 2 vectors per lane)
 //    before any arithmetic, to keep many bytes in flight per SM.
 //  * Grid: persistent, at most one wave of resident CTAs; programmatic

@@ -95,3 +95,16 @@ def test_profiled_traffic_requires_matching_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("qknr_bulk_kernel", "gqa") is None
     assert bench.profiled_traffic("qknr_fused_kernel", "dit") is None
     assert bench.kernel_source_hash("qknr_fused_kernel") != bench.kernel_source_hash("qknr_bulk_kernel")
+
+
+def test_source_hash_ignores_comments_only():
+    """The profile hash follows the code: comments and layout do not change it,
+    a code change does."""
+    src = "int f(int x) {\n  return x + 1;  // one\n}\n/* block\n comment */\n"
+    same = "int f(int x) { return x + 1; }\n// another comment\n"
+    other = "int f(int x) { return x + 2; }\n"
+    assert bench.code_tokens(src) == bench.code_tokens(same)
+    assert bench.code_tokens(src) != bench.code_tokens(other)
+    h = bench.kernel_source_hash("qknr_fused_kernel")
+    assert h == bench.kernel_source_hash("qknr_fused_kernel", read=lambda n: open(
+        os.path.join(ROOT, "qk_rmsnorm_rope_gb300", "csrc", n)).read() + "\n// trailing note\n")
