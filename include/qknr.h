@@ -289,6 +289,9 @@ int qknr_sync(void *stream);
 int qknr_set_tuning(int key, int value);
 int qknr_get_tuning(int key, int *value);
 
+/* Logging: with the environment variable QKNR_LOG=1, every distinct call shape
+ * prints one line on stderr with the kernel, grid and work map chosen for it. */
+
 #define QKNR_WORK_MAP_FIELDS 12
 /*
  * The launch qknr_apply would make for these sizes (no launch, no pointers;

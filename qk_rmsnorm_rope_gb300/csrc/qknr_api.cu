@@ -39,6 +39,8 @@
 #include <functional>
 #include <initializer_list>
 #include <mutex>
+#include <array>
+#include <set>
 #include <string>
 
 namespace {
@@ -571,7 +573,32 @@ int validate(const Call &c) {
     return QKNR_OK;
 }
 
+// QKNR_LOG=1 (environment): one line on stderr per distinct call shape with
+// the launch chosen for it.
+void log_launch(const WorkMap &wm, const Call &c) {
+    static const bool on = [] {
+        const char *e = std::getenv("QKNR_LOG");
+        return e && *e && std::strcmp(e, "0") != 0;
+    }();
+    if (!on) return;
+    static std::mutex mu;
+    static std::set<std::array<long long, 10>> seen;
+    const std::array<long long, 10> key = {c.num_tokens, c.n_qo, c.n_kv, c.head_dim, c.rope_dim, c.is_neox,
+                                           c.dtype, wm.kind, wm.threads, wm.grid};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!seen.insert(key).second) return;
+    static const char *const kinds[] = {"auto", "register", "bulk", "async", "lean"};
+    std::fprintf(stderr,
+                 "qknr: T=%lld n_qo=%d n_kv=%d head_dim=%d rope_dim=%d %s %s pos%s -> %s kernel, grid %d x %d, "
+                 "%d CTAs/SM, %lld items (%d per token), %d passes per token, PDL %s\n",
+                 c.num_tokens, c.n_qo, c.n_kv, c.head_dim, c.rope_dim, c.is_neox ? "neox" : "interleaved",
+                 (c.dtype & 0xff) == QKNR_FP16 ? "fp16" : "bf16", (c.dtype & QKNR_POS_I64) ? "64" : "32",
+                 (wm.kind >= 0 && wm.kind <= 4) ? kinds[wm.kind] : "?", wm.grid, wm.threads, wm.ctas_per_sm,
+                 wm.items, wm.chunks_per_token, wm.passes_per_token, wm.pdl ? "on" : "off");
+}
+
 int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStream_t stream) {
+    log_launch(wm, c);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(wm.grid));
     cfg.blockDim = dim3(static_cast<unsigned>(wm.threads));

@@ -379,6 +379,65 @@ def test_cuda_graph_capture_and_replay(qknr, pdl):
         qknr.set_tuning(reset=True)
 
 
+def test_guard_bands_around_q_and_k(qknr):
+    """Canary bytes right before q, between q and k and right after k (one
+    allocation) keep every bit, for each kernel."""
+    w = _make(128, 64, True, "i64", 97, 6, 2, dtype="fp16", seed=4)
+    cpu = workloads.make_inputs(w)
+    eq, ek = _expected(cpu, w)
+    nq, nk, pad = cpu["q"].numel(), cpu["k"].numel(), 4096
+    for kernel in (1, 2, 3, 4):
+        buf = torch.full((pad + nq + pad + nk + pad,), -31.0, dtype=torch.float16, device="cuda")
+        dq = buf[pad:pad + nq].view(cpu["q"].shape)
+        dk = buf[2 * pad + nq:2 * pad + nq + nk].view(cpu["k"].shape)
+        dq.copy_(cpu["q"])
+        dk.copy_(cpu["k"])
+        dev = workloads.to_device(cpu, w, "cuda")
+        qknr.set_tuning(reset=True, kernel=kernel)
+        try:
+            qknr.apply(dq, dk, dev["q_w"], dev["k_w"], dev["cos_sin_cache"], dev["positions"],
+                       is_neox=w.is_neox, eps=w.eps)
+            torch.cuda.synchronize()
+        finally:
+            qknr.set_tuning(reset=True)
+        host = buf.cpu()
+        for lo, hi in ((0, pad), (pad + nq, 2 * pad + nq), (2 * pad + nq + nk, 3 * pad + nq + nk)):
+            assert (host[lo:hi] == -31.0).all(), (kernel, lo)
+        _assert_close(dq.double().cpu().numpy(), eq, torch.float16, f"q kernel {kernel}")
+        _assert_close(dk.double().cpu().numpy(), ek, torch.float16, f"k kernel {kernel}")
+
+
+_LOG_SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r})
+sys.path.insert(0, {tests!r})
+import torch, workloads
+import qk_rmsnorm_rope_gb300 as q
+q.init(0)
+w = workloads.scaled(workloads.get("dit"), 40)
+d = workloads.to_device(workloads.make_inputs(w), w, "cuda")
+for _ in range(3):
+    q.apply(d["q"], d["k"], d["q_w"], d["k_w"], d["cos_sin_cache"], d["positions"], is_neox=False)
+w2 = workloads.scaled(w, 41)
+d2 = workloads.to_device(workloads.make_inputs(w2), w2, "cuda")
+q.apply(d2["q"], d2["k"], d2["q_w"], d2["k_w"], d2["cos_sin_cache"], d2["positions"], is_neox=False)
+torch.cuda.synchronize()
+"""
+
+
+def test_log_prints_once_per_shape(qknr):
+    """QKNR_LOG=1 prints one line per distinct call shape (fresh process)."""
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, QKNR_LOG="1")
+    r = subprocess.run([sys.executable, "-c", _LOG_SCRIPT.format(root=root, tests=os.path.dirname(
+        os.path.abspath(__file__)))], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("qknr: ")]
+    assert len(lines) == 2, r.stderr
+    assert "T=40 " in lines[0] and "T=41 " in lines[1] and "register kernel" in lines[0]
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
