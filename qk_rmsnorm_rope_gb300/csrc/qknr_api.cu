@@ -244,18 +244,31 @@ struct WorkMap {
     const void *kernel = nullptr;
 };
 
-int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u_idx, int threads,
-                  const void *kernel, int *out) {
-    std::atomic<int> &slot = st.occupancy[dt][pos64][d_idx][mode][u_idx][threads_index(threads)];
+// Resident CTAs per SM of `kernel` at `threads` threads and no dynamic shared
+// memory: asked of the occupancy API once, then cached in `slot`.
+int cached_occupancy(std::atomic<int> &slot, const void *kernel, int threads, const char *what, int *out) {
     int v = slot.load(std::memory_order_relaxed);
     if (v == 0) {
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, 0);
-        if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-        if (v <= 0) return fail(QKNR_ERR_CUDA, "kernel cannot be resident with %d threads", threads);
+        if (e != cudaSuccess) return fail_cuda(e, what);
+        if (v <= 0) return fail(QKNR_ERR_CUDA, "%s: the kernel cannot be resident with %d threads", what, threads);
         slot.store(v, std::memory_order_relaxed);
     }
     *out = v;
     return QKNR_OK;
+}
+
+// A persistent grid: CTAs for every warp item, at most one wave of resident CTAs.
+int persistent_grid(long long items, int threads, int ctas_per_sm, int sm_count) {
+    const long long warps_per_cta = threads / qknr::kWarp;
+    const long long needed = (items + warps_per_cta - 1) / warps_per_cta;
+    return static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(ctas_per_sm) * sm_count)));
+}
+
+int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u_idx, int threads,
+                  const void *kernel, int *out) {
+    return cached_occupancy(st.occupancy[dt][pos64][d_idx][mode][u_idx][threads_index(threads)], kernel, threads,
+                            "cudaOccupancyMaxActiveBlocksPerMultiprocessor(register)", out);
 }
 
 // Register kernel: items are (token, chunk of warp passes); the default is the
@@ -293,9 +306,7 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     const int force = tune(QKNR_TUNE_CTAS_PER_SM);
     if (force > 0) occ = std::min(occ, force);
     wm->ctas_per_sm = occ;
-    const long long warps_per_cta = threads / qknr::kWarp;
-    const long long needed = (wm->items + warps_per_cta - 1) / warps_per_cta;
-    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(occ) * st.sm_count)));
+    wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
     wm->interleave = tune(QKNR_TUNE_ORDER) == 1 ? 0 : 1;   // interleaved unless asked otherwise
     return QKNR_OK;
 }
@@ -438,20 +449,14 @@ int plan_lean(DeviceState &st, const Call &c, WorkMap *wm) {
     const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
     wm->kernel = dt ? qknr::lean_kernel_fp16(pos64, d_idx, mode) : qknr::lean_kernel_bf16(pos64, d_idx, mode);
     if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no lean kernel for this shape");
-    std::atomic<int> &slot = st.lean_occ[dt][pos64][d_idx][mode][threads_index(threads)];
-    int occ = slot.load(std::memory_order_relaxed);
-    if (occ == 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wm->kernel, threads, 0);
-        if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(lean)");
-        if (occ <= 0) return fail(QKNR_ERR_CUDA, "lean kernel cannot be resident with %d threads", threads);
-        slot.store(occ, std::memory_order_relaxed);
-    }
+    int occ = 0;
+    const int rc = cached_occupancy(st.lean_occ[dt][pos64][d_idx][mode][threads_index(threads)], wm->kernel, threads,
+                                    "cudaOccupancyMaxActiveBlocksPerMultiprocessor(lean)", &occ);
+    if (rc) return rc;
     const int force = tune(QKNR_TUNE_CTAS_PER_SM);
     if (force > 0) occ = std::min(occ, force);
     wm->ctas_per_sm = occ;
-    const long long warps_per_cta = threads / qknr::kWarp;
-    const long long needed = (wm->items + warps_per_cta - 1) / warps_per_cta;
-    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(occ) * st.sm_count)));
+    wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
     return QKNR_OK;
 }
 
@@ -492,17 +497,12 @@ int plan_unfused(DeviceState &st, const Call &c, int op, WorkMap *wm) {
     wm->kernel = dt ? qknr::unfused_kernel_fp16(op, pos64, d_idx, mode)
                     : qknr::unfused_kernel_bf16(op, pos64, d_idx, mode);
     if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no unfused kernel for this shape");
-    std::atomic<int> &slot = st.unfused_occ[dt][op - 1][pos64][d_idx][mode];
-    int occ = slot.load(std::memory_order_relaxed);
-    if (occ == 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wm->kernel, wm->threads, 0);
-        if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(unfused)");
-        if (occ <= 0) return fail(QKNR_ERR_CUDA, "unfused kernel cannot be resident");
-        slot.store(occ, std::memory_order_relaxed);
-    }
+    int occ = 0;
+    const int rc = cached_occupancy(st.unfused_occ[dt][op - 1][pos64][d_idx][mode], wm->kernel, wm->threads,
+                                    "cudaOccupancyMaxActiveBlocksPerMultiprocessor(unfused)", &occ);
+    if (rc) return rc;
     wm->ctas_per_sm = occ;
-    const long long needed = (wm->items + 7) / 8;
-    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(occ) * st.sm_count)));
+    wm->grid = persistent_grid(wm->items, wm->threads, occ, st.sm_count);
     const int pdl = tune(QKNR_TUNE_PDL);
     wm->pdl = pdl < 0 ? 1 : pdl;
     return QKNR_OK;
