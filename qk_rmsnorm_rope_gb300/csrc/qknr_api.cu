@@ -683,6 +683,10 @@ int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStr
         prm.passes_per_token = wm.passes_per_token;
         prm.cache_vec = (c.rope_dim % 8 == 0) && aligned(c.cache, 16);
         prm.interleave = wm.interleave;
+        if (wm.chunks_per_token <= qknr::kBoundTable)
+            for (int ch = 0; ch <= wm.chunks_per_token; ++ch)
+                prm.pass_bound[ch] = static_cast<short>((static_cast<long long>(ch) * wm.passes_per_token) /
+                                                        wm.chunks_per_token);
         prm.eps = c.eps;
         prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
         cfg.dynamicSmemBytes = 0;

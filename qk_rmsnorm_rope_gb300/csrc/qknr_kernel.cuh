@@ -37,6 +37,7 @@
 namespace qknr {
 
 constexpr int kWarp = 32;
+constexpr int kBoundTable = 32;       // items per token up to which pass bounds come from a table
 
 // Kernel parameters, passed by value as a __grid_constant__.
 struct Params {
@@ -60,6 +61,7 @@ struct Params {
     int interleave;               // 1: warp w takes items w, w + W, ... (W warps); 0: a contiguous range
     float eps;
     float inv_d;                  // 1 / head_dim (exact: head_dim is a power of two)
+    short pass_bound[kBoundTable + 1];  // first pass of chunk c, c <= chunks_per_token <= kBoundTable
 };
 
 template <class P>
@@ -173,8 +175,18 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
             ch += step_c;
             if (ch >= chunks) { ch -= chunks; ++t; }
         }
-        const int pb = chunks == 1 ? 0 : (ch * p.passes_per_token) / chunks;
-        const int pe = chunks == 1 ? p.passes_per_token : ((ch + 1) * p.passes_per_token) / chunks;
+        // The item's passes [pb, pe): from the host's table, or by division. An
+        // integer division costs about twenty instructions and the kernel runs
+        // its items back to back, so the table is worth 1-2% (interleaved); the
+        // NeoX instantiations keep the division, which measured faster there.
+        int pb, pe;
+        if (MODE == kInterleaved && chunks <= kBoundTable) {
+            pb = p.pass_bound[ch];
+            pe = p.pass_bound[ch + 1];
+        } else {
+            pb = chunks == 1 ? 0 : (ch * p.passes_per_token) / chunks;
+            pe = chunks == 1 ? p.passes_per_token : ((ch + 1) * p.passes_per_token) / chunks;
+        }
 
         // this token's rows; k's is shifted back by n_qo heads so that head h
         // (q heads first, then k heads) is row + h * head_stride for both
