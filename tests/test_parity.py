@@ -438,6 +438,32 @@ def test_log_prints_once_per_shape(qknr):
     assert "T=40 " in lines[0] and "T=41 " in lines[1] and "register kernel" in lines[0]
 
 
+def test_pass_bound_table_and_division_agree(qknr):
+    """Interleaved items take their passes from a host table when a token has
+    at most 32 items, else by division: 160 heads of D=128 give 40 passes per
+    token, so one pass per item (decode-sized calls) takes the division and 4
+    passes per item take the table. Same bits either way, within tolerance."""
+    w = _make(128, 128, False, "i32", 37, 80, 80, dtype="bf16", seed=21)
+    cpu = workloads.make_inputs(w)
+    eq, ek = _expected(cpu, w)
+    outs = []
+    for passes in (1, 4):
+        qknr.set_tuning(reset=True, passes=passes)
+        try:
+            m = qknr.work_map(w.num_tokens, w.n_qo, w.n_kv, w.head_dim, w.rope_dim, w.is_neox,
+                              qknr.QKNR_BF16)
+            assert m["items_per_token"] == (40 if passes == 1 else 10)
+            dev = workloads.to_device(cpu, w, "cuda")
+            _run_gpu(qknr, dev, w)
+        finally:
+            qknr.set_tuning(reset=True)
+        _assert_close(dev["q"].double().cpu().numpy(), eq, w.torch_dtype, f"q passes={passes}")
+        _assert_close(dev["k"].double().cpu().numpy(), ek, w.torch_dtype, f"k passes={passes}")
+        outs.append((dev["q"].cpu(), dev["k"].cpu()))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
