@@ -464,6 +464,74 @@ def test_pass_bound_table_and_division_agree(qknr):
     assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
 
 
+def _random_case(g):
+    D = int(g.choice([64, 96, 128, 192, 256]))
+    neox = bool(g.integers(0, 2))
+    if neox:
+        R = int(g.choice([r for r in (2, 4, 6, 8, 16, 32, 48, 64, 96, 128, 192, 256) if r <= D and
+                          (r % 16 == 0 or r <= 8)]))
+    else:
+        R = int(g.choice([r for r in range(2, D + 1, 2)]))
+    return dict(D=D, R=R, neox=neox, T=int(g.integers(1, 70)), n_qo=int(g.integers(1, 20)),
+                n_kv=int(g.integers(1, 9)), dtype=str(g.choice(["bf16", "fp16"])),
+                pos=str(g.choice(["i32", "i64"])), head_pad=int(g.choice([0, 0, 8, 24])),
+                tok_pad=int(g.choice([0, 0, 8, 40])), kernel=int(g.choice([1, 1, 2, 3, 4])),
+                passes=int(g.integers(0, 5)), threads=int(g.choice([0, 64, 128, 256, 512])))
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_configurations(qknr, case):
+    """Seeded random configurations: head_dim, rope_dim, pairing, dtype,
+    position type, GQA head counts, padded head and token strides, kernel and
+    launch tuning together. Against the oracle, and bit for bit against the
+    automatic launch on a contiguous copy."""
+    g = np.random.default_rng(1000 + case)
+    c = _random_case(g)
+    w = _make(c["D"], c["R"], c["neox"], c["pos"], c["T"], c["n_qo"], c["n_kv"], dtype=c["dtype"],
+              seed=case, cache_len=97)
+    cpu = workloads.make_inputs(w)
+    eq, ek = _expected(cpu, w)
+    D, hs = c["D"], c["D"] + c["head_pad"]
+    dt = w.torch_dtype
+
+    def strided(x, n):
+        buf = torch.full((c["T"], n * hs + c["tok_pad"]), -5.0, dtype=dt, device="cuda")
+        view = buf[:, :n * hs].view(c["T"], n, hs)[:, :, :D]
+        view.copy_(x)
+        return buf, view
+
+    qbuf, dq = strided(cpu["q"], c["n_qo"])
+    kbuf, dk = strided(cpu["k"], c["n_kv"])
+    dev = workloads.to_device(cpu, w, "cuda")
+    kernel = c["kernel"]
+    if D in (96, 192) or (c["R"] % 8 and kernel in (2, 3)):
+        kernel = 1
+    tune = {"kernel": kernel}
+    if kernel in (1, 4) and c["passes"]:
+        tune["passes"] = c["passes"]
+    if c["threads"] and kernel in (1, 3, 4):
+        tune["threads"] = c["threads"] if kernel == 1 else min(c["threads"], 256)
+    qknr.set_tuning(reset=True, **tune)
+    try:
+        qknr.apply(dq, dk, dev["q_w"], dev["k_w"], dev["cos_sin_cache"], dev["positions"],
+                   is_neox=w.is_neox, eps=w.eps)
+        torch.cuda.synchronize()
+    finally:
+        qknr.set_tuning(reset=True)
+    _assert_close(dq.double().cpu().numpy(), eq, dt, f"q {c}")
+    _assert_close(dk.double().cpu().numpy(), ek, dt, f"k {c}")
+    ref = workloads.to_device(cpu, w, "cuda")
+    _run_gpu(qknr, ref, w)
+    assert torch.equal(dq.cpu().view(torch.int16), ref["q"].cpu().view(torch.int16)), c
+    assert torch.equal(dk.cpu().view(torch.int16), ref["k"].cpu().view(torch.int16)), c
+    # bytes outside the heads keep every bit
+    for buf, n in ((qbuf, c["n_qo"]), (kbuf, c["n_kv"])):
+        host = buf.cpu()
+        mask = torch.ones_like(host, dtype=torch.bool)
+        mask[:, :n * hs].view(c["T"], n, hs)[:, :, :D] = False
+        assert (host[mask] == -5.0).all(), c
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
