@@ -278,6 +278,35 @@ def _marshal(q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_d
     return out
 
 
+def _prepare(q, positions, stream):
+    """The raw stream handle for a call on q's device, and positions as the op
+    takes them: int32 or int64, contiguous, on q's device. Positions on another
+    device, on the host or of another integer type are converted there first (as
+    the page's upstream wrapper does); the call's stream then waits for that copy
+    and keeps the converted tensor alive until the kernel has run."""
+    import torch
+    if q.device.type != "cuda":
+        raise QknrError(2, "all tensors must be on one CUDA device (CPU tensors are refused: no CPU path)")
+    cur = torch.cuda.current_stream(q.device)
+    if stream is None:
+        s_obj = cur
+    elif isinstance(stream, int):
+        s_obj = torch.cuda.ExternalStream(stream, device=q.device)
+    else:
+        s_obj = stream
+    if not (positions.dtype in (torch.int32, torch.int64) and positions.device == q.device
+            and positions.is_contiguous()):
+        if positions.dtype.is_floating_point or positions.dtype.is_complex or positions.dtype == torch.bool:
+            raise QknrError(2, f"positions must be an integer tensor, not {positions.dtype}")
+        dt = torch.int32 if positions.dtype == torch.int32 else torch.int64
+        with torch.cuda.device(q.device):
+            positions = positions.to(device=q.device, dtype=dt).contiguous()
+        if s_obj != cur:
+            s_obj.wait_stream(cur)
+            positions.record_stream(s_obj)
+    return positions, s_obj.cuda_stream
+
+
 def apply(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float = 1e-6,
           head_dim: int = 0, rope_dim: int = 0, stream=None) -> None:
     """In-place fused QK RMSNorm + RoPE on torch CUDA tensors (returns None).
@@ -286,15 +315,12 @@ def apply(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float
     overwritten. Runs on ``stream`` (a torch.cuda.Stream or raw handle),
     default torch's current stream on q's device. q and k may have different
     head strides (qknr_apply_strided); with one shared stride this is
-    qknr_apply.
+    qknr_apply. Positions may be any integer tensor (see _prepare).
     """
     import torch
+    positions, stream = _prepare(q, positions, stream)
     T, n_qo, n_kv, D, R, qs, ks, hs, code, khs = _marshal(
         q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim, split_strides=True)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-    elif not isinstance(stream, int):
-        stream = stream.cuda_stream
     with torch.cuda.device(q.device):
         if khs == hs:
             _check(qknr_apply(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
@@ -313,12 +339,9 @@ def apply_checked(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, ep
     cache. Synchronous; raises QknrError (QKNR_ERR_POSITION_OOB) if one does
     not, leaving those tokens untouched."""
     import torch
+    positions, stream = _prepare(q, positions, stream)
     T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(q, k, q_w, k_w, cos_sin_cache, positions,
                                                       is_neox, head_dim, rope_dim)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-    elif not isinstance(stream, int):
-        stream = stream.cuda_stream
     with torch.cuda.device(q.device):
         _check(qknr_apply_checked(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
                                   cos_sin_cache.data_ptr(), cos_sin_cache.shape[0],
@@ -331,12 +354,9 @@ def apply_unfused(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, ep
     """The unfused two-kernel baseline (RMSNorm kernel, then RoPE kernel), in
     place; for measuring what fusion saves. See qknr_apply_unfused."""
     import torch
+    positions, stream = _prepare(q, positions, stream)
     T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(q, k, q_w, k_w, cos_sin_cache, positions,
                                                       is_neox, head_dim, rope_dim)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-    elif not isinstance(stream, int):
-        stream = stream.cuda_stream
     with torch.cuda.device(q.device):
         _check(qknr_apply_unfused(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
                                   cos_sin_cache.data_ptr(), positions.data_ptr(), T, n_qo, n_kv, D,

@@ -532,6 +532,33 @@ def test_random_configurations(qknr, case):
         assert (host[mask] == -5.0).all(), c
 
 
+def test_positions_are_converted(qknr):
+    """apply() takes positions of any integer type, on the host or the device,
+    converting them to q's device first (the reference wrapper does the same);
+    on a side stream too. Same bits as device int32 positions. Float positions
+    are refused."""
+    w = _make(128, 64, True, "i32", 61, 8, 2, dtype="bf16", seed=31, cache_len=120)
+    cpu = workloads.make_inputs(w)
+    ref = workloads.to_device(cpu, w, "cuda")
+    _run_gpu(qknr, ref, w)
+    p32 = cpu["positions"]
+    variants = [p32.to(torch.int64), p32.to(torch.int16), p32.to(torch.uint8), p32,
+                p32.cuda().to(torch.int16), p32.to(torch.int64)[::1]]
+    side = torch.cuda.Stream()
+    for i, pos in enumerate(variants):
+        dev = workloads.to_device(cpu, w, "cuda")
+        stream = side if i % 2 else None
+        qknr.apply(dev["q"], dev["k"], dev["q_w"], dev["k_w"], dev["cos_sin_cache"], pos,
+                   is_neox=w.is_neox, eps=w.eps, stream=stream)
+        torch.cuda.synchronize()
+        assert torch.equal(dev["q"].view(torch.int16), ref["q"].view(torch.int16)), (i, pos.dtype)
+        assert torch.equal(dev["k"].view(torch.int16), ref["k"].view(torch.int16)), (i, pos.dtype)
+    dev = workloads.to_device(cpu, w, "cuda")
+    with pytest.raises(qknr.QknrError):
+        qknr.apply(dev["q"], dev["k"], dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
+                   p32.float(), is_neox=w.is_neox, eps=w.eps)
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
