@@ -238,11 +238,23 @@ def can_use(head_dim: int, rope_dim: int, is_neox: bool, dtype=None) -> bool:
     return bool(qknr_can_use(head_dim, rope_dim, int(is_neox), code))
 
 
+def _as_tokens(t, name):
+    """A [B, S, H, D] tensor as the [B*S, H, D] view of the same memory (the op
+    works in place, so a copy would not do); 3-D tensors as they are."""
+    if t.dim() == 4:
+        try:
+            return t.view(t.shape[0] * t.shape[1], t.shape[2], t.shape[3])
+        except RuntimeError:
+            raise QknrError(2, f"{name}: a 4-D tensor whose batch and sequence dims do not merge "
+                               "into one token dim without a copy") from None
+    return t
+
+
 def _marshal(q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim,
              same_device=True, split_strides=False):
     import torch
     if q.dim() != 3 or k.dim() != 3:
-        raise QknrError(2, "q and k must be [num_tokens, heads, head_dim] (reshape 4-D inputs)")
+        raise QknrError(2, "q and k must be [num_tokens, heads, head_dim] or [batch, seq, heads, head_dim]")
     T, n_qo, D = q.shape
     if k.shape[0] != T or k.shape[2] != D:
         raise QknrError(2, f"k shape {tuple(k.shape)} does not match q {tuple(q.shape)}")
@@ -311,13 +323,15 @@ def apply(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float
           head_dim: int = 0, rope_dim: int = 0, stream=None) -> None:
     """In-place fused QK RMSNorm + RoPE on torch CUDA tensors (returns None).
 
-    q [T, n_qo, D] and k [T, n_kv, D] (bf16/fp16, unit innermost stride) are
+    q [T, n_qo, D] and k [T, n_kv, D] (bf16/fp16, unit innermost stride; or
+    [B, S, H, D] when B and S merge into one token dim without a copy) are
     overwritten. Runs on ``stream`` (a torch.cuda.Stream or raw handle),
     default torch's current stream on q's device. q and k may have different
     head strides (qknr_apply_strided); with one shared stride this is
     qknr_apply. Positions may be any integer tensor (see _prepare).
     """
     import torch
+    q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
     positions, stream = _prepare(q, positions, stream)
     T, n_qo, n_kv, D, R, qs, ks, hs, code, khs = _marshal(
         q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim, split_strides=True)
@@ -339,6 +353,7 @@ def apply_checked(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, ep
     cache. Synchronous; raises QknrError (QKNR_ERR_POSITION_OOB) if one does
     not, leaving those tokens untouched."""
     import torch
+    q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
     positions, stream = _prepare(q, positions, stream)
     T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(q, k, q_w, k_w, cos_sin_cache, positions,
                                                       is_neox, head_dim, rope_dim)
@@ -354,6 +369,7 @@ def apply_unfused(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, ep
     """The unfused two-kernel baseline (RMSNorm kernel, then RoPE kernel), in
     place; for measuring what fusion saves. See qknr_apply_unfused."""
     import torch
+    q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
     positions, stream = _prepare(q, positions, stream)
     T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(q, k, q_w, k_w, cos_sin_cache, positions,
                                                       is_neox, head_dim, rope_dim)

@@ -559,6 +559,27 @@ def test_positions_are_converted(qknr):
                    p32.float(), is_neox=w.is_neox, eps=w.eps)
 
 
+def test_four_d_inputs(qknr):
+    """[B, S, H, D] q and k whose batch and sequence dims merge without a copy
+    run in place (same bits as the 3-D call); ones that do not are refused."""
+    w = _make(64, 64, False, "i32", 63, 4, 2, dtype="fp16", seed=41, cache_len=80)
+    cpu = workloads.make_inputs(w)
+    ref = workloads.to_device(cpu, w, "cuda")
+    _run_gpu(qknr, ref, w)
+    dev = workloads.to_device(cpu, w, "cuda")
+    q4, k4 = dev["q"].view(3, 21, 4, 64), dev["k"].view(3, 21, 2, 64)
+    qknr.apply(q4, k4, dev["q_w"], dev["k_w"], dev["cos_sin_cache"], dev["positions"],
+               is_neox=False, eps=w.eps)
+    torch.cuda.synchronize()
+    assert torch.equal(dev["q"].view(torch.int16), ref["q"].view(torch.int16))
+    assert torch.equal(dev["k"].view(torch.int16), ref["k"].view(torch.int16))
+    qt = dev["q"].view(3, 21, 4, 64).transpose(0, 1)     # [S, B, H, D]: no single token stride
+    kt = dev["k"].view(3, 21, 2, 64).transpose(0, 1)
+    with pytest.raises(qknr.QknrError, match="merge"):
+        qknr.apply(qt, kt, dev["q_w"], dev["k_w"], dev["cos_sin_cache"], dev["positions"],
+                   is_neox=False, eps=w.eps)
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
