@@ -82,8 +82,8 @@ int qknr_version(void);
 /*
  * Shape gate, the counterpart of the deep-dive's can_use check (§5.2) for
  * this library's own kernels. Returns 1 if (head_dim, rope_dim, is_neox,
- * dtype) is in the accepted set, else 0. Accepted: head_dim in {64, 96, 128,
- * 192, 256} (96 and 192 with the register kernel only);
+ * dtype) is in the accepted set, else 0. Accepted: head_dim in {64, 80, 96,
+ * 128, 192, 256} (80, 96 and 192 with the register kernel only);
  * rope_dim even with 0 < rope_dim <= head_dim; interleaved pairing takes
  * every such rope_dim; NeoX pairing takes rope_dim % 16 == 0 or rope_dim in
  * {2, 4, 6, 8}. This contains the page's set (head_dim/32 elements per lane,

@@ -210,7 +210,7 @@ bool shape_ok(int head_dim, int rope_dim, int is_neox) {
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Heads one warp pass covers: a head's lane group is head_dim/16 lanes rounded
-// up to a power of two (the kernels' padding for head_dim 96 and 192).
+// up to a power of two (the kernels' padding for head_dim 80, 96 and 192).
 int heads_per_pass(int head_dim) {
     int lph = 1;
     while (lph < head_dim / 16) lph *= 2;
@@ -529,7 +529,7 @@ int validate(const Call &c) {
         return fail(QKNR_ERR_INVALID_ARG, "head counts n_qo=%d n_kv=%d must be >= 1", c.n_qo, c.n_kv);
     if (!shape_ok(c.head_dim, c.rope_dim, c.is_neox))
         return fail(QKNR_ERR_UNSUPPORTED,
-                    "unsupported head_dim=%d rope_dim=%d is_neox=%d (head_dim in {64,96,128,192,256}; rope_dim even, "
+                    "unsupported head_dim=%d rope_dim=%d is_neox=%d (head_dim in {64,80,96,128,192,256}; rope_dim even, "
                     "0 < rope_dim <= head_dim; NeoX needs rope_dim %% 16 == 0 or rope_dim <= 8)",
                     c.head_dim, c.rope_dim, c.is_neox);
     if (!std::isfinite(c.eps) || c.eps < 0.f) return fail(QKNR_ERR_INVALID_ARG, "eps must be a finite value >= 0");

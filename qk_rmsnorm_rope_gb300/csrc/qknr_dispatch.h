@@ -8,8 +8,9 @@ constexpr int kNumUnroll = 2;
 constexpr int kUnrollClass[kNumUnroll] = {2, 4};
 
 // head_dim classes
-constexpr int kNumHeadDim = 5;
-constexpr int kHeadDims[kNumHeadDim] = {64, 96, 128, 192, 256};  // 96 and 192: register kernel only
+constexpr int kNumHeadDim = 6;
+// 80, 96 and 192 (lane groups padded to a power of two): register kernel only
+constexpr int kHeadDims[kNumHeadDim] = {64, 96, 128, 192, 256, 80};
 
 // Kernel entry for (position type, head_dim class, mode, unroll class), or
 // nullptr. Defined in qknr_inst_bf16.cu / qknr_inst_fp16.cu.

@@ -35,6 +35,7 @@ const void *by_head_dim(int d_idx, int mode, int u_idx) {
         case 2: return by_mode<P, 128>(mode, u_idx);
         case 3: return by_mode<P, 192>(mode, u_idx);
         case 4: return by_mode<P, 256>(mode, u_idx);
+        case 5: return by_mode<P, 80>(mode, u_idx);
         default: return nullptr;
     }
 }
@@ -47,7 +48,7 @@ const void *bulk_by_mode(int mode) {
 
 template <class P>
 const void *bulk_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {   // head_dim 96 / 192: register kernel only
+    switch (d_idx) {   // head_dim 80 / 96 / 192: register kernel only
         case 0: return bulk_by_mode<P, 64>(mode);
         case 2: return bulk_by_mode<P, 128>(mode);
         case 4: return bulk_by_mode<P, 256>(mode);
@@ -76,7 +77,7 @@ const void *async_by_mode(int mode) {
 
 template <class P>
 const void *async_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {   // head_dim 96 / 192: register kernel only
+    switch (d_idx) {   // head_dim 80 / 96 / 192: register kernel only
         case 0: return async_by_mode<P, 64>(mode);
         case 2: return async_by_mode<P, 128>(mode);
         case 4: return async_by_mode<P, 256>(mode);
@@ -92,7 +93,7 @@ const void *lean_by_mode(int mode) {
 
 template <class P>
 const void *lean_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {   // head_dim 96 / 192: register kernel only
+    switch (d_idx) {   // head_dim 80 / 96 / 192: register kernel only
         case 0: return lean_by_mode<P, 64>(mode);
         case 2: return lean_by_mode<P, 128>(mode);
         case 4: return lean_by_mode<P, 256>(mode);
@@ -117,6 +118,7 @@ const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode) {
         case 2: return unfused_by_op<128>(op, pos64, mode);
         case 3: return unfused_by_op<192>(op, pos64, mode);
         case 4: return unfused_by_op<256>(op, pos64, mode);
+        case 5: return unfused_by_op<80>(op, pos64, mode);
         default: return nullptr;
     }
 }

@@ -75,7 +75,7 @@ __device__ __forceinline__ long long load_position(const void *positions, long l
 template <class T, class P, int D, int MODE, int UMAX, int OP = kOpFused>
 __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__ Params p) {
     // A head's data takes NVH lanes (two 16-byte vectors each); its lane group
-    // is LPH lanes, NVH rounded up to a power of two (head_dim 96 and 192 leave
+    // is LPH lanes, NVH rounded up to a power of two (head_dim 80, 96 and 192 leave
     // 2 and 4 lanes of the group idle: no loads, no stores, zero in the sum).
     constexpr int NVH = D / 16;
     constexpr int LPH = NVH <= 1 ? 1 : NVH <= 2 ? 2 : NVH <= 4 ? 4 : NVH <= 8 ? 8 : NVH <= 16 ? 16 : 32;

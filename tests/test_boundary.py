@@ -86,7 +86,8 @@ def test_can_use_contains_the_pages_set():
 
 
 def test_can_use_rejects():
-    assert qknr.qknr_can_use(80, 64, 0, 0) == 0          # head_dim outside {64,96,128,192,256}
+    assert qknr.qknr_can_use(72, 64, 0, 0) == 0          # head_dim outside {64,80,96,128,192,256}
+    assert qknr.qknr_can_use(80, 32, 1, 0) == 1          # Phi-2-like: head_dim 80, NeoX rotary 32
     assert qknr.qknr_can_use(96, 64, 1, 0) == 1          # head_dim 96 (register kernel)
     assert qknr.qknr_can_use(192, 96, 1, 0) == 1
     assert qknr.qknr_can_use(128, 0, 0, 0) == 0          # rope_dim 0

@@ -125,12 +125,12 @@ def test_workload_full_size_sampled(qknr, name):
 
 def _rope_dims(D, neox):
     if neox:
-        return sorted({r for r in (4, 8, 16, 32, 64, D // 2, D) if r <= D})
+        return sorted({r for r in (4, 8, 16, 32, 64, D // 2, D) if r <= D and (r % 16 == 0 or r <= 8)})
     return sorted({r for r in (2, 6, 8, 24, 64, D // 2, D - 8, D) if 0 < r <= D})
 
 
 GRID = [(D, R, neox, pos, T)
-        for D in (64, 96, 128, 192, 256)
+        for D in (64, 80, 96, 128, 192, 256)
         for neox in (False, True)
         for R in _rope_dims(D, neox)
         for pos in ("i32", "i64")
@@ -153,7 +153,7 @@ def test_shape_grid(qknr, D, R, neox, pos, T, kernel):
     rope_dim % 8 == 0 (elsewhere that case runs the register kernel)."""
     w = _make(D, R, neox, pos, T, 4, 2, dtype="bf16" if (D + R + T) % 2 == 0 else "fp16")
     kind = {"register": 1, "bulk": 2, "async": 3, "lean": 4}[kernel]
-    if D in (96, 192) or (R % 8 and kind in (2, 3)):
+    if D in (80, 96, 192) or (R % 8 and kind in (2, 3)):
         kind = 1    # cases only the register kernel takes
     qknr.set_tuning(reset=True, kernel=kind)
     try:
@@ -162,10 +162,15 @@ def test_shape_grid(qknr, D, R, neox, pos, T, kernel):
         qknr.set_tuning(reset=True)
 
 
+def _neox_half(D):
+    """A NeoX rope_dim near half of head_dim that the op takes (a multiple of 16)."""
+    return D // 2 if (D // 2) % 16 == 0 else (D // 2) // 16 * 16
+
+
 @pytest.mark.parametrize("n_qo,n_kv", [(1, 1), (8, 1), (32, 8), (5, 3), (1, 7), (64, 64)])
-@pytest.mark.parametrize("D", [64, 96, 128, 192, 256])
+@pytest.mark.parametrize("D", [64, 80, 96, 128, 192, 256])
 def test_gqa_head_counts(qknr, n_qo, n_kv, D):
-    w = _make(D, D // 2, True, "i64", 33, n_qo, n_kv, dtype="fp16", seed=n_qo * 100 + n_kv)
+    w = _make(D, _neox_half(D), True, "i64", 33, n_qo, n_kv, dtype="fp16", seed=n_qo * 100 + n_kv)
     _check_workload(qknr, w)
 
 
@@ -465,7 +470,7 @@ def test_pass_bound_table_and_division_agree(qknr):
 
 
 def _random_case(g):
-    D = int(g.choice([64, 96, 128, 192, 256]))
+    D = int(g.choice([64, 80, 96, 128, 192, 256]))
     neox = bool(g.integers(0, 2))
     if neox:
         R = int(g.choice([r for r in (2, 4, 6, 8, 16, 32, 48, 64, 96, 128, 192, 256) if r <= D and
@@ -504,7 +509,7 @@ def test_random_configurations(qknr, case):
     kbuf, dk = strided(cpu["k"], c["n_kv"])
     dev = workloads.to_device(cpu, w, "cuda")
     kernel = c["kernel"]
-    if D in (96, 192) or (c["R"] % 8 and kernel in (2, 3)):
+    if D in (80, 96, 192) or (c["R"] % 8 and kernel in (2, 3)):
         kernel = 1
     tune = {"kernel": kernel}
     if kernel in (1, 4) and c["passes"]:
@@ -624,7 +629,7 @@ def test_empty_and_errors_leave_inputs_untouched(qknr):
     # stride not a multiple of 8 elements
     assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 128, 64, 0, 260, 256, 128, 1e-6, 0, s) == 4
     # unsupported shapes
-    assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 80, 64, 0, 256, 256, 128, 1e-6, 0, s) == 3
+    assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 72, 64, 0, 256, 256, 128, 1e-6, 0, s) == 3
     assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 128, 24, 1, 256, 256, 128, 1e-6, 0, s) == 3
     # invalid arguments
     assert qknr.qknr_apply(qp, kp, *common, -1, 2, 2, 128, 64, 0, 256, 256, 128, 1e-6, 0, s) == 2
@@ -756,20 +761,20 @@ def test_unfused_norm_step_is_the_fused_op_at_position_zero(qknr):
 def test_planned_passes_cover_every_head(qknr):
     """The host's passes per token must match the kernels' lane groups: a head
     takes head_dim/16 lanes rounded up to a power of two, so a pass covers
-    32 / that many heads (head_dim 96 and 192 pad their groups)."""
-    for D in (64, 96, 128, 192, 256):
+    32 / that many heads (head_dim 80, 96 and 192 pad their groups)."""
+    for D in (64, 80, 96, 128, 192, 256):
         group = 1
         while group < D // 16:
             group *= 2
         per_pass = 32 // group
         for n_qo, n_kv in ((1, 1), (8, 1), (4, 2), (1, 7), (24, 24), (32, 8), (13, 5)):
             H = n_qo + n_kv
-            for kernel in (1, 4) if D in (96, 192) else (1, 2, 3, 4):
-                if D in (96, 192) and kernel != 1:
+            for kernel in (1, 4) if D in (80, 96, 192) else (1, 2, 3, 4):
+                if D in (80, 96, 192) and kernel != 1:
                     continue
                 qknr.set_tuning(reset=True, kernel=kernel)
                 try:
-                    m = qknr.work_map(33, n_qo, n_kv, D, D // 2, True, qknr.QKNR_FP16)
+                    m = qknr.work_map(33, n_qo, n_kv, D, _neox_half(D), True, qknr.QKNR_FP16)
                 finally:
                     qknr.set_tuning(reset=True)
                 if m["kernel"] == "bulk":

@@ -26,7 +26,7 @@ def test_can_use_gate():
     assert torch_op.can_use_fused_inplace_qknorm_rope(128, 64, True, torch.float16)
     assert torch_op.can_use_fused_inplace_qknorm_rope(256, 128, False, torch.bfloat16)
     assert torch_op.can_use_fused_inplace_qknorm_rope(96, 64, False, torch.bfloat16)
-    assert not torch_op.can_use_fused_inplace_qknorm_rope(80, 64, False, torch.bfloat16)
+    assert not torch_op.can_use_fused_inplace_qknorm_rope(72, 64, False, torch.bfloat16)
     assert not torch_op.can_use_fused_inplace_qknorm_rope(128, 64, False, torch.float32)
 
 
