@@ -585,6 +585,36 @@ def test_four_d_inputs(qknr):
                    is_neox=False, eps=w.eps)
 
 
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
+def test_offsets_beyond_two_gib(qknr, kernel):
+    """q spans 2.5 GB, so its last tokens sit more than 2^31 bytes from its
+    start (64-bit addressing); sampled tokens over the whole range against the
+    oracle, for every kernel. Inputs are drawn on the device (seeded), samples
+    copied back."""
+    T, n_qo, n_kv, D, R, L = 600_000, 16, 4, 128, 128, 4096
+    g = torch.Generator(device="cuda").manual_seed(77)
+    q = torch.randn(T, n_qo, D, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(T, n_kv, D, device="cuda", generator=g).to(torch.bfloat16)
+    assert (T - 1) * q.stride(0) * 2 > 2 ** 31
+    qw = (1 + 0.1 * torch.randn(D, device="cuda", generator=g)).to(torch.bfloat16)
+    kw = (1 + 0.1 * torch.randn(D, device="cuda", generator=g)).to(torch.bfloat16)
+    cache = workloads.build_cos_sin_cache(L, R, 1e4)
+    pos = torch.randint(0, L, (T,), device="cuda", generator=g, dtype=torch.int64)
+    idx = _sample_tokens(T, 96, 5)
+    idx = torch.cat([idx, torch.arange(T - 8, T)]).unique()
+    q0, k0, p0 = q[idx.cuda()].cpu(), k[idx.cuda()].cpu(), pos[idx.cuda()].cpu()
+    qknr.set_tuning(reset=True, kernel=kernel)
+    try:
+        qknr.apply(q, k, qw, kw, cache.cuda(), pos, is_neox=False, eps=1e-6)
+        torch.cuda.synchronize()
+    finally:
+        qknr.set_tuning(reset=True)
+    eq, ek = oracle.apply(q0, k0, qw.cpu(), kw.cpu(), cache, p0, is_neox=False, eps=1e-6)
+    _assert_close(q[idx.cuda()].double().cpu().numpy(), eq, torch.bfloat16, "q beyond 2 GiB")
+    _assert_close(k[idx.cuda()].double().cpu().numpy(), ek, torch.bfloat16, "k")
+    del q, k
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
