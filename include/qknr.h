@@ -255,6 +255,16 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
  */
 int qknr_sync(void *stream);
 
+/*
+ * Exercises the watchdog path: launches on `stream` a one-thread kernel whose
+ * bounded wait (the bulk kernel's, about one second) is on a barrier that
+ * nothing arrives on. The wait runs out, the kernel sets the watchdog bit and
+ * returns; the next qknr_sync on the device then reports QKNR_ERR_WATCHDOG
+ * and clears it. No fault, no unbounded wait: the context stays usable. For
+ * tests of a caller's error handling. The op has no counterpart on the pages.
+ */
+int qknr_selftest_watchdog(void *stream);
+
 /* kernels (QKNR_TUNE_KERNEL values and qknr_query_work_map out[0]) */
 #define QKNR_KERNEL_AUTO 0
 #define QKNR_KERNEL_REGISTER 1 /* loads straight into registers; every accepted shape */

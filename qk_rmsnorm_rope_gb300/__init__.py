@@ -21,7 +21,7 @@ __all__ = [
     "QKNR_HOST_DIRECT", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
     "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-    "qknr_apply_host", "qknr_apply_strided", "qknr_sync",
+    "qknr_apply_host", "qknr_apply_strided", "qknr_sync", "qknr_selftest_watchdog",
     "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map", "TUNE_KEYS",
     "init", "apply", "apply_checked", "apply_unfused", "apply_host", "can_use", "dtype_code",
     "work_map", "set_tuning", "get_tuning", "sync",
@@ -85,13 +85,14 @@ def _load() -> ctypes.CDLL:
     lib.qknr_apply_strided.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
                                        i64, i64, i64, i64, f32, i32, vp]
     lib.qknr_sync.argtypes = [vp]
+    lib.qknr_selftest_watchdog.argtypes = [vp]
     lib.qknr_set_tuning.argtypes = [i32, i32]
     lib.qknr_get_tuning.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
     lib.qknr_query_work_map.argtypes = [i64, i32, i32, i32, i32, i32, i32,
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
                  "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-                 "qknr_apply_host", "qknr_apply_strided", "qknr_sync",
+                 "qknr_apply_host", "qknr_apply_strided", "qknr_sync", "qknr_selftest_watchdog",
                  "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
@@ -189,6 +190,10 @@ def qknr_apply_strided(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_q
     return _get_lib().qknr_apply_strided(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens,
                                          n_qo, n_kv, head_dim, rope_dim, int(is_neox), q_stride,
                                          k_stride, q_head_stride, k_head_stride, eps, dtype, stream)
+
+
+def qknr_selftest_watchdog(stream) -> int:
+    return _get_lib().qknr_selftest_watchdog(stream)
 
 
 def qknr_sync(stream) -> int:

@@ -723,6 +723,19 @@ int run_checked(DeviceState &st, const WorkMap &wm, const Call &c, cudaStream_t 
     return QKNR_OK;
 }
 
+// Watchdog self-test: one thread waits, with the bulk kernel's bounded wait,
+// on a shared-memory barrier that nothing arrives on. After the limit (about a
+// second) the wait gives up, the watchdog bit is set and the kernel returns,
+// exactly as a stalled bulk-kernel wait would; the context stays usable.
+__global__ void qknr_watchdog_selftest_kernel(unsigned long long *status) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x == 0) {
+        qknr::mbar_init(qknr::smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!qknr::mbar_wait_bounded(qknr::smem_u32(&bar), 0u)) atomicOr(status + 2, qknr::kWatchdogBit);
+    }
+}
+
 int apply_impl(const Call &c, void *stream, bool checked) {
     DeviceState *st = current_state();
     if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
@@ -1212,6 +1225,15 @@ int qknr_apply_strided(void *q, void *k, const void *q_w, const void *k_w, const
                        is_neox, q_stride, k_stride, q_head_stride, eps, dtype);
     c.k_head_stride = k_head_stride;
     return apply_strided_impl(c, stream);
+}
+
+int qknr_selftest_watchdog(void *stream) {
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    qknr_watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st->status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "watchdog self-test launch");
+    return QKNR_OK;
 }
 
 int qknr_sync(void *stream) {

@@ -153,7 +153,8 @@ rc4 = q.qknr_sync(None)
 rc5 = q.qknr_apply_host(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 1e-6, 0,
                         0, 0, None)
 rc6 = q.qknr_apply_strided(16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 128, 1e-6, 0, None)
-print(rc2, rc3, rc4, rc5, rc6)
+rc7 = q.qknr_selftest_watchdog(None)
+print(rc2, rc3, rc4, rc5, rc6, rc7)
 """
 
 
@@ -165,4 +166,4 @@ def test_calls_before_init_are_refused():
     assert r.returncode == 0, r.stderr
     first, second = r.stdout.strip().splitlines()[-2:]
     assert first.startswith("1 ") and "qknr_init" in first
-    assert second.split() == ["1", "1", "1", "1", "1"]
+    assert second.split() == ["1", "1", "1", "1", "1", "1"]

@@ -615,6 +615,24 @@ def test_offsets_beyond_two_gib(qknr, kernel):
     del q, k
 
 
+def test_watchdog_runs_out_and_recovers(qknr):
+    """A bounded kernel wait that runs out (a barrier nothing arrives on) sets
+    the watchdog bit after about a second; qknr_sync reports it once and clears
+    it, and the context stays usable for correct calls."""
+    import time
+    s = torch.cuda.current_stream().cuda_stream
+    assert qknr.qknr_sync(s) == 0
+    t0 = time.perf_counter()
+    assert qknr.qknr_selftest_watchdog(s) == 0
+    rc = qknr.qknr_sync(s)
+    dt = time.perf_counter() - t0
+    assert rc == 7 and "watchdog" in qknr.qknr_last_error(), (rc, qknr.qknr_last_error())
+    assert 0.9 < dt < 60, dt
+    assert qknr.qknr_sync(s) == 0
+    w = workloads.scaled(workloads.get("gqa"), 50, cache_len=4096)
+    _check_workload(qknr, w)
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
