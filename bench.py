@@ -274,18 +274,33 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    # segment boundaries for the spread of the time per step (10 segments; an
+    # event between two launches once every K/10 steps)
+    n_seg = 10 if args.steps >= 100 and graph is None else 0
+    seg_len = args.steps // n_seg if n_seg else 0
+    seg_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_seg)]
     ev0.record(stream)
     if graph is not None:
         for _ in range(args.steps // n_rep):
             graph.replay()
     else:
         for i in range(args.steps):
+            if n_seg and i % seg_len == 0 and i // seg_len < n_seg:
+                seg_ev[i // seg_len].record(stream)
             calls[i % n_rep]()
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     clocks = sampler.stop()
     ms = ev0.elapsed_time(ev1)
+    spread = None
+    if n_seg:
+        bounds = seg_ev + [ev1]
+        lens = [seg_len] * (n_seg - 1) + [args.steps - seg_len * (n_seg - 1)]
+        per_step = sorted(bounds[j].elapsed_time(bounds[j + 1]) / lens[j] for j in range(n_seg))
+        pick = lambda f: per_step[min(n_seg - 1, int(round(f * (n_seg - 1))))]
+        spread = {"p10": round(pick(0.1), 6), "p50": round(pick(0.5), 6), "p90": round(pick(0.9), 6),
+                  "unit": "ms per step", "over": f"{n_seg} segments of the timed steps"}
     ms_max = max_over_ranks(dist, ms, device)
 
     # end to end through the C ABI from pinned host buffers: H2D of q, k and
@@ -313,6 +328,7 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "ms_per_step_spread": spread,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "shape": workloads.describe(w),
