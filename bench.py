@@ -469,6 +469,28 @@ def _sample_bytes(w, n_tok):
     return workloads.algorithmic_bytes(workloads.scaled(w, n_tok, cache_len=w.cache_len))
 
 
+def host_cpu() -> str:
+    """The host CPU's model and core count (lscpu, else /proc/cpuinfo)."""
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith(("model name", "cpu part")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return f"{model or 'unknown'}, {os.cpu_count()} cores"
+
+
 def cpu_baseline(w, cpu, budget_s: float = 10.0) -> Dict:
     """The oracle as it stands (one thread, double precision) on a bounded
     sample: consecutive token blocks of the workload until ~budget_s seconds."""
@@ -490,7 +512,7 @@ def cpu_baseline(w, cpu, budget_s: float = 10.0) -> Dict:
     return {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{done_tok} tokens of {w.name} in blocks of {block} ({t_used:.1f} s, "
                       f"double precision, single thread)",
-            "heads_per_s": done_tok * (w.n_qo + w.n_kv) / t_used,
+            "heads_per_s": done_tok * (w.n_qo + w.n_kv) / t_used, "host": host_cpu(),
             "all_cores": cpu_baseline_all_cores(w, cpu, budget_s / 2)}
 
 
@@ -585,6 +607,7 @@ def run_reference(args, w: workloads.Workload, rank: int, world: int) -> Optiona
                    "storage_dtype": w.dtype, "sample_tokens_per_step": n_tok},
         "heads_per_s": n_tok * (w.n_qo + w.n_kv) * args.steps / secs,
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "host": host_cpu(),
                          "sample": f"{n_tok} consecutive tokens of {w.name} per step, in blocks of "
                                    f"{block} over {cores} threads"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
