@@ -953,6 +953,10 @@ int apply_host_impl(const Call &dc, void *h_q, void *h_k, const void *h_pos, lon
             return fail(QKNR_ERR_INVALID_ARG,
                         "QKNR_HOST_DIRECT: h_q, h_k and h_positions must be mapped pinned or managed memory");
     }
+    if (!dc.q || !dc.k || !dc.positions)
+        return fail(QKNR_ERR_INVALID_ARG,
+                    "the host buffers are not all device-mapped (pinned or managed memory), so the staged mode "
+                    "runs and needs d_q, d_k and d_positions");
     rc = validate(dc);  // staged: the device staging buffers
     if (rc) return rc;
     long long chunk = chunk_tokens;

@@ -171,6 +171,10 @@ def test_host_path_errors(qknr):
                         is_neox=False, chunk_tokens=-1)
     with pytest.raises(qknr.QknrError):     # staged without staging buffers
         qknr.apply_host(h_q, h_k, *args, h_pos, is_neox=False, mode="staged")
+    # pageable host memory in the automatic mode without staging buffers: a clear refusal
+    with pytest.raises(qknr.QknrError, match="staged mode"):
+        qknr.apply_host(cpu["q"].clone(), cpu["k"].clone(), *args, cpu["positions"].clone(),
+                        is_neox=False, mode="auto")
     with pytest.raises(qknr.QknrError):     # host tensor on the device
         qknr.apply_host(dev["q"], h_k, *args, h_pos, dev["q"], dev["k"], dev["positions"],
                         is_neox=False)
