@@ -67,9 +67,10 @@ extern "C" {
 int qknr_init(int device);
 
 /*
- * Release what qknr_init allocated, on every device. Callers must make sure
- * no launch from this library is still running. After it, qknr_init must be
- * called again before any apply.
+ * Release what qknr_init allocated, and the streams and events of the
+ * host-buffer pipeline (qknr_apply_host), on every device. Callers must make
+ * sure no launch from this library is still running. After it, qknr_init
+ * must be called again before any apply.
  */
 int qknr_shutdown(void);
 

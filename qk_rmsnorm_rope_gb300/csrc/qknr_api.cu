@@ -49,7 +49,7 @@ using qknr::BulkParams;
 using qknr::Params;
 
 constexpr int kMaxDevices = 64;
-constexpr int kVersion = 10100;             // 1.1.0
+constexpr int kVersion = 10200;             // 1.2.0: host buffers, separate head strides, head_dim 80
 constexpr int kStatusWords = 3;             // {bad-token count, first bad token, watchdog bits}
 constexpr int kMaxBulkSmem = 232448;        // dynamic shared memory per CTA on sm_100/sm_103 (227 KB)
 constexpr int kDefaultTileBytes = 24576;    // bulk kernel: max bytes of heads per tile
