@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     }
 
     // (token, chunk) of the current item, advanced incrementally: no 64-bit
-    // division per item (each one costs dozens of instructions, and the
-    // kernel is close to instruction-issue bound)
+    // division per item (each one costs dozens of instructions, and a warp
+    // runs its items back to back, so every instruction per item shows)
     const int chunks = p.chunks_per_token;
     long long t = it_begin / chunks;
     int ch = static_cast<int>(it_begin - t * chunks);
