@@ -159,6 +159,36 @@ def test_host_path_pageable_memory(qknr):
     assert torch.equal(h_k.view(torch.int16), ref["k"].cpu().view(torch.int16))
 
 
+def test_host_path_registered_memory(qknr):
+    """Pageable buffers registered with cudaHostRegister (mapped) run in the
+    direct mode: the staging buffers stay untouched and the bits match."""
+    w = workloads.scaled(workloads.get("mha_neox"), 90, cache_len=4096)
+    cpu = workloads.make_inputs(w)
+    ref = workloads.to_device(cpu, w, "cuda")
+    qknr.apply(ref["q"], ref["k"], ref["q_w"], ref["k_w"], ref["cos_sin_cache"], ref["positions"],
+               is_neox=w.is_neox, eps=w.eps)
+    h_q, h_k, h_pos = cpu["q"].clone(), cpu["k"].clone(), cpu["positions"].clone()
+    cudart = torch.cuda.cudart()
+    regs = []
+    try:
+        for t in (h_q, h_k, h_pos):
+            rc = cudart.cudaHostRegister(t.data_ptr(), t.numel() * t.element_size(), 2)  # mapped
+            assert int(rc) == 0, rc
+            regs.append(t)
+        d_q, d_k = _staging(h_q), _staging(h_k)
+        d_pos = torch.empty_like(h_pos, device="cuda")
+        dev = workloads.to_device(cpu, w, "cuda")
+        qknr.apply_host(h_q, h_k, dev["q_w"], dev["k_w"], dev["cos_sin_cache"], h_pos, d_q, d_k,
+                        d_pos, is_neox=w.is_neox, eps=w.eps, mode="auto")
+        torch.cuda.synchronize()
+        assert torch.equal(h_q.view(torch.int16), ref["q"].cpu().view(torch.int16))
+        assert torch.equal(h_k.view(torch.int16), ref["k"].cpu().view(torch.int16))
+        assert torch.isnan(d_q.float()).all()      # direct: staging untouched
+    finally:
+        for t in regs:
+            cudart.cudaHostUnregister(t.data_ptr())
+
+
 def test_host_path_errors(qknr):
     w = workloads.scaled(workloads.get("tiny"), 8)
     cpu = workloads.make_inputs(w)
