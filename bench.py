@@ -12,9 +12,19 @@ bytes = read + write of every Q/K head, one fp32 cos|sin row and one position
 per token, and the two weight vectors; also heads/s and the fraction of the
 measured HBM copy bandwidth.
 
+The line also carries: the roofline object (ncu DRAM traffic from profiles/
+while its source hash matches), SM clocks sampled during the timed region,
+the spread of the time per step over ten segments, the end-to-end leg
+through qknr_apply_host from pinned host memory (direct mode; staged mode
+beside it), and the CPU baseline: the oracle on one core and on every core.
+
 --impl reference times the double-precision CPU oracle (the reference
-implementation here: there is no runnable upstream code) on the host cores,
+implementation here: there is no runnable upstream code) on every host core,
 each step a bounded sample of tokens of the same workload.
+
+Other options: --tokens N (decode-sized calls), --graph (replays of a CUDA
+graph of calls), --variant unfused (the two-kernel chain), --ceiling (torch's
+own in-place elementwise kernel at the same bytes).
 """
 from __future__ import annotations
 
