@@ -224,3 +224,64 @@ def test_host_path_errors(qknr):
                                 h_pos.data_ptr(), dev["q"].data_ptr(), dev["k"].data_ptr(),
                                 dev["positions"].data_ptr(), 0, 4, 4, 64, 64, 0, 256, 256, 64,
                                 1e-6, 0, 0, 0, None) == 0
+
+
+def test_concurrent_calls_from_threads(qknr):
+    """Four host threads, each on its own stream and buffers, call apply,
+    apply_checked and apply_host (staged and direct) at the same time; every
+    result equals the same call made alone."""
+    import threading
+    cases = [("gqa", 97), ("dit", 60), ("fused_qkv", 33), ("mha_neox", 41)]
+    ws = [workloads.scaled(workloads.get(n), T, cache_len=min(workloads.get(n).cache_len, 4096))
+          for n, T in cases]
+    cpus = [workloads.make_inputs(w) for w in ws]
+    refs = []
+    for w, cpu in zip(ws, cpus):
+        r = workloads.to_device(cpu, w, "cuda")
+        qknr.apply(r["q"], r["k"], r["q_w"], r["k_w"], r["cos_sin_cache"], r["positions"],
+                   is_neox=w.is_neox, eps=w.eps)
+        refs.append((r["q"].cpu(), r["k"].cpu()))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(i):
+        try:
+            w, cpu = ws[i], cpus[i]
+            s = torch.cuda.Stream()
+            for it in range(12):
+                kind = (i + it) % 4
+                dev = workloads.to_device(cpu, w, "cuda")
+                torch.cuda.synchronize()
+                if kind == 0:
+                    qknr.apply(dev["q"], dev["k"], dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
+                               dev["positions"], is_neox=w.is_neox, eps=w.eps, stream=s)
+                    s.synchronize()
+                    got = (dev["q"].cpu(), dev["k"].cpu())
+                elif kind == 1:
+                    qknr.apply_checked(dev["q"], dev["k"], dev["q_w"], dev["k_w"],
+                                       dev["cos_sin_cache"], dev["positions"], is_neox=w.is_neox,
+                                       eps=w.eps, stream=s)
+                    got = (dev["q"].cpu(), dev["k"].cpu())
+                else:
+                    h_q, h_k, _ = _host_inputs(cpu, w, 0)
+                    h_pos = cpu["positions"].clone().pin_memory()
+                    d_q, d_k = _staging(h_q), _staging(h_k)
+                    d_pos = torch.empty_like(h_pos, device="cuda")
+                    qknr.apply_host(h_q, h_k, dev["q_w"], dev["k_w"], dev["cos_sin_cache"], h_pos,
+                                    d_q, d_k, d_pos, is_neox=w.is_neox, eps=w.eps, chunk_tokens=16,
+                                    mode="staged" if kind == 2 else "direct", stream=s)
+                    s.synchronize()
+                    got = (h_q.clone(), h_k.clone())
+                for a, b in zip(got, refs[i]):
+                    if not torch.equal(a.contiguous().view(torch.int16), b.view(torch.int16)):
+                        errors.append((i, it, kind))
+        except Exception as e:   # noqa: BLE001 - reported below
+            errors.append((i, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(ws))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=600)
+    assert not any(t.is_alive() for t in threads)
+    assert not errors, errors[:5]
