@@ -63,3 +63,26 @@ def test_op_matches_direct_call_eager_and_compiled():
     assert torch.equal(cq, ref["q"]) and torch.equal(ck, ref["k"])
     # the compiled function worked on copies: its inputs keep their values
     assert torch.equal(src["q"].cpu(), cpu["q"])
+
+
+@pytest.mark.gpu
+def test_op_takes_model_layout_and_host_positions():
+    """The registered op on [B, S, H, D] q/k and positions given on the host
+    (converted like the reference wrapper does): the bits of the 3-D call."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import qk_rmsnorm_rope_gb300 as q
+    q.init(0)
+    w = workloads.scaled(workloads.get("dit"), 48)
+    cpu = workloads.make_inputs(w)
+    ref = workloads.to_device(cpu, w, "cuda")
+    q.apply(ref["q"], ref["k"], ref["q_w"], ref["k_w"], ref["cos_sin_cache"], ref["positions"],
+            is_neox=False, eps=w.eps)
+    dev = workloads.to_device(cpu, w, "cuda")
+    q4 = dev["q"].view(4, 12, w.n_qo, w.head_dim)
+    k4 = dev["k"].view(4, 12, w.n_kv, w.head_dim)
+    torch.ops.qknr.fused_inplace_qknorm_rope(q4, k4, dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
+                                             cpu["positions"].to(torch.int64), False, w.eps)
+    torch.cuda.synchronize()
+    assert torch.equal(dev["q"].view(torch.int16), ref["q"].view(torch.int16))
+    assert torch.equal(dev["k"].view(torch.int16), ref["k"].view(torch.int16))
