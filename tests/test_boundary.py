@@ -167,3 +167,21 @@ def test_calls_before_init_are_refused():
     first, second = r.stdout.strip().splitlines()[-2:]
     assert first.startswith("1 ") and "qknr_init" in first
     assert second.split() == ["1", "1", "1", "1", "1", "1"]
+
+
+def test_four_d_inputs_view_or_refuse():
+    """[B, S, H, D] tensors become the [B*S, H, D] view of the same memory when
+    B and S merge; otherwise they are refused (a copy would not be in place)."""
+    x = torch.zeros(3, 5, 4, 64, dtype=torch.bfloat16)
+    v = qknr._as_tokens(x, "q")
+    assert v.shape == (15, 4, 64) and v.data_ptr() == x.data_ptr()
+    assert qknr._as_tokens(v, "q") is v                      # 3-D: as it is
+    with pytest.raises(qknr.QknrError, match="merge"):
+        qknr._as_tokens(x.transpose(0, 1), "q")
+
+
+def test_float_positions_refused_before_any_device_work():
+    q = torch.zeros(2, 2, 64, dtype=torch.bfloat16)
+    w = torch.ones(64, dtype=torch.bfloat16)
+    with pytest.raises(qknr.QknrError):
+        qknr.apply(q, q, w, w, torch.zeros(4, 64), torch.zeros(2), is_neox=False)
