@@ -218,7 +218,7 @@ class PreparedCall:
     """One qknr_apply call's arguments, built once (pointers of one replica)."""
 
     def __init__(self, q, dev: Dict[str, torch.Tensor], w: workloads.Workload, stream: int,
-                 entry: str = "qknr_apply"):
+                 entry: str = "qknr_apply", inputs_ready: bool = False):
         T, n_qo, D = dev["q"].shape
         n_kv = dev["k"].shape[1]
         hs = dev["q"].stride(1) if n_qo > 1 else dev["k"].stride(1)
@@ -227,7 +227,8 @@ class PreparedCall:
                      dev["k_w"].data_ptr(), dev["cos_sin_cache"].data_ptr(),
                      dev["positions"].data_ptr(), T, n_qo, n_kv, D, w.rope_dim, int(w.is_neox),
                      dev["q"].stride(0), dev["k"].stride(0), hs, w.eps,
-                     q.dtype_code(dev["q"].dtype, dev["positions"].dtype), stream)
+                     q.dtype_code(dev["q"].dtype, dev["positions"].dtype)
+                     | (q.QKNR_INPUTS_READY if inputs_ready else 0), stream)
         self.q = q
 
     def __call__(self):
@@ -256,7 +257,7 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     reps = [workloads.to_device(cpu, w, device) for _ in range(n_rep)]
     entry = "qknr_apply_unfused" if args.variant == "unfused" else "qknr_apply"
     launches_per_step = 2 if args.variant == "unfused" else 1
-    calls = [PreparedCall(q, r, w, sh, entry) for r in reps]
+    calls = [PreparedCall(q, r, w, sh, entry, args.inputs_ready) for r in reps]
     algo = workloads.algorithmic_bytes(w)
     heads = workloads.num_heads_total(w)
 
@@ -271,7 +272,7 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             cs = torch.cuda.current_stream().cuda_stream
-            gcalls = [PreparedCall(q, r, w, cs, entry) for r in reps]
+            gcalls = [PreparedCall(q, r, w, cs, entry, args.inputs_ready) for r in reps]
             for c in gcalls:
                 c()
         graph.replay()
@@ -349,7 +350,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
                           if n_rep > 1 else "inputs larger than 4x L2"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": (f"CUDA graph of {n_rep} calls, replayed" if args.graph
-                              else "one C-ABI call per step from Python"),
+                              else "one C-ABI call per step from Python")
+                             + (", QKNR_INPUTS_READY" if args.inputs_ready else ""),
                    "work_map": wm},
         "heads_per_s": world * heads * args.steps / secs,
         "pct_of_peak": round(100.0 * achieved / peak, 2),
@@ -677,6 +679,8 @@ def main(argv: Optional[List[str]] = None) -> int:
     ap.add_argument("--ceiling", action="store_true",
                     help="print torch's in-place elementwise and copy throughput at this "
                          "workload's byte count instead (context, not the op)")
+    ap.add_argument("--inputs-ready", action="store_true",
+                    help="pass QKNR_INPUTS_READY (weights and positions not written by the previous kernel)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of a CUDA graph of calls (GPU time per call, no host launch rate)")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],

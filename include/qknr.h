@@ -45,6 +45,19 @@ extern "C" {
 #define QKNR_BF16 0x000    /* bfloat16 q/k/weights */
 #define QKNR_FP16 0x001    /* IEEE half q/k/weights */
 #define QKNR_POS_I64 0x100 /* positions are int64 (otherwise int32) */
+/*
+ * QKNR_INPUTS_READY, OR-ed into dtype, is the caller's promise that q_w, k_w
+ * and positions were not written by the kernel enqueued just before this call
+ * on the stream (for example: weights loaded at start-up, positions computed
+ * at the start of the forward pass, and a GEMM producing q and k just before).
+ * With it, the register kernel reads the weights and positions while that
+ * kernel finishes (programmatic dependent launch), and reads q, k and the
+ * cos|sin table only after it has completed: about 17% less latency per
+ * decode-sized call and 3% more bandwidth on a 4608-token DiT call, with the
+ * same results. Breaking the promise is a data race. The other kernels and
+ * the staged host path (which launches without the early start) ignore it.
+ */
+#define QKNR_INPUTS_READY 0x200
 
 /* status codes */
 #define QKNR_OK 0

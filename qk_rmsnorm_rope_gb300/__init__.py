@@ -17,7 +17,7 @@ import os
 from typing import Dict, Optional
 
 __all__ = [
-    "QKNR_BF16", "QKNR_FP16", "QKNR_POS_I64", "QKNR_HOST_AUTO", "QKNR_HOST_STAGED",
+    "QKNR_BF16", "QKNR_FP16", "QKNR_POS_I64", "QKNR_INPUTS_READY", "QKNR_HOST_AUTO", "QKNR_HOST_STAGED",
     "QKNR_HOST_DIRECT", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
     "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
@@ -30,6 +30,7 @@ __all__ = [
 QKNR_BF16 = 0x000
 QKNR_FP16 = 0x001
 QKNR_POS_I64 = 0x100
+QKNR_INPUTS_READY = 0x200   # caller's promise: weights and positions are not written by the kernel just before
 
 STATUS_NAMES = {
     0: "QKNR_OK", 1: "QKNR_ERR_NOT_INITIALIZED", 2: "QKNR_ERR_INVALID_ARG",
@@ -325,7 +326,7 @@ def _prepare(q, positions, stream):
 
 
 def apply(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float = 1e-6,
-          head_dim: int = 0, rope_dim: int = 0, stream=None) -> None:
+          head_dim: int = 0, rope_dim: int = 0, stream=None, inputs_ready: bool = False) -> None:
     """In-place fused QK RMSNorm + RoPE on torch CUDA tensors (returns None).
 
     q [T, n_qo, D] and k [T, n_kv, D] (bf16/fp16, unit innermost stride; or
@@ -334,12 +335,17 @@ def apply(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, eps: float
     default torch's current stream on q's device. q and k may have different
     head strides (qknr_apply_strided); with one shared stride this is
     qknr_apply. Positions may be any integer tensor (see _prepare).
+    ``inputs_ready=True`` is the caller's promise that q_w, k_w and positions
+    were not written by the kernel enqueued just before on the stream
+    (QKNR_INPUTS_READY): the kernel then reads them while that kernel finishes.
     """
     import torch
     q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
     positions, stream = _prepare(q, positions, stream)
     T, n_qo, n_kv, D, R, qs, ks, hs, code, khs = _marshal(
         q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim, split_strides=True)
+    if inputs_ready:
+        code |= QKNR_INPUTS_READY
     with torch.cuda.device(q.device):
         if khs == hs:
             _check(qknr_apply(q.data_ptr(), k.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),

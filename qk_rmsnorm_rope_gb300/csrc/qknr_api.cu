@@ -162,7 +162,7 @@ struct DeviceState {
     unsigned long long *status_host = nullptr;  // pinned host copy (qknr_init) or nullptr
     std::mutex checked_mu;                      // serialises status read-backs on this device
     // resident CTAs per SM for the register kernel, by (dtype, pos64, d_idx, mode, u_idx, threads class)
-    std::atomic<int> occupancy[2][2][qknr::kNumHeadDim][2][qknr::kNumUnroll][4];
+    std::atomic<int> occupancy[2][2][2][qknr::kNumHeadDim][2][qknr::kNumUnroll][4];  // [early][dt]...
     // bulk kernels whose dynamic shared-memory limit was raised, by (dtype, pos64, d_idx, mode)
     std::atomic<bool> bulk_attr[2][2][qknr::kNumHeadDim][2];
     // resident CTAs per SM of the unfused-baseline kernels, by (dtype, op-1, pos64, d_idx, mode)
@@ -265,10 +265,10 @@ int persistent_grid(long long items, int threads, int ctas_per_sm, int sm_count)
     return static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(ctas_per_sm) * sm_count)));
 }
 
-int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u_idx, int threads,
+int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u_idx, int threads, int early,
                   const void *kernel, int *out) {
-    return cached_occupancy(st.occupancy[dt][pos64][d_idx][mode][u_idx][threads_index(threads)], kernel, threads,
-                            "cudaOccupancyMaxActiveBlocksPerMultiprocessor(register)", out);
+    return cached_occupancy(st.occupancy[early][dt][pos64][d_idx][mode][u_idx][threads_index(threads)], kernel,
+                            threads, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(register)", out);
 }
 
 // Register kernel: items are (token, chunk of warp passes); the default is the
@@ -297,11 +297,14 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
     const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
     const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
-    wm->kernel = dt ? qknr::kernel_fp16(pos64, d_idx, mode, wm->u_idx)
-                    : qknr::kernel_bf16(pos64, d_idx, mode, wm->u_idx);
+    const int early = (c.dtype & QKNR_INPUTS_READY) ? 1 : 0;
+    wm->kernel = early ? (dt ? qknr::kernel_fp16_early(pos64, d_idx, mode, wm->u_idx)
+                             : qknr::kernel_bf16_early(pos64, d_idx, mode, wm->u_idx))
+                       : (dt ? qknr::kernel_fp16(pos64, d_idx, mode, wm->u_idx)
+                             : qknr::kernel_bf16(pos64, d_idx, mode, wm->u_idx));
     if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no kernel for this shape");
     int occ = 0;
-    int rc = resident_ctas(st, dt, pos64, d_idx, mode, wm->u_idx, threads, wm->kernel, &occ);
+    int rc = resident_ctas(st, dt, pos64, d_idx, mode, wm->u_idx, threads, early, wm->kernel, &occ);
     if (rc) return rc;
     const int force = tune(QKNR_TUNE_CTAS_PER_SM);
     if (force > 0) occ = std::min(occ, force);
@@ -522,8 +525,10 @@ long long row_bytes(int n, long long head_stride_b, int head_dim) {
 
 int validate(const Call &c) {
     const int dtype = c.dtype;
-    if ((dtype & ~(0xff | QKNR_POS_I64)) != 0 || ((dtype & 0xff) != QKNR_BF16 && (dtype & 0xff) != QKNR_FP16))
-        return fail(QKNR_ERR_INVALID_ARG, "dtype 0x%x is not QKNR_BF16/QKNR_FP16 [| QKNR_POS_I64]", dtype);
+    if ((dtype & ~(0xff | QKNR_POS_I64 | QKNR_INPUTS_READY)) != 0 ||
+        ((dtype & 0xff) != QKNR_BF16 && (dtype & 0xff) != QKNR_FP16))
+        return fail(QKNR_ERR_INVALID_ARG,
+                    "dtype 0x%x is not QKNR_BF16/QKNR_FP16 [| QKNR_POS_I64] [| QKNR_INPUTS_READY]", dtype);
     if (c.num_tokens < 0) return fail(QKNR_ERR_INVALID_ARG, "num_tokens %lld < 0", c.num_tokens);
     if (c.n_qo < 1 || c.n_kv < 1)
         return fail(QKNR_ERR_INVALID_ARG, "head counts n_qo=%d n_kv=%d must be >= 1", c.n_qo, c.n_kv);
@@ -1096,7 +1101,7 @@ int qknr_version(void) { return kVersion; }
 const char *qknr_last_error(void) { return t_last_error.c_str(); }
 
 int qknr_can_use(int head_dim, int rope_dim, int is_neox, int dtype) {
-    if ((dtype & ~(0xff | QKNR_POS_I64)) != 0) return 0;
+    if ((dtype & ~(0xff | QKNR_POS_I64 | QKNR_INPUTS_READY)) != 0) return 0;
     if ((dtype & 0xff) != QKNR_BF16 && (dtype & 0xff) != QKNR_FP16) return 0;
     return shape_ok(head_dim, rope_dim, is_neox) ? 1 : 0;
 }
@@ -1123,12 +1128,13 @@ int qknr_init(int device) {
         rc = fail_cuda(e, "cudaMallocHost(status)");
     if (!rc && (e = cudaMemset(st.status, 0, words)) != cudaSuccess) rc = fail_cuda(e, "cudaMemset(status)");
     if (!rc) {
-        for (auto &a : st.occupancy)
-            for (auto &b : a)
-                for (auto &c : b)
-                    for (auto &d : c)
-                        for (auto &u : d)
-                            for (auto &x : u) x.store(0);
+        for (auto &e : st.occupancy)
+            for (auto &a : e)
+                for (auto &b : a)
+                    for (auto &c : b)
+                        for (auto &d : c)
+                            for (auto &u : d)
+                                for (auto &x : u) x.store(0);
         st.ready.store(true, std::memory_order_release);
     } else {
         if (st.status) cudaFree(st.status);

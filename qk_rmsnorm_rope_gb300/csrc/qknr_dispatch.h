@@ -16,6 +16,10 @@ constexpr int kHeadDims[kNumHeadDim] = {64, 96, 128, 192, 256, 80};
 // nullptr. Defined in qknr_inst_bf16.cu / qknr_inst_fp16.cu.
 const void *kernel_bf16(int pos64, int d_idx, int mode, int u_idx);
 const void *kernel_fp16(int pos64, int d_idx, int mode, int u_idx);
+// The same with the weights and positions read before waiting for the previous
+// grid (QKNR_INPUTS_READY). Defined in qknr_inst_{bf16,fp16}_early.cu.
+const void *kernel_bf16_early(int pos64, int d_idx, int mode, int u_idx);
+const void *kernel_fp16_early(int pos64, int d_idx, int mode, int u_idx);
 
 // Bulk-copy ring kernel entry for (position type, head_dim class, mode).
 const void *bulk_kernel_bf16(int pos64, int d_idx, int mode);

@@ -4,41 +4,10 @@
 #include "qknr_bulk_kernel.cuh"
 #include "qknr_kernel.cuh"
 #include "qknr_lean_kernel.cuh"
+#include "qknr_register_table.cuh"
 
 namespace qknr {
 namespace {
-
-template <class P, int D, int MODE, int U>
-const void *entry() {
-    return reinterpret_cast<const void *>(&qknr_fused_kernel<__nv_bfloat16, P, D, MODE, U>);
-}
-
-template <class P, int D, int MODE>
-const void *by_unroll(int u_idx) {
-    switch (u_idx) {
-        case 0: return entry<P, D, MODE, 2>();
-        case 1: return entry<P, D, MODE, 4>();
-        default: return nullptr;
-    }
-}
-
-template <class P, int D>
-const void *by_mode(int mode, int u_idx) {
-    return mode == kNeox ? by_unroll<P, D, kNeox>(u_idx) : by_unroll<P, D, kInterleaved>(u_idx);
-}
-
-template <class P>
-const void *by_head_dim(int d_idx, int mode, int u_idx) {
-    switch (d_idx) {
-        case 0: return by_mode<P, 64>(mode, u_idx);
-        case 1: return by_mode<P, 96>(mode, u_idx);
-        case 2: return by_mode<P, 128>(mode, u_idx);
-        case 3: return by_mode<P, 192>(mode, u_idx);
-        case 4: return by_mode<P, 256>(mode, u_idx);
-        case 5: return by_mode<P, 80>(mode, u_idx);
-        default: return nullptr;
-    }
-}
 
 template <class P, int D>
 const void *bulk_by_mode(int mode) {
@@ -128,7 +97,7 @@ const void *bulk_kernel_bf16(int pos64, int d_idx, int mode) {
 }
 
 const void *kernel_bf16(int pos64, int d_idx, int mode, int u_idx) {
-    return pos64 ? by_head_dim<long long>(d_idx, mode, u_idx) : by_head_dim<int>(d_idx, mode, u_idx);
+    return RegisterTable<__nv_bfloat16, false>::get(pos64, d_idx, mode, u_idx);
 }
 
 }  // namespace qknr

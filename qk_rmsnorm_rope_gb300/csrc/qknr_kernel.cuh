@@ -71,8 +71,11 @@ __device__ __forceinline__ long long load_position(const void *positions, long l
 
 // T: storage type (bf16/half); P: position type (int / long long);
 // D: head_dim; MODE: pairing; UMAX: max warp passes per item (loads in flight);
-// OP: fused (the product) or one step of the unfused baseline.
-template <class T, class P, int D, int MODE, int UMAX, int OP = kOpFused>
+// OP: fused (the product) or one step of the unfused baseline;
+// EARLY: the caller has promised that the weights and positions were not
+// written by the grid this launch depends on (QKNR_INPUTS_READY), so they are
+// read before waiting for that grid.
+template <class T, class P, int D, int MODE, int UMAX, int OP = kOpFused, bool EARLY = false>
 __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__ Params p) {
     // A head's data takes NVH lanes (two 16-byte vectors each); its lane group
     // is LPH lanes, NVH rounded up to a power of two (head_dim 80, 96 and 192 leave
@@ -85,8 +88,10 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 900)
     // Programmatic dependent launch: do not touch memory before the previous
     // grid in the stream has completed; then let the next grid get resident.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");
+    if (!EARLY) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;");
+    }
 #endif
 
     const int lane = threadIdx.x & (kWarp - 1);
@@ -155,6 +160,14 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
         if (it_j < it_end) my_pos = load_position<P>(p.positions, it_j / p.chunks_per_token);
     }
 
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 900)
+    // EARLY: the weights and the first positions are in flight; only q, k and
+    // the cos|sin rows are read after the previous grid has completed
+    if (EARLY) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;");
+    }
+#endif
     // (token, chunk) of the current item, advanced incrementally: no 64-bit
     // division per item (each one costs dozens of instructions, and a warp
     // runs its items back to back, so every instruction per item shows)

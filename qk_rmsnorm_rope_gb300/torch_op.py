@@ -24,14 +24,16 @@ __all__ = ["fused_inplace_qknorm_rope", "can_use_fused_inplace_qknorm_rope"]
 def fused_inplace_qknorm_rope(q: torch.Tensor, k: torch.Tensor, q_weight: torch.Tensor,
                               k_weight: torch.Tensor, cos_sin_cache: torch.Tensor,
                               positions: torch.Tensor, is_neox: bool, eps: float = 1e-6,
-                              head_dim: int = 0, rope_dim: int = 0) -> None:
+                              head_dim: int = 0, rope_dim: int = 0,
+                              inputs_ready: bool = False) -> None:
     apply(q, k, q_weight, k_weight, cos_sin_cache, positions, is_neox=is_neox, eps=eps,
-          head_dim=head_dim, rope_dim=rope_dim)
+          head_dim=head_dim, rope_dim=rope_dim, inputs_ready=inputs_ready)
 
 
 @fused_inplace_qknorm_rope.register_fake
 def _fused_inplace_qknorm_rope_fake(q, k, q_weight, k_weight, cos_sin_cache, positions,
-                                    is_neox, eps=1e-6, head_dim=0, rope_dim=0) -> None:
+                                    is_neox, eps=1e-6, head_dim=0, rope_dim=0,
+                                    inputs_ready=False) -> None:
     return None
 
 

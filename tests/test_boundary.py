@@ -53,6 +53,7 @@ def test_constants_match_header():
     assert c["QKNR_BF16"] == qknr.QKNR_BF16
     assert c["QKNR_FP16"] == qknr.QKNR_FP16
     assert c["QKNR_POS_I64"] == qknr.QKNR_POS_I64
+    assert c["QKNR_INPUTS_READY"] == qknr.QKNR_INPUTS_READY
     for name in ("QKNR_HOST_AUTO", "QKNR_HOST_STAGED", "QKNR_HOST_DIRECT"):
         assert c[name] == getattr(qknr, name)
     for code, name in qknr.STATUS_NAMES.items():
@@ -95,7 +96,8 @@ def test_can_use_rejects():
     assert qknr.qknr_can_use(128, 63, 0, 0) == 0         # odd rope_dim
     assert qknr.qknr_can_use(128, 24, 1, 0) == 0         # NeoX half crosses 16-byte vectors
     assert qknr.qknr_can_use(128, 64, 0, 2) == 0         # unknown element type
-    assert qknr.qknr_can_use(128, 64, 0, 0x200) == 0     # unknown flag
+    assert qknr.qknr_can_use(128, 64, 0, 0x400) == 0     # unknown flag
+    assert qknr.qknr_can_use(128, 64, 0, qknr.QKNR_INPUTS_READY) == 1
     assert qknr.qknr_can_use(128, 8, 1, 0) == 1
     assert qknr.qknr_can_use(64, 2, 0, 0) == 1
 

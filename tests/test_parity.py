@@ -633,6 +633,58 @@ def test_watchdog_runs_out_and_recovers(qknr):
     _check_workload(qknr, w)
 
 
+INPUTS_READY_CASES = [("tiny", 16, {}), ("dit", 300, {}), ("mha_neox", 257, {}), ("gqa", 513, {}),
+                      ("fused_qkv", 129, {}), ("gqa", 40, {"passes": 1}), ("dit", 77, {"threads": 512}),
+                      ("mha_neox", 33, {"passes": 2, "threads": 64})]
+
+
+@pytest.mark.parametrize("name,T,tune", INPUTS_READY_CASES,
+                         ids=[f"{c[0]}-T{c[1]}-{c[2]}" for c in INPUTS_READY_CASES])
+def test_inputs_ready_same_bits_and_ordering(qknr, name, T, tune):
+    """QKNR_INPUTS_READY only moves the weight and position reads before the
+    wait for the previous kernel: the same bits as without it, also when the
+    previous kernel wrote q and k (two calls in a row on the same tensors, so
+    the second reads what the first wrote), and under graph capture."""
+    base = workloads.get(name)
+    w = workloads.scaled(base, T, cache_len=min(base.cache_len, 4096))
+    cpu = workloads.make_inputs(w)
+    qknr.set_tuning(reset=True, **tune)
+    try:
+        ref = workloads.to_device(cpu, w, "cuda")
+        for _ in range(2):
+            qknr.apply(ref["q"], ref["k"], ref["q_w"], ref["k_w"], ref["cos_sin_cache"],
+                       ref["positions"], is_neox=w.is_neox, eps=w.eps)
+        dev = workloads.to_device(cpu, w, "cuda")
+        for _ in range(2):
+            qknr.apply(dev["q"], dev["k"], dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
+                       dev["positions"], is_neox=w.is_neox, eps=w.eps, inputs_ready=True)
+        torch.cuda.synchronize()
+        assert torch.equal(dev["q"].view(torch.int16), ref["q"].view(torch.int16))
+        assert torch.equal(dev["k"].view(torch.int16), ref["k"].view(torch.int16))
+        # captured: two calls in one graph, replayed on fresh values
+        g_dev = workloads.to_device(cpu, w, "cuda")
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            qknr.apply(g_dev["q"], g_dev["k"], g_dev["q_w"], g_dev["k_w"], g_dev["cos_sin_cache"],
+                       g_dev["positions"], is_neox=w.is_neox, eps=w.eps, inputs_ready=True)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(2):
+                qknr.apply(g_dev["q"], g_dev["k"], g_dev["q_w"], g_dev["k_w"], g_dev["cos_sin_cache"],
+                           g_dev["positions"], is_neox=w.is_neox, eps=w.eps, inputs_ready=True)
+        g_dev["q"].copy_(cpu["q"].cuda() if not w.fused_total_heads else cpu["q"].to("cuda"))
+        g_dev["k"].copy_(cpu["k"].cuda() if not w.fused_total_heads else cpu["k"].to("cuda"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(g_dev["q"].view(torch.int16), ref["q"].view(torch.int16))
+        assert torch.equal(g_dev["k"].view(torch.int16), ref["k"].view(torch.int16))
+    finally:
+        qknr.set_tuning(reset=True)
+
+
 def test_extreme_values(qknr):
     """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
