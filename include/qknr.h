@@ -62,7 +62,7 @@ extern "C" {
 /* status codes */
 #define QKNR_OK 0
 #define QKNR_ERR_NOT_INITIALIZED 1 /* qknr_init was not called for the current device */
-#define QKNR_ERR_INVALID_ARG 2     /* null pointer, negative size, overlapping q/k, bad dtype */
+#define QKNR_ERR_INVALID_ARG 2     /* null pointer, negative or oversized size, overlapping q/k, bad dtype */
 #define QKNR_ERR_UNSUPPORTED 3     /* head_dim / rope_dim / pairing outside the accepted set */
 #define QKNR_ERR_MISALIGNED 4      /* pointer or stride breaks the 16-byte vector rule */
 #define QKNR_ERR_CUDA 5            /* a CUDA runtime call failed; message has the CUDA error */
@@ -116,7 +116,8 @@ int qknr_can_use(int head_dim, int rope_dim, int is_neox, int dtype);
  *               A position outside the cache is undefined behaviour here, as
  *               on the page (§4.4); qknr_apply_checked checks them.
  * num_tokens    T >= 0 (0: nothing is launched).
- * n_qo, n_kv    query and key head counts, each >= 1 (GQA: n_qo != n_kv).
+ * n_qo, n_kv    query and key head counts, each >= 1 (GQA: n_qo != n_kv), and
+ *               n_qo + n_kv <= 2^24.
  * head_dim      D; rope_dim R: see qknr_can_use.
  * is_neox       0 = interleaved (GPT-J) pairing, 1 = NeoX pairing.
  * q_stride      elements between consecutive tokens of q; k_stride the same for k.
@@ -129,7 +130,9 @@ int qknr_can_use(int head_dim, int rope_dim, int is_neox, int dtype);
  * Alignment: q, k, q_w, k_w 16-byte aligned; q_stride, k_stride, head_stride
  * multiples of 8 elements; cos_sin_cache 4-byte aligned; positions aligned to
  * their size. q and k must not overlap (disjoint views of one fused QKV buffer
- * are fine). The caller owns every buffer; nothing is retained after return.
+ * are fine). Neither q nor k may span more than 2^56 bytes, and no size or
+ * stride may exceed 2^56 (QKNR_ERR_INVALID_ARG), so that no byte offset can
+ * wrap. The caller owns every buffer; nothing is retained after return.
  */
 int qknr_apply(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
                const void *positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim,

@@ -54,6 +54,8 @@ constexpr int kStatusWords = 3;             // {bad-token count, first bad token
 constexpr int kMaxBulkSmem = 232448;        // dynamic shared memory per CTA on sm_100/sm_103 (227 KB)
 constexpr int kDefaultTileBytes = 24576;    // bulk kernel: max bytes of heads per tile
 constexpr int kMaxStages = 32;
+constexpr int kMaxHeads = 1 << 24;                // largest n_qo + n_kv accepted
+constexpr long long kMaxExtentBytes = 1LL << 56;  // largest q or k extent accepted (far above any GPU's memory)
 
 thread_local std::string t_last_error;
 
@@ -532,6 +534,9 @@ int validate(const Call &c) {
     if (c.num_tokens < 0) return fail(QKNR_ERR_INVALID_ARG, "num_tokens %lld < 0", c.num_tokens);
     if (c.n_qo < 1 || c.n_kv < 1)
         return fail(QKNR_ERR_INVALID_ARG, "head counts n_qo=%d n_kv=%d must be >= 1", c.n_qo, c.n_kv);
+    if (static_cast<long long>(c.n_qo) + c.n_kv > kMaxHeads)  // the kernels count a token's heads in an int
+        return fail(QKNR_ERR_INVALID_ARG, "n_qo + n_kv = %lld exceeds %d heads per token",
+                    static_cast<long long>(c.n_qo) + c.n_kv, kMaxHeads);
     if (!shape_ok(c.head_dim, c.rope_dim, c.is_neox))
         return fail(QKNR_ERR_UNSUPPORTED,
                     "unsupported head_dim=%d rope_dim=%d is_neox=%d (head_dim in {64,80,96,128,192,256}; rope_dim even, "
@@ -542,6 +547,19 @@ int validate(const Call &c) {
         return fail(QKNR_ERR_INVALID_ARG, "null pointer argument");
     const long long k_hs = c.k_head_stride < 0 ? c.head_stride : c.k_head_stride;
     if (c.q_stride < 0 || c.k_stride < 0 || c.head_stride < 0) return fail(QKNR_ERR_INVALID_ARG, "negative stride");
+    // Every byte offset below (and in the kernels) is a signed 64-bit value.
+    // Bound each tensor's extent first, in 128-bit arithmetic, so that none of
+    // them can wrap, whatever sizes a caller passes.
+    {
+        using wide = __int128;
+        const wide last = c.num_tokens > 0 ? c.num_tokens - 1 : 0;
+        const wide q_ext = last * c.q_stride * 2 + static_cast<wide>(c.n_qo - 1) * c.head_stride * 2 + 2 * c.head_dim;
+        const wide k_ext = last * c.k_stride * 2 + static_cast<wide>(c.n_kv - 1) * k_hs * 2 + 2 * c.head_dim;
+        const wide limit = kMaxExtentBytes;
+        if (q_ext > limit || k_ext > limit || c.q_stride > kMaxExtentBytes || c.k_stride > kMaxExtentBytes ||
+            c.head_stride > kMaxExtentBytes || k_hs > kMaxExtentBytes || c.num_tokens > kMaxExtentBytes)
+            return fail(QKNR_ERR_INVALID_ARG, "q or k would span more than 2^56 bytes (sizes or strides out of range)");
+    }
     if ((c.n_qo > 1 && c.head_stride < c.head_dim) || (c.n_kv > 1 && k_hs < c.head_dim))
         return fail(QKNR_ERR_INVALID_ARG, "head stride %lld < head_dim %d: heads overlap",
                     c.n_qo > 1 && c.head_stride < c.head_dim ? c.head_stride : k_hs, c.head_dim);
@@ -1289,7 +1307,9 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     if (!out) return fail(QKNR_ERR_INVALID_ARG, "out is null");
     DeviceState *st = current_state();
     if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
-    if (num_tokens < 0 || n_qo < 1 || n_kv < 1) return fail(QKNR_ERR_INVALID_ARG, "bad sizes");
+    if (num_tokens < 0 || n_qo < 1 || n_kv < 1 || num_tokens > kMaxExtentBytes ||
+        static_cast<long long>(n_qo) + n_kv > kMaxHeads)
+        return fail(QKNR_ERR_INVALID_ARG, "bad sizes");
     if (!qknr_can_use(head_dim, rope_dim, is_neox, dtype))
         return fail(QKNR_ERR_UNSUPPORTED, "shape outside the accepted set");
     // the plan depends on the table only through its alignment: use an aligned stand-in

@@ -739,6 +739,15 @@ def test_empty_and_errors_leave_inputs_untouched(qknr):
     assert qknr.qknr_apply(0, kp, *common, 16, 2, 2, 128, 64, 0, 256, 256, 128, 1e-6, 0, s) == 2
     assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 128, 64, 0, 256, 256, 128, -1.0, 0, s) == 2
     assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 128, 64, 0, 256, 256, 128, 1e-6, 7, s) == 2
+    # sizes whose byte extents would wrap a signed 64-bit offset
+    assert qknr.qknr_apply(qp, kp, *common, 2 ** 62, 2, 2, 128, 64, 0, 256, 256, 128, 1e-6, 0, s) == 2
+    assert qknr.qknr_apply(qp, kp, *common, 16, 2, 2, 128, 64, 0, 2 ** 62, 256, 128, 1e-6, 0, s) == 2
+    assert qknr.qknr_apply(qp, kp, *common, 1, 2, 2, 128, 64, 0, 256, 2 ** 63 - 8, 128, 1e-6, 0, s) == 2
+    assert qknr.qknr_apply(qp, kp, *common, 16, 2 ** 20, 2, 128, 64, 0, 256, 256, 2 ** 40, 1e-6, 0, s) == 2
+    assert "2^56" in qknr.qknr_last_error()
+    assert qknr.qknr_apply(qp, kp, *common, 1, 2 ** 31 - 1, 2 ** 31 - 1, 128, 64, 0, 256, 256, 128, 1e-6, 0,
+                           s) == 2
+    assert "heads per token" in qknr.qknr_last_error()
     torch.cuda.synchronize()
     assert torch.equal(dev["q"], before_q) and torch.equal(dev["k"], before_k)
 
