@@ -488,8 +488,8 @@ def _random_case(g):
 def test_random_configurations(qknr, case):
     """Seeded random configurations: head_dim, rope_dim, pairing, dtype,
     position type, GQA head counts, padded head and token strides, kernel and
-    launch tuning together. Against the oracle, and bit for bit against the
-    automatic launch on a contiguous copy."""
+    launch tuning, and the early-read flag together. Against the oracle, and
+    bit for bit against the automatic launch on a contiguous copy."""
     g = np.random.default_rng(1000 + case)
     c = _random_case(g)
     w = _make(c["D"], c["R"], c["neox"], c["pos"], c["T"], c["n_qo"], c["n_kv"], dtype=c["dtype"],
@@ -516,10 +516,14 @@ def test_random_configurations(qknr, case):
         tune["passes"] = c["passes"]
     if c["threads"] and kernel in (1, 3, 4):
         tune["threads"] = c["threads"] if kernel == 1 else min(c["threads"], 256)
+    # half of the cases take the early-read instantiations (a draw of its own,
+    # so that the configurations above stay what they were)
+    ready = bool(np.random.default_rng(5000 + case).random() < 0.5)
+    c["inputs_ready"] = ready
     qknr.set_tuning(reset=True, **tune)
     try:
         qknr.apply(dq, dk, dev["q_w"], dev["k_w"], dev["cos_sin_cache"], dev["positions"],
-                   is_neox=w.is_neox, eps=w.eps)
+                   is_neox=w.is_neox, eps=w.eps, inputs_ready=ready)
         torch.cuda.synchronize()
     finally:
         qknr.set_tuning(reset=True)
