@@ -60,7 +60,8 @@ struct Params {
     int cache_vec;                // 1: cos/sin rows may be read as float4
     int interleave;               // 1: warp w takes items w, w + W, ... (W warps); 0: a contiguous range
     float eps;
-    float inv_d;                  // 1 / head_dim (exact: head_dim is a power of two)
+    float inv_d;                  // 1 / head_dim in fp32 (exact for 64, 128 and 256; for 80, 96 and 192
+                                  // the rounded reciprocal moves the mean by at most about one ulp)
     short pass_bound[kBoundTable + 1];  // first pass of chunk c, c <= chunks_per_token <= kBoundTable
 };
 
