@@ -701,6 +701,31 @@ def test_extreme_values(qknr):
         _check_workload_inputs(qknr, w, cpu)
 
 
+def test_fp16_store_overflow_rounds_to_inf(qknr):
+    """Weights of 3e4 on every fourth dim push some outputs past fp16's range.
+    Rounding to nearest even sends every value at or beyond 65520 to +-inf, so
+    those elements must be infinite with the oracle's sign. Values below 65504
+    keep the usual tolerance; the few in between may end as 65504 or inf."""
+    w = _make(128, 128, False, "i32", 24, 2, 2, dtype="fp16", seed=11)
+    cpu = workloads.make_inputs(w)
+    weight = torch.ones(128, dtype=torch.float16)
+    weight[::4] = 3.0e4
+    cpu["q_w"], cpu["k_w"] = weight.clone(), weight.clone()
+    eq, ek = _expected(cpu, w)
+    dev = workloads.to_device(cpu, w, "cuda")
+    _run_gpu(qknr, dev, w)
+    torch.cuda.synchronize()
+    for name, got, exp in (("q", dev["q"], eq), ("k", dev["k"], ek)):
+        g = got.double().cpu().numpy()
+        over = np.abs(exp) > 65520.0 * (1 + 1e-5)
+        under = np.abs(exp) < 65504.0
+        mid = ~(over | under)
+        assert over.sum() > 10 and under.sum() > 1000, (name, over.sum(), under.sum())
+        assert np.all(np.isinf(g[over])) and np.all(np.sign(g[over]) == np.sign(exp[over])), name
+        _assert_close(g[under], exp[under], w.torch_dtype, f"{name} in range")
+        assert np.all((np.abs(g[mid]) == 65504.0) | np.isinf(g[mid])), name
+
+
 def _check_workload_inputs(q, w, cpu):
     eq, ek = _expected(cpu, w)
     dev = workloads.to_device(cpu, w, "cuda")
