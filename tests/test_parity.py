@@ -690,9 +690,10 @@ def test_inputs_ready_same_bits_and_ordering(qknr, name, T, tune):
 
 
 def test_extreme_values(qknr):
-    """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads."""
+    """Zero heads, tiny and large magnitudes, eps = 0 on non-zero heads, and
+    fp16 subnormal inputs (scale 1e-6) that eps = 0 normalises to order one."""
     for dtype, scale, eps in (("bf16", 1e-20, 1e-6), ("bf16", 1e15, 1e-6), ("fp16", 3e3, 1e-6),
-                              ("fp16", 1e-3, 0.0), ("bf16", 1.0, 0.0)):
+                              ("fp16", 1e-3, 0.0), ("bf16", 1.0, 0.0), ("fp16", 1e-6, 0.0)):
         w = _make(128, 128, False, "i32", 50, 3, 2, dtype=dtype, seed=9, x_scale=scale, eps=eps)
         cpu = workloads.make_inputs(w)
         cpu["q"][3].zero_()
