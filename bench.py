@@ -23,8 +23,9 @@ implementation here: there is no runnable upstream code) on every host core,
 each step a bounded sample of tokens of the same workload.
 
 Other options: --tokens N (decode-sized calls), --graph (replays of a CUDA
-graph of calls), --variant unfused (the two-kernel chain), --ceiling (torch's
-own in-place elementwise kernel at the same bytes).
+graph of calls), --inputs-ready (calls that set QKNR_INPUTS_READY), --variant
+unfused (the two-kernel chain), --ceiling (torch's own in-place elementwise
+kernel at the same bytes).
 """
 from __future__ import annotations
 
