@@ -395,6 +395,8 @@ def apply_host(h_q, h_k, q_w, k_w, cos_sin_cache, h_positions, d_q=None, d_k=Non
                rope_dim: int = 0, chunk_tokens: int = 0, mode: str = "auto", stream=None) -> None:
     """The op on host tensors h_q, h_k, h_positions, written back into h_q and
     h_k (see qknr_apply_host). q_w, k_w and cos_sin_cache are device tensors.
+    As in ``apply``, q and k may be [B, S, H, D] when B and S merge into one
+    token dim without a copy (positions then [B*S]).
     ``mode``: "direct" (the kernel works on pinned, device-mapped host memory
     in place), "staged" (chunked copies through the device tensors d_q, d_k,
     d_positions of the same shapes and strides) or "auto" (direct when
@@ -403,6 +405,9 @@ def apply_host(h_q, h_k, q_w, k_w, cos_sin_cache, h_positions, d_q=None, d_k=Non
     import torch
     if mode not in HOST_MODES:
         raise QknrError(2, f"mode must be one of {sorted(HOST_MODES)}")
+    h_q, h_k = _as_tokens(h_q, "h_q"), _as_tokens(h_k, "h_k")
+    d_q = _as_tokens(d_q, "d_q") if d_q is not None else None
+    d_k = _as_tokens(d_k, "d_k") if d_k is not None else None
     for name, h in (("q", h_q), ("k", h_k), ("positions", h_positions)):
         if h.device.type != "cpu":
             raise QknrError(2, f"h_{name} must be a host (CPU) tensor")

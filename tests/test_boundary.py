@@ -180,6 +180,12 @@ def test_four_d_inputs_view_or_refuse():
     assert qknr._as_tokens(v, "q") is v                      # 3-D: as it is
     with pytest.raises(qknr.QknrError, match="merge"):
         qknr._as_tokens(x.transpose(0, 1), "q")
+    # the host-buffer entry point takes the same path, before any device work
+    w_ = torch.ones(64, dtype=torch.bfloat16)
+    cache = torch.zeros(8, 64)
+    with pytest.raises(qknr.QknrError, match="merge"):
+        qknr.apply_host(x.transpose(0, 1), x.transpose(0, 1), w_, w_, cache,
+                        torch.zeros(15, dtype=torch.int32), is_neox=False)
 
 
 def test_float_positions_refused_before_any_device_work():

@@ -136,6 +136,41 @@ def test_host_path_two_calls_and_stream_order(qknr):
         assert torch.equal(hk.view(torch.int16), ref["k"].cpu().view(torch.int16)), mode
 
 
+def test_host_path_four_d_inputs(qknr):
+    """[B, S, H, D] host (and staging) tensors: the same bits as the device call
+    on the [B*S, H, D] layout, in both modes; a 4-D view whose batch and
+    sequence dims do not merge without a copy is refused before any work."""
+    base = workloads.get("gqa")
+    w = workloads.scaled(base, 96, cache_len=min(base.cache_len, 8192))
+    cpu = workloads.make_inputs(w)
+    ref = workloads.to_device(cpu, w, "cuda")
+    qknr.apply(ref["q"], ref["k"], ref["q_w"], ref["k_w"], ref["cos_sin_cache"], ref["positions"],
+               is_neox=w.is_neox, eps=w.eps)
+    torch.cuda.synchronize()
+    dev = workloads.to_device(cpu, w, "cuda")
+    four_d = (lambda t: t.view(4, 24, t.shape[1], t.shape[2]))
+    for mode in ("staged", "direct"):
+        hq = four_d(cpu["q"].clone().pin_memory())
+        hk = four_d(cpu["k"].clone().pin_memory())
+        h_pos = cpu["positions"].clone().pin_memory()
+        staging = ((four_d(torch.empty_like(cpu["q"], device="cuda")),
+                    four_d(torch.empty_like(cpu["k"], device="cuda")),
+                    torch.empty_like(h_pos, device="cuda")) if mode == "staged" else (None, None, None))
+        qknr.apply_host(hq, hk, dev["q_w"], dev["k_w"], dev["cos_sin_cache"], h_pos, *staging,
+                        is_neox=w.is_neox, eps=w.eps, mode=mode)
+        torch.cuda.synchronize()
+        assert torch.equal(hq.reshape(ref["q"].shape).view(torch.int16), ref["q"].cpu().view(torch.int16)), mode
+        assert torch.equal(hk.reshape(ref["k"].shape).view(torch.int16), ref["k"].cpu().view(torch.int16)), mode
+    # [S, B, ...] storage seen as [B, S, ...]: no single token stride, so refused
+    hq = cpu["q"].clone().pin_memory().view(24, 4, w.n_qo, w.head_dim).transpose(0, 1)
+    hk = cpu["k"].clone().pin_memory().view(24, 4, w.n_kv, w.head_dim).transpose(0, 1)
+    before = hq.clone()
+    with pytest.raises(qknr.QknrError):
+        qknr.apply_host(hq, hk, dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
+                        cpu["positions"].clone().pin_memory(), is_neox=w.is_neox, eps=w.eps)
+    assert torch.equal(hq, before)
+
+
 def test_host_path_pageable_memory(qknr):
     """Pageable host memory is not mapped: the automatic mode stages it (and
     gets the same bits), the direct mode refuses it before any launch."""
