@@ -1,26 +1,44 @@
 """Benchmark: fused in-place QK RMSNorm + RoPE on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|NAME] [--impl ours|reference]
 
 One step = one call of the fused op (qknr_apply, one kernel launch) over the
 whole workload with inputs resident in HBM. Between timed steps the call
 rotates over input replicas totalling at least 4x the L2 size, so no step
 finds its inputs in L2. Rank 0 prints one JSON line.
 
+By default every configuration runs (tiny, dit, mha_neox, gqa, fused_qkv),
+one after another on the same GPU, each with its own W warm-up and K timed
+steps. The line's headline is fused_qkv, the largest configuration;
+``per_config`` carries every configuration's value, time per step and its
+spread, roofline, clocks and CPU baseline. ``--workload NAME`` runs one.
+
+Timing: the first warm-up step runs alone, then a synchronize and a barrier;
+the other warm-up steps are enqueued back to back and the timed region's start
+event is recorded right behind them, so the GPU is busy when it starts. K
+steps follow, then an end event, a synchronize and a barrier; the time is the
+maximum over ranks. The spread of the time per step comes from ten
+further runs of K steps behind the timed region when K < 1000, else from
+ten segments of it (an event between two launches costs the second its
+programmatic overlap, so the timed region itself holds only two events).
+
 Metric: effective HBM bandwidth = algorithmic bytes / time, where algorithmic
 bytes = read + write of every Q/K head, one fp32 cos|sin row and one position
 per token, and the two weight vectors; also heads/s and the fraction of the
 measured HBM copy bandwidth.
 
-The line also carries: the roofline object (ncu DRAM traffic from profiles/
-while its source hash matches), SM clocks sampled during the timed region,
-the spread of the time per step over ten segments, the end-to-end leg
-through qknr_apply_host from pinned host memory (direct mode; staged mode
-beside it), and the CPU baseline: the oracle on one core and on every core.
+The line also carries: the roofline object (DRAM read and write bytes of a
+steady-state launch from the ncu summary in profiles/, while its source hash
+matches the kernel's code, beside the algorithmic reads and writes), SM clocks
+sampled around the timed region, the end-to-end leg through qknr_apply_host
+from pinned host memory on the headline configuration (direct mode; staged
+mode beside it), and the CPU baseline: the oracle on one core and on every
+core.
 
 --impl reference times the double-precision CPU oracle (the reference
 implementation here: there is no runnable upstream code) on every host core,
-each step a bounded sample of tokens of the same workload.
+each step a bounded sample of tokens of the same workload (the headline's by
+default), and prints the same config dict as this arm.
 
 Other options: --tokens N (decode-sized calls), --graph (replays of a CUDA
 graph of calls), --inputs-ready (calls that set QKNR_INPUTS_READY), --variant
@@ -51,8 +69,11 @@ import workloads  # noqa: E402
 METRIC = "fused QK-RMSNorm+RoPE effective HBM GB/s (% of GB300 peak) and heads/sec"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_NAMES = {"bulk": "qknr_bulk_kernel", "register": "qknr_fused_kernel",
-                "async": "qknr_async_kernel", "lean": "qknr_lean_kernel"}
+KERNEL_NAMES = {"register": "qknr_fused_kernel"}
+# every configuration of the benchmark, small to large; the headline is the
+# largest one that fits one GPU
+CONFIGS = ["tiny", "dit", "mha_neox", "gqa", "fused_qkv"]
+HEADLINE = "fused_qkv"
 
 
 # ------------------------------------------------------------------ environment
@@ -98,10 +119,6 @@ def measured_peaks() -> Dict:
 # while these are unchanged)
 KERNEL_SOURCES = {
     "qknr_fused_kernel": ["qknr_math.cuh", "qknr_kernel.cuh"],
-    "qknr_bulk_kernel": ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_bulk_kernel.cuh"],
-    "qknr_async_kernel": ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_bulk_kernel.cuh",
-                          "qknr_async_kernel.cuh"],
-    "qknr_lean_kernel": ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_lean_kernel.cuh"],
 }
 
 
@@ -129,9 +146,14 @@ def kernel_source_hash(kernel: str = "qknr_fused_kernel", read=None) -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(kernel: str, workload: str) -> Optional[float]:
+def profiled_traffic(kernel: str, workload: str) -> Optional[Dict[str, float]]:
     """DRAM bytes per launch from the committed ncu summary for this kernel and
-    workload, if it was taken on the current kernel sources; else None."""
+    workload, if it was taken on the current kernel sources; else None.
+
+    The summary gives the steady-state launch: the second of two back-to-back
+    launches captured without cache flushes, so its writes include the lines
+    the launch before it left dirty in L2 (what every launch of the timed loop
+    pays) and miss those it leaves dirty itself."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     try:
         with open(path) as f:
@@ -146,9 +168,11 @@ def profiled_traffic(kernel: str, workload: str) -> Optional[float]:
     if kernel not in KERNEL_SOURCES or fields.get("source_sha256") != kernel_source_hash(kernel):
         return None
     try:
-        return float(fields["traffic_bytes_per_launch"])
+        rd = float(fields["dram_read_bytes_per_launch"])
+        wr = float(fields["dram_write_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+    return {"read": rd, "write": wr, "total": rd + wr}
 
 
 def smi_id(device) -> str:
@@ -238,17 +262,116 @@ class PreparedCall:
             raise self.q.QknrError(rc, self.q.qknr_last_error())
 
 
-def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> Optional[Dict]:
-    import qk_rmsnorm_rope_gb300 as q
+def config_of(w: workloads.Workload) -> Dict:
+    """The workload a line measures: the same dict in both arms."""
+    return {"workload": w.name, "shape": workloads.describe(w), "storage_dtype": w.dtype,
+            "bytes_per_step": workloads.algorithmic_bytes(w),
+            "heads_per_step": workloads.num_heads_total(w)}
 
-    backend = "nccl" if torch.cuda.is_available() else "gloo"
-    dist = init_dist(world, backend)
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    q.init(local)
-    stream = torch.cuda.current_stream(device)
+
+def peak_hbm() -> tuple:
+    peak = measured_peaks().get("hbm_gbs")
+    return (float(peak), "measured") if peak else (FALLBACK_HBM_GBS, "fallback")
+
+
+# An event recorded between two launches costs the second one its
+# programmatic overlap with the first (measured on dit: 21.1 -> 24.6 us per
+# step with an event after every step). So the timed region holds only its
+# two boundary events. The spread of the time per step comes, for K >= this
+# many steps, from ten segments of the timed region (ten events: at most
+# 0.16% of its time); below it, from ten further runs of K steps right
+# behind the timed region, each between two events like the timed one.
+SEGMENTS_FROM = 1000
+SPREAD_RUNS = 10
+
+
+def _spread(per_step: List[float], over: str) -> Dict:
+    per = sorted(per_step)
+    n = len(per)
+    pick = lambda f: per[min(n - 1, int(round(f * (n - 1))))]
+    return {"p10": round(pick(0.1), 6), "p50": round(pick(0.5), 6), "p90": round(pick(0.9), 6),
+            "unit": "ms per step", "over": over}
+
+
+def timed_region(calls, n_rep: int, steps: int, warmup: int, stream, device, dist, graph=None,
+                 replays_per_step: int = 1) -> Dict:
+    """W warm-up steps, then exactly K timed steps, on ``stream``.
+
+    The first warm-up step runs alone (first-use host work), then a full
+    synchronize and a barrier. The other warm-up steps go out back to back
+    and the timed region starts directly behind them on the same stream (its
+    start event is recorded right after the last warm-up call, with no
+    synchronize in between), so the GPU is never idle at its start. A
+    synchronize and a barrier close it. Clocks are sampled from before the
+    warm-up to after the region."""
+    sampler = ClockSampler(smi_id(device))
+    if graph is None:
+        calls[0]()
+    torch.cuda.synchronize()
+    sampler.start()
+    barrier(dist)
+    torch.cuda.synchronize()
+    if graph is None:
+        for i in range(1, warmup):
+            calls[i % n_rep]()
+    else:
+        for _ in range(warmup):
+            graph.replay()
+    segments = graph is None and steps >= SEGMENTS_FROM
+    n_seg = SPREAD_RUNS if segments else 0
+    seg_len = steps // n_seg if n_seg else 0
+    nxt = [warmup]
+
+    def run(n: int, bounds=None):
+        if graph is not None:
+            for _ in range(n // replays_per_step):
+                graph.replay()
+            return
+        for i in range(n):
+            calls[nxt[0] % n_rep]()
+            nxt[0] += 1
+            if bounds is not None and (i + 1) % seg_len == 0 and len(bounds) < n_seg:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(stream)
+                bounds.append(ev)
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    bounds = [ev0]
+    run(steps, bounds if segments else None)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev1.record(stream)
+    # the spread's further runs (K < SEGMENTS_FROM): not part of the timed region
+    runs = []
+    if not segments:
+        prev = ev1
+        for _ in range(SPREAD_RUNS):
+            run(steps)
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            runs.append((prev, ev))
+            prev = ev
+    torch.cuda.synchronize()
+    barrier(dist)
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if segments:
+        bounds.append(ev1)
+        lens = [seg_len] * (n_seg - 1) + [steps - seg_len * (n_seg - 1)]
+        spread = _spread([bounds[j].elapsed_time(bounds[j + 1]) / lens[j] for j in range(n_seg)],
+                         f"{n_seg} segments of the timed steps")
+    else:
+        spread = _spread([ms / steps] + [a.elapsed_time(b) / steps for a, b in runs],
+                         f"the timed run and {SPREAD_RUNS} further runs of {steps} steps right behind "
+                         "it, each between two events")
+    return {"ms": max_over_ranks(dist, ms, device), "spread": spread, "clocks": clocks}
+
+
+def measure_config(q, args, w: workloads.Workload, rank: int, world: int, device, stream, dist,
+                   *, headline: bool) -> Optional[Dict]:
+    """One workload on this GPU: build the input replicas, time K steps,
+    and (rank 0) assemble its numbers."""
     sh = stream.cuda_stream
-
     cpu = workloads.make_inputs(w)
     qk_bytes = 2 * (w.n_qo + w.n_kv) * w.num_tokens * w.head_dim
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -262,14 +385,14 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
     algo = workloads.algorithmic_bytes(w)
     heads = workloads.num_heads_total(w)
 
-    for i in range(args.warmup):
-        calls[i % n_rep]()
-    torch.cuda.synchronize()
-
     graph = None
+    steps = args.steps
     if args.graph:
         # one graph of n_rep calls (one per replica), replayed: GPU time per
         # call without the host's launch rate (decode-sized calls)
+        for c in calls:
+            c()
+        torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             cs = torch.cuda.current_stream().cuda_stream
@@ -278,56 +401,20 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
                 c()
         graph.replay()
         torch.cuda.synchronize()
-        args.steps = max(1, args.steps // n_rep) * n_rep
+        steps = max(1, steps // n_rep) * n_rep
+    t = timed_region(calls, n_rep, steps, args.warmup, stream, device, dist, graph, n_rep)
 
-    sampler = ClockSampler(smi_id(device))
-    sampler.start()
-    barrier(dist)
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    # segment boundaries for the spread of the time per step (10 segments; an
-    # event between two launches once every K/10 steps)
-    n_seg = 10 if args.steps >= 100 and graph is None else 0
-    seg_len = args.steps // n_seg if n_seg else 0
-    seg_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_seg)]
-    ev0.record(stream)
-    if graph is not None:
-        for _ in range(args.steps // n_rep):
-            graph.replay()
-    else:
-        for i in range(args.steps):
-            if n_seg and i % seg_len == 0 and i // seg_len < n_seg:
-                seg_ev[i // seg_len].record(stream)
-            calls[i % n_rep]()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    spread = None
-    if n_seg:
-        bounds = seg_ev + [ev1]
-        lens = [seg_len] * (n_seg - 1) + [args.steps - seg_len * (n_seg - 1)]
-        per_step = sorted(bounds[j].elapsed_time(bounds[j + 1]) / lens[j] for j in range(n_seg))
-        pick = lambda f: per_step[min(n_seg - 1, int(round(f * (n_seg - 1))))]
-        spread = {"p10": round(pick(0.1), 6), "p50": round(pick(0.5), 6), "p90": round(pick(0.9), 6),
-                  "unit": "ms per step", "over": f"{n_seg} segments of the timed steps"}
-    ms_max = max_over_ranks(dist, ms, device)
-
-    # end to end through the C ABI from pinned host buffers: H2D of q, k and
-    # positions, the call, D2H of q and k, every step
-    e2e = run_e2e(q, cpu, w, device, stream, args.e2e_steps, dist, entry)
+    e2e = None
+    if headline:
+        # end to end through the C ABI from pinned host buffers, every step
+        e2e = run_e2e(q, cpu, w, device, stream, args.e2e_steps, dist, entry)
 
     if rank != 0:
         return None
-    secs = ms_max / 1e3
-    value = world * algo * args.steps / secs / 1e9
-    peaks = measured_peaks()
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = float(peak or FALLBACK_HBM_GBS)
-    per_launch_s = secs / args.steps
+    secs = t["ms"] / 1e3
+    value = world * algo * steps / secs / 1e9
+    peak, peak_src = peak_hbm()
+    per_launch_s = secs / steps
     achieved = algo / per_launch_s / 1e9
     wm = q.work_map(w.num_tokens, w.n_qo, w.n_kv, w.head_dim, w.rope_dim, w.is_neox,
                     q.dtype_code(w.torch_dtype, w.pos_torch_dtype))
@@ -337,38 +424,87 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int, local: int) -> 
         wm = {"kernel": "register (norm step, rope step)"}
     full_size = w.num_tokens == workloads.get(w.name).num_tokens
     traffic = profiled_traffic(kernel, w.name) if (args.variant == "fused" and full_size) else None
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
-        "ms_per_step_spread": spread,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": w.name, "shape": workloads.describe(w),
-                   "storage_dtype": w.dtype, "bytes_per_step": algo, "heads_per_step": heads,
-                   "l2": (f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.1f} MB, L2-resident: "
-                          "a latency measurement)" if l2_resident else
-                          f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.0f} MB >= 4x L2)"
-                          if n_rep > 1 else "inputs larger than 4x L2"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": (f"CUDA graph of {n_rep} calls, replayed" if args.graph
-                              else "one C-ABI call per step from Python")
-                             + (", QKNR_INPUTS_READY" if args.inputs_ready else ""),
-                   "work_map": wm},
-        "heads_per_s": world * heads * args.steps / secs,
+    out = {
+        "value": round(value, 1), "ms_per_step": t["ms"] / steps, "ms_per_step_spread": t["spread"],
+        "config": config_of(w),
+        "setup": {"l2": (f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.1f} MB, L2-resident: "
+                         "a latency measurement)" if l2_resident else
+                         f"rotating {n_rep} input replicas ({n_rep * qk_bytes / 1e6:.0f} MB >= 4x L2)"
+                         if n_rep > 1 else "inputs larger than 4x L2"),
+                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                  "launch": (f"CUDA graph of {n_rep} calls, replayed" if args.graph
+                             else "one C-ABI call per step from Python")
+                            + (", QKNR_INPUTS_READY" if args.inputs_ready else ""),
+                  "work_map": wm},
+        "heads_per_s": world * heads * steps / secs,
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes": algo,
+                     "traffic": traffic["total"] if traffic else None,
+                     "traffic_read": traffic["read"] if traffic else None,
+                     "traffic_write": traffic["write"] if traffic else None,
+                     "algorithmic_bytes": algo,
+                     "algorithmic_read": workloads.algorithmic_read_bytes(w),
+                     "algorithmic_write": workloads.algorithmic_write_bytes(w),
                      "kernel": kernel},
-        "clocks": clocks,
-        "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step,
+        "clocks": t["clocks"],
+        "gpu_launches": steps * launches_per_step,
     }
+    if e2e is not None:
+        out["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        budget = args.cpu_seconds if headline else max(1.0, args.cpu_seconds / 4)
+        out["cpu_baseline"] = cpu_baseline(w, cpu, budget_s=budget)
+    del reps, calls, graph
+    torch.cuda.empty_cache()
+    return out
+
+
+PER_CONFIG_KEYS = ["value", "ms_per_step", "ms_per_step_spread", "heads_per_s", "pct_of_peak",
+                   "roofline", "clocks", "gpu_launches", "cpu_baseline", "config", "setup"]
+
+
+def run_ours(args, names: List[str], rank: int, world: int, local: int) -> Optional[Dict]:
+    import qk_rmsnorm_rope_gb300 as q
+
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist = init_dist(world, backend)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    q.init(local)
+    stream = torch.cuda.current_stream(device)
+    head = HEADLINE if HEADLINE in names else names[-1]
+    results = {}
+    for name in names:
+        w = workloads.get(name)
+        if args.tokens > 0:
+            w = workloads.scaled(w, args.tokens)
+        results[name] = measure_config(q, args, w, rank, world, device, stream, dist,
+                                       headline=(name == head))
+    if rank != 0:
+        return None
+    h = results[head]
+    line = {
+        "metric": METRIC, "value": h["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": h["ms_per_step"],
+        "ms_per_step_spread": h["ms_per_step_spread"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": h["config"],
+        "setup": h["setup"],
+        "heads_per_s": h["heads_per_s"], "pct_of_peak": h["pct_of_peak"],
+        "roofline": h["roofline"], "clocks": h["clocks"], "e2e": h.get("e2e"),
+        "gpu_launches": h["gpu_launches"],
+    }
+    if "cpu_baseline" in h:
+        line["cpu_baseline"] = h["cpu_baseline"]
     if args.variant == "unfused":
         line["variant"] = ("unfused baseline: RMSNorm kernel then RoPE kernel, in place "
                            "(value counts the fused op's algorithmic bytes)")
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, cpu, budget_s=args.cpu_seconds)
+    if len(names) > 1:
+        line["headline"] = f"{head}: the largest configuration; per_config holds every configuration"
+        line["per_config"] = {n: {k: results[n][k] for k in PER_CONFIG_KEYS if k in results[n]}
+                              for n in names}
     return line
 
 
@@ -616,13 +752,14 @@ def run_reference(args, w: workloads.Workload, rank: int, world: int) -> Optiona
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "shape": workloads.describe(w),
-                   "storage_dtype": w.dtype, "sample_tokens_per_step": n_tok},
+        "config": config_of(w),
+        "sample_tokens_per_step": n_tok,
         "heads_per_s": n_tok * (w.n_qo + w.n_kv) * args.steps / secs,
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "host": host_cpu(),
-                         "sample": f"{n_tok} consecutive tokens of {w.name} per step, in blocks of "
-                                   f"{block} over {cores} threads"},
+                         "sample": (f"{n_tok} consecutive tokens of {w.name} per step"
+                                    + (" (the whole workload)" if n_tok == T else "")
+                                    + f", in blocks of {block} over {cores} threads")},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -668,9 +805,10 @@ def run_ceiling(args, w: workloads.Workload) -> Dict:
 def main(argv: Optional[List[str]] = None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="dit", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="all", choices=["all"] + sorted(workloads.WORKLOADS),
+                    help="all (default): every configuration, headline on the largest; or one of them")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -689,18 +827,22 @@ def main(argv: Optional[List[str]] = None) -> int:
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
     rank, world, local = dist_env()
     if world != args.gpus and world > 1:
         print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
-    w = workloads.get(args.workload)
-    if args.tokens > 0:
-        w = workloads.scaled(w, args.tokens)
-    if args.ceiling:
-        line = run_ceiling(args, w) if rank == 0 else None
-    elif args.impl == "reference":
-        line = run_reference(args, w, rank, world)
+    names = CONFIGS if args.workload == "all" else [args.workload]
+    if args.ceiling or args.impl == "reference":
+        w = workloads.get(HEADLINE if args.workload == "all" else args.workload)
+        if args.tokens > 0:
+            w = workloads.scaled(w, args.tokens)
+        if args.ceiling:
+            line = run_ceiling(args, w) if rank == 0 else None
+        else:
+            line = run_reference(args, w, rank, world)
     else:
-        line = run_ours(args, w, rank, world, local)
+        line = run_ours(args, names, rank, world, local)
     if line is not None:
         print(json.dumps(line), flush=True)
     return 0

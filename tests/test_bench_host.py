@@ -86,15 +86,46 @@ def test_profiled_traffic_requires_matching_sources(tmp_path, monkeypatch):
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "qk_rmsnorm_rope_gb300").symlink_to(os.path.join(ROOT, "qk_rmsnorm_rope_gb300"))
-    f = prof / "qknr_bulk_kernel_dit.txt"
-    f.write_text(f"source_sha256: {bench.kernel_source_hash('qknr_bulk_kernel')}\n"
+    f = prof / "qknr_fused_kernel_dit.txt"
+    f.write_text(f"source_sha256: {bench.kernel_source_hash('qknr_fused_kernel')}\n"
+                 "dram_read_bytes_per_launch: 100\ndram_write_bytes_per_launch: 23\n")
+    assert bench.profiled_traffic("qknr_fused_kernel", "dit") == {"read": 100.0, "write": 23.0,
+                                                                  "total": 123.0}
+    # a summary without the read/write split is not used
+    f.write_text(f"source_sha256: {bench.kernel_source_hash('qknr_fused_kernel')}\n"
                  "traffic_bytes_per_launch: 123\n")
-    assert bench.profiled_traffic("qknr_bulk_kernel", "dit") == 123.0
-    f.write_text("source_sha256: 00\ntraffic_bytes_per_launch: 123\n")
-    assert bench.profiled_traffic("qknr_bulk_kernel", "dit") is None
-    assert bench.profiled_traffic("qknr_bulk_kernel", "gqa") is None
     assert bench.profiled_traffic("qknr_fused_kernel", "dit") is None
-    assert bench.kernel_source_hash("qknr_fused_kernel") != bench.kernel_source_hash("qknr_bulk_kernel")
+    f.write_text("source_sha256: 00\ndram_read_bytes_per_launch: 100\ndram_write_bytes_per_launch: 23\n")
+    assert bench.profiled_traffic("qknr_fused_kernel", "dit") is None
+    assert bench.profiled_traffic("qknr_fused_kernel", "gqa") is None
+    assert bench.profiled_traffic("qknr_other_kernel", "dit") is None
+
+
+def test_reference_arm_config_matches_ours():
+    """Both arms name the workload with the same dict (the reference arm's
+    token sample per step is reported beside it, not inside it)."""
+    r = _run_bench(["--impl", "reference", "--workload", "dit", "--steps", "3", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    w = bench.workloads.get("dit")
+    assert d["config"] == bench.config_of(w)
+    assert set(d["config"]) == {"workload", "shape", "storage_dtype", "bytes_per_step", "heads_per_step"}
+    assert d["config"]["bytes_per_step"] == bench.workloads.algorithmic_bytes(w)
+    assert d["sample_tokens_per_step"] >= 1
+
+
+def test_default_workload_is_every_config_with_the_largest_as_headline():
+    assert bench.CONFIGS == ["tiny", "dit", "mha_neox", "gqa", "fused_qkv"]
+    sizes = {n: bench.workloads.algorithmic_bytes(bench.workloads.get(n)) for n in bench.CONFIGS}
+    assert bench.HEADLINE == max(sizes, key=sizes.get)
+
+
+def test_algorithmic_read_write_split():
+    for n in bench.CONFIGS:
+        w = bench.workloads.get(n)
+        rd, wr = bench.workloads.algorithmic_read_bytes(w), bench.workloads.algorithmic_write_bytes(w)
+        assert rd + wr == bench.workloads.algorithmic_bytes(w)
+        assert wr == 2 * (w.n_qo + w.n_kv) * w.num_tokens * w.head_dim
 
 
 def test_source_hash_ignores_comments_only():

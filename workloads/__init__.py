@@ -37,7 +37,8 @@ import numpy as np
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "to_device", "build_cos_sin_cache",
-           "scaled", "algorithmic_bytes", "num_heads_total", "describe"]
+           "scaled", "algorithmic_bytes", "algorithmic_read_bytes", "algorithmic_write_bytes",
+           "num_heads_total", "describe"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -105,15 +106,25 @@ def num_heads_total(w: Workload) -> int:
     return (w.n_qo + w.n_kv) * w.num_tokens
 
 
+def algorithmic_write_bytes(w: Workload) -> int:
+    """Bytes the op must write once: every Q/K head."""
+    return (w.n_qo + w.n_kv) * w.num_tokens * w.head_dim * 2
+
+
+def algorithmic_read_bytes(w: Workload) -> int:
+    """Bytes the op must read once: every Q/K head, one fp32 cache row and one
+    position per token, and both weight vectors."""
+    psz = 4 if w.pos_dtype == "i32" else 8
+    return (algorithmic_write_bytes(w)
+            + w.num_tokens * w.rope_dim * 4
+            + w.num_tokens * psz
+            + 2 * w.head_dim * 2)
+
+
 def algorithmic_bytes(w: Workload) -> int:
     """Bytes the op must move once: read + write every Q/K head, one fp32 cache
     row and one position per token, and both weight vectors."""
-    esz = 2
-    psz = 4 if w.pos_dtype == "i32" else 8
-    return (2 * (w.n_qo + w.n_kv) * w.num_tokens * w.head_dim * esz
-            + w.num_tokens * w.rope_dim * 4
-            + w.num_tokens * psz
-            + 2 * w.head_dim * esz)
+    return algorithmic_read_bytes(w) + algorithmic_write_bytes(w)
 
 
 def build_cos_sin_cache(cache_len: int, rope_dim: int, base: float) -> torch.Tensor:
