@@ -54,7 +54,7 @@ extern "C" {
  * kernel finishes (programmatic dependent launch), and reads q, k and the
  * cos|sin table only after it has completed: about 17% less latency per
  * decode-sized call and 3% more bandwidth on a 4608-token DiT call, with the
- * same results. Breaking the promise is a data race. The other kernels and
+ * same results. Breaking the promise is a data race. The unfused baseline and
  * the staged host path (which launches without the early start) ignore it.
  */
 #define QKNR_INPUTS_READY 0x200
@@ -67,12 +67,11 @@ extern "C" {
 #define QKNR_ERR_MISALIGNED 4      /* pointer or stride breaks the 16-byte vector rule */
 #define QKNR_ERR_CUDA 5            /* a CUDA runtime call failed; message has the CUDA error */
 #define QKNR_ERR_POSITION_OOB 6    /* qknr_apply_checked: a position outside [0, cache_len) */
-#define QKNR_ERR_WATCHDOG 7        /* a bounded wait inside a kernel ran out; that call's output is incomplete */
 
 /*
  * Prepare the library for CUDA device `device`: reads the SM count and other
- * limits, and allocates a 24-byte status block (position-check counters and
- * the kernels' watchdog flag) used by qknr_apply_checked and qknr_sync.
+ * limits, and allocates a 16-byte status block (the position-check counters
+ * of qknr_apply_checked).
  * Idempotent; safe to call from several threads. Restores the caller's
  * current device before returning. Returns QKNR_OK or QKNR_ERR_CUDA /
  * QKNR_ERR_INVALID_ARG (no such device).
@@ -97,10 +96,9 @@ int qknr_version(void);
  * Shape gate, the counterpart of the deep-dive's can_use check (§5.2) for
  * this library's own kernels. Returns 1 if (head_dim, rope_dim, is_neox,
  * dtype) is in the accepted set, else 0. Accepted: head_dim in {64, 80, 96,
- * 128, 192, 256} (80, 96 and 192 with the register kernel only);
- * rope_dim even with 0 < rope_dim <= head_dim; interleaved pairing takes
- * every such rope_dim; NeoX pairing takes rope_dim % 16 == 0 or rope_dim in
- * {2, 4, 6, 8}. This contains the page's set (head_dim/32 elements per lane,
+ * 128, 192, 256}; rope_dim even with 0 < rope_dim <= head_dim; interleaved
+ * pairing takes every such rope_dim; NeoX pairing takes rope_dim % 16 == 0 or
+ * rope_dim in {2, 4, 6, 8}. This contains the page's set (head_dim/32 elements per lane,
  * rotary lanes a power of two) and more.
  */
 int qknr_can_use(int head_dim, int rope_dim, int is_neox, int dtype);
@@ -179,15 +177,18 @@ int qknr_apply_unfused(void *q, void *k, const void *q_w, const void *k_w,
  *
  * Same arguments, results and QKNR_ERR_POSITION_OOB report as
  * qknr_apply_checked, but qknr_init is not needed and nothing is allocated:
- * the 24-byte status block lives in a 256-byte file-scope __device__ array
+ * the 16-byte status block lives in a 256-byte file-scope __device__ array
  * of the library, which every GPU that loads the library holds until the
- * process exits. A call needs those 24 bytes whatever its num_tokens, so no
+ * process exits. A call needs those 16 bytes whatever its num_tokens, so no
  * problem size exceeds the array. The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture. Each call resets the status
- * it reads, and waits for `stream` before returning. All calls share the one
- * array: calls on one device are serialised on the host, and two launches
- * that used the array at the same time on the GPU would race.
+ * make that first call before any stream capture. That set-up is kept for
+ * the life of the process: a device reset (cudaDeviceReset) after the first
+ * call on a device is not supported by this entry point. Each call resets
+ * the status it reads, and waits for `stream` before returning (it is
+ * synchronous, like qknr_apply_checked). All calls share the one array:
+ * calls on one device are serialised on the host, and two launches that used
+ * the array at the same time on the GPU would race.
  */
 int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_w,
                                const float *cos_sin_cache, int64_t cache_len,
@@ -263,55 +264,25 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
                     int64_t head_stride, float eps, int dtype, int64_t chunk_tokens, int flags,
                     void *stream);
 
-/*
- * Reports whether any earlier call on the current device had a kernel wait
- * run out (the bulk kernel bounds every wait at about one second; it never
- * runs out in normal operation). Waits for `stream`, then returns QKNR_OK or
- * QKNR_ERR_WATCHDOG and clears the flag. qknr_apply is asynchronous, so this
- * is how a caller checks it; the checked entry points report it themselves.
- */
-int qknr_sync(void *stream);
+/* kernel (qknr_query_work_map out[0]) */
+#define QKNR_KERNEL_REGISTER 1 /* the register kernel: loads straight into registers; every accepted shape */
 
-/*
- * Exercises the watchdog path: launches on `stream` a one-thread kernel whose
- * bounded wait (the bulk kernel's, about one second) is on a barrier that
- * nothing arrives on. The wait runs out, the kernel sets the watchdog bit and
- * returns; the next qknr_sync on the device then reports QKNR_ERR_WATCHDOG
- * and clears it. No fault, no unbounded wait: the context stays usable. For
- * tests of a caller's error handling. The op has no counterpart on the pages.
- */
-int qknr_selftest_watchdog(void *stream);
-
-/* kernels (QKNR_TUNE_KERNEL values and qknr_query_work_map out[0]) */
-#define QKNR_KERNEL_AUTO 0
-#define QKNR_KERNEL_REGISTER 1 /* loads straight into registers; every accepted shape */
-#define QKNR_KERNEL_BULK 2     /* cp.async.bulk ring in shared memory; rope_dim % 8 == 0, 16-byte aligned table */
-#define QKNR_KERNEL_ASYNC 3    /* per-warp cp.async pipeline; same requirements as QKNR_KERNEL_BULK */
-#define QKNR_KERNEL_LEAN 4     /* register kernel with weights and cos|sin row in shared memory */
-
-/* tuning keys for qknr_set_tuning / qknr_get_tuning */
+/* tuning keys for qknr_set_tuning / qknr_get_tuning (1, 6, 7 and 8 are not used) */
 #define QKNR_TUNE_RESET 0       /* qknr_set_tuning(QKNR_TUNE_RESET, 0): every key back to automatic */
-#define QKNR_TUNE_KERNEL 1      /* 0 auto (the register kernel), 1 register, 2 bulk, 3 async, 4 lean */
-#define QKNR_TUNE_PASSES 2      /* register kernel: warp passes per item, 1..4 (0 auto: 4, or 1 when
-                                   the whole call has at most 16 warp passes per SM) */
-#define QKNR_TUNE_THREADS 3     /* register / async kernel: threads per CTA, 64/128/256/512 (0 auto =
-                                   256; the async kernel takes at most 256) */
-#define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy; bulk: 1) */
+#define QKNR_TUNE_PASSES 2      /* warp passes per item, 1..4 (0 auto: 4, or 1 when the whole call has
+                                   at most 16 warp passes per SM) */
+#define QKNR_TUNE_THREADS 3     /* threads per CTA, 64/128/256/512 (0 auto = 256) */
+#define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy) */
 #define QKNR_TUNE_PDL 5         /* programmatic dependent launch: -1 auto (on), 0 off, 1 on */
-#define QKNR_TUNE_CONSUMERS 6   /* bulk kernel: consumer warps per CTA, 1..16 (0 auto: one per warp
-                                   pass of a tile, 4..16) */
-#define QKNR_TUNE_STAGES 7      /* bulk kernel: ring depth, 1..32; async kernel: per-warp ring depth,
-                                   2..8 (0 auto: what fits) */
-#define QKNR_TUNE_TILE_BYTES 8  /* bulk kernel: max bytes of heads per tile (0 auto = 24576) */
-#define QKNR_TUNE_ORDER 9       /* register kernel item order: 0 auto (= 2), 1 a contiguous range per
-                                   warp, 2 interleaved (warp w takes items w, w + W, ...) */
+#define QKNR_TUNE_ORDER 9       /* item order: 0 auto (= 2), 1 a contiguous range per warp,
+                                   2 interleaved (warp w takes items w, w + W, ...) */
 
 /*
  * Process-wide launch tuning, for benchmarks and tests; results do not depend
  * on it (every setting gives the same bits). Invalid values return
  * QKNR_ERR_INVALID_ARG and change nothing. The environment variable
- * QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=1,pdl=1,consumers=8,stages=16,tile=24576,order=2"
- * sets the same keys at first use.
+ * QKNR_TUNE="passes=4,threads=256,ctas=2,pdl=1,order=2" sets the same keys at
+ * first use.
  */
 int qknr_set_tuning(int key, int value);
 int qknr_get_tuning(int key, int *value);
@@ -323,11 +294,10 @@ int qknr_get_tuning(int key, int *value);
 /*
  * The launch qknr_apply would make for these sizes (no launch, no pointers;
  * assumes a 16-byte aligned cos|sin table). out[QKNR_WORK_MAP_FIELDS]:
- *  0 kernel (QKNR_KERNEL_REGISTER / QKNR_KERNEL_BULK)  1 grid CTAs  2 threads per CTA
- *  3 work items (warp items / tiles)  4 items per token  5 resident CTAs per SM
- *  6 PDL on  7 passes per token (register) / heads per tile (bulk)
- *  8 unroll class (register) / ring stages (bulk, async)  9 consumer warps (bulk)
- * 10 dynamic shared memory bytes  11 bytes per ring stage
+ *  0 kernel (QKNR_KERNEL_REGISTER)  1 grid CTAs  2 threads per CTA
+ *  3 warp items  4 items per token  5 resident CTAs per SM  6 PDL on
+ *  7 warp passes per token  8 unroll class (passes of loads in flight)
+ *  9 item order (1 contiguous, 2 interleaved)  10, 11 reserved (0)
  */
 int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
                         int is_neox, int dtype, int64_t *out);

@@ -21,10 +21,10 @@ __all__ = [
     "QKNR_HOST_DIRECT", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
     "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-    "qknr_apply_host", "qknr_apply_strided", "qknr_sync", "qknr_selftest_watchdog",
+    "qknr_apply_host", "qknr_apply_strided",
     "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map", "TUNE_KEYS",
     "init", "apply", "apply_checked", "apply_unfused", "apply_host", "can_use", "dtype_code",
-    "work_map", "set_tuning", "get_tuning", "sync",
+    "work_map", "set_tuning", "get_tuning",
 ]
 
 QKNR_BF16 = 0x000
@@ -35,17 +35,16 @@ QKNR_INPUTS_READY = 0x200   # caller's promise: weights and positions are not wr
 STATUS_NAMES = {
     0: "QKNR_OK", 1: "QKNR_ERR_NOT_INITIALIZED", 2: "QKNR_ERR_INVALID_ARG",
     3: "QKNR_ERR_UNSUPPORTED", 4: "QKNR_ERR_MISALIGNED", 5: "QKNR_ERR_CUDA",
-    6: "QKNR_ERR_POSITION_OOB", 7: "QKNR_ERR_WATCHDOG",
+    6: "QKNR_ERR_POSITION_OOB",
 }
 
-QKNR_KERNEL_AUTO, QKNR_KERNEL_REGISTER, QKNR_KERNEL_BULK, QKNR_KERNEL_ASYNC, QKNR_KERNEL_LEAN = 0, 1, 2, 3, 4
+QKNR_KERNEL_REGISTER = 1
 QKNR_HOST_AUTO, QKNR_HOST_STAGED, QKNR_HOST_DIRECT = 0, 1, 2
 HOST_MODES = {"auto": QKNR_HOST_AUTO, "staged": QKNR_HOST_STAGED, "direct": QKNR_HOST_DIRECT}
 # QKNR_TUNE_* keys (include/qknr.h)
-TUNE_KEYS = {"reset": 0, "kernel": 1, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5,
-             "consumers": 6, "stages": 7, "tile_bytes": 8, "order": 9}
+TUNE_KEYS = {"reset": 0, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5, "order": 9}
 WORK_MAP_FIELDS = ["kernel", "grid", "threads", "items", "items_per_token", "ctas_per_sm", "pdl",
-                   "passes_or_heads", "unroll_or_stages", "consumers", "smem_bytes", "stage_bytes"]
+                   "passes_per_token", "unroll", "order", "reserved10", "reserved11"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -85,16 +84,13 @@ def _load() -> ctypes.CDLL:
                                     i64, i64, i64, f32, i32, i64, i32, vp]
     lib.qknr_apply_strided.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
                                        i64, i64, i64, i64, f32, i32, vp]
-    lib.qknr_sync.argtypes = [vp]
-    lib.qknr_selftest_watchdog.argtypes = [vp]
     lib.qknr_set_tuning.argtypes = [i32, i32]
     lib.qknr_get_tuning.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
     lib.qknr_query_work_map.argtypes = [i64, i32, i32, i32, i32, i32, i32,
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
                  "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-                 "qknr_apply_host", "qknr_apply_strided", "qknr_sync", "qknr_selftest_watchdog",
-                 "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
+                 "qknr_apply_host", "qknr_apply_strided", "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -191,14 +187,6 @@ def qknr_apply_strided(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_q
     return _get_lib().qknr_apply_strided(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens,
                                          n_qo, n_kv, head_dim, rope_dim, int(is_neox), q_stride,
                                          k_stride, q_head_stride, k_head_stride, eps, dtype, stream)
-
-
-def qknr_selftest_watchdog(stream) -> int:
-    return _get_lib().qknr_selftest_watchdog(stream)
-
-
-def qknr_sync(stream) -> int:
-    return _get_lib().qknr_sync(stream)
 
 
 def qknr_set_tuning(key: int, value: int) -> int:
@@ -453,17 +441,6 @@ def get_tuning(name: str) -> int:
     return v.value
 
 
-def sync(stream=None) -> None:
-    """qknr_sync on ``stream`` (default: torch's current stream); raises
-    QknrError(QKNR_ERR_WATCHDOG) if a kernel wait ran out since the last check."""
-    import torch
-    if stream is None:
-        stream = torch.cuda.current_stream().cuda_stream
-    elif not isinstance(stream, int):
-        stream = stream.cuda_stream
-    _check(qknr_sync(stream))
-
-
 def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int,
              is_neox: bool, dtype: int) -> Dict[str, int]:
     """The launch qknr_apply would make (kernel, grid, threads, items, ...)."""
@@ -471,5 +448,8 @@ def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int
     _check(qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox), dtype,
                                out))
     d = dict(zip(WORK_MAP_FIELDS, [int(v) for v in out]))
-    d["kernel"] = {1: "register", 2: "bulk", 3: "async", 4: "lean"}.get(d["kernel"], d["kernel"])
+    d["kernel"] = {QKNR_KERNEL_REGISTER: "register"}.get(d["kernel"], d["kernel"])
+    d["order"] = {1: "contiguous", 2: "interleaved"}.get(d["order"], d["order"])
+    for key in ("reserved10", "reserved11"):
+        d.pop(key)
     return d

@@ -22,8 +22,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libqknr.so")
 SOURCES = ["qknr_api.cu", "qknr_inst_bf16.cu", "qknr_inst_fp16.cu", "qknr_inst_bf16_early.cu",
            "qknr_inst_fp16_early.cu"]
-HEADERS = ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_bulk_kernel.cuh", "qknr_async_kernel.cuh", "qknr_lean_kernel.cuh",
-           "qknr_register_table.cuh", "qknr_dispatch.h"]
+HEADERS = ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_register_table.cuh", "qknr_dispatch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

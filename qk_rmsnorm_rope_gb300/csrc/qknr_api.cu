@@ -5,25 +5,14 @@
 // launch, int32 or int64 positions, grid sized from occupancy x SM count, the
 // CUDA launch error checked), restated for this library's kernels.
 //
-// Four kernels compute the op (identical arithmetic and lane mapping):
-//   register kernel  qknr_fused_kernel  (qknr_kernel.cuh): loads straight into
-//                    registers; any accepted shape and alignment.
-//   bulk kernel      qknr_bulk_kernel   (qknr_bulk_kernel.cuh): cp.async.bulk
-//                    copies into a shared-memory ring; needs rope_dim % 8 == 0
-//                    and a 16-byte aligned cos|sin table.
-//   async kernel     qknr_async_kernel  (qknr_async_kernel.cuh): a per-warp
-//                    cp.async pipeline; same requirements as the bulk kernel.
-//   lean kernel      qknr_lean_kernel   (qknr_lean_kernel.cuh): the register
-//                    kernel with weights and the cos|sin row in shared memory.
-// The automatic choice is the register kernel (measured fastest on GB300); the
-// others run when QKNR_TUNE_KERNEL asks for them.
+// One kernel computes the op: the register kernel qknr_fused_kernel
+// (qknr_kernel.cuh), which loads straight into registers and takes any
+// accepted shape and alignment.
 //
 // Entry points beyond the op itself: the position-checked variants (one with
 // no allocation), the unfused two-kernel baseline, the host-buffer variant
 // (direct or staged) and the variant with separate q and k head strides.
 #include "../../include/qknr.h"
-#include "qknr_async_kernel.cuh"
-#include "qknr_bulk_kernel.cuh"
 #include "qknr_dispatch.h"
 #include "qknr_kernel.cuh"
 
@@ -45,15 +34,11 @@
 
 namespace {
 
-using qknr::BulkParams;
 using qknr::Params;
 
 constexpr int kMaxDevices = 64;
-constexpr int kVersion = 10200;             // 1.2.0: host buffers, separate head strides, head_dim 80
-constexpr int kStatusWords = 3;             // {bad-token count, first bad token, watchdog bits}
-constexpr int kMaxBulkSmem = 232448;        // dynamic shared memory per CTA on sm_100/sm_103 (227 KB)
-constexpr int kDefaultTileBytes = 24576;    // bulk kernel: max bytes of heads per tile
-constexpr int kMaxStages = 32;
+constexpr int kVersion = 10300;             // 1.3.0: the register kernel alone
+constexpr int kStatusWords = 2;             // {bad-token count, first bad token}
 constexpr int kMaxHeads = 1 << 24;                // largest n_qo + n_kv accepted
 constexpr long long kMaxExtentBytes = 1LL << 56;  // largest q or k extent accepted (far above any GPU's memory)
 
@@ -74,7 +59,7 @@ int fail_cuda(cudaError_t e, const char *what) {
 }
 
 // ------------------------------------------------------------------ tuning
-constexpr int kNumTuneKeys = 10;  // keys 1..9 (QKNR_TUNE_*); slot 0 unused
+constexpr int kNumTuneKeys = 10;  // keys 2..5 and 9 (QKNR_TUNE_*); the other slots are unused
 // the value that means "automatic" for each key
 constexpr int kTuneAuto[kNumTuneKeys] = {0, 0, 0, 0, 0, -1, 0, 0, 0, 0};
 std::atomic<int> g_tune[kNumTuneKeys] = {{0}, {0}, {0}, {0}, {0}, {-1}, {0}, {0}, {0}, {0}};
@@ -82,11 +67,6 @@ std::once_flag g_env_once;
 
 int tune_check(int key, int value) {
     switch (key) {
-        case QKNR_TUNE_KERNEL:
-            return (value >= 0 && value <= 4)
-                       ? QKNR_OK
-                       : fail(QKNR_ERR_INVALID_ARG,
-                              "kernel must be 0 (auto), 1 (register), 2 (bulk), 3 (async) or 4 (lean)");
         case QKNR_TUNE_PASSES:
             return (value >= 0 && value <= qknr::kUnrollClass[qknr::kNumUnroll - 1])
                        ? QKNR_OK
@@ -102,37 +82,24 @@ int tune_check(int key, int value) {
         case QKNR_TUNE_PDL:
             return (value >= -1 && value <= 1) ? QKNR_OK
                                                 : fail(QKNR_ERR_INVALID_ARG, "use_pdl must be -1, 0 or 1");
-        case QKNR_TUNE_CONSUMERS:
-            return (value >= 0 && value <= 16) ? QKNR_OK
-                                               : fail(QKNR_ERR_INVALID_ARG, "consumer warps must be in [0, 16]");
-        case QKNR_TUNE_STAGES:
-            return (value >= 0 && value <= kMaxStages)
-                       ? QKNR_OK
-                       : fail(QKNR_ERR_INVALID_ARG, "stages must be in [0, %d]", kMaxStages);
         case QKNR_TUNE_ORDER:
             return (value >= 0 && value <= 2)
                        ? QKNR_OK
                        : fail(QKNR_ERR_INVALID_ARG, "order must be 0 (auto), 1 (contiguous) or 2 (interleaved)");
-        case QKNR_TUNE_TILE_BYTES:
-            return (value == 0 || (value >= 512 && value <= 196608))
-                       ? QKNR_OK
-                       : fail(QKNR_ERR_INVALID_ARG, "tile bytes must be 0 or in [512, 196608]");
         default:
             return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
     }
 }
 
-// QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=1,pdl=1,consumers=8,stages=16,tile=24576"
+// QKNR_TUNE="passes=4,threads=256,ctas=2,pdl=1,order=2"
 void read_env_tuning() {
     const char *s = std::getenv("QKNR_TUNE");
     if (!s) return;
     static const struct {
         const char *name;
         int key;
-    } names[] = {{"kernel", QKNR_TUNE_KERNEL},   {"passes", QKNR_TUNE_PASSES},
-                 {"threads", QKNR_TUNE_THREADS}, {"ctas", QKNR_TUNE_CTAS_PER_SM},
-                 {"pdl", QKNR_TUNE_PDL},         {"consumers", QKNR_TUNE_CONSUMERS},
-                 {"stages", QKNR_TUNE_STAGES},   {"tile", QKNR_TUNE_TILE_BYTES},
+    } names[] = {{"passes", QKNR_TUNE_PASSES}, {"threads", QKNR_TUNE_THREADS},
+                 {"ctas", QKNR_TUNE_CTAS_PER_SM}, {"pdl", QKNR_TUNE_PDL},
                  {"order", QKNR_TUNE_ORDER}};
     std::string spec(s);
     size_t pos = 0;
@@ -165,14 +132,8 @@ struct DeviceState {
     std::mutex checked_mu;                      // serialises status read-backs on this device
     // resident CTAs per SM for the register kernel, by (dtype, pos64, d_idx, mode, u_idx, threads class)
     std::atomic<int> occupancy[2][2][2][qknr::kNumHeadDim][2][qknr::kNumUnroll][4];  // [early][dt]...
-    // bulk kernels whose dynamic shared-memory limit was raised, by (dtype, pos64, d_idx, mode)
-    std::atomic<bool> bulk_attr[2][2][qknr::kNumHeadDim][2];
     // resident CTAs per SM of the unfused-baseline kernels, by (dtype, op-1, pos64, d_idx, mode)
     std::atomic<int> unfused_occ[2][2][2][qknr::kNumHeadDim][2];
-    // async kernels whose dynamic shared-memory limit was raised, by (dtype, pos64, d_idx, mode)
-    std::atomic<bool> async_attr[2][2][qknr::kNumHeadDim][2];
-    // resident CTAs per SM of the lean kernel, by (dtype, pos64, d_idx, mode, threads class)
-    std::atomic<int> lean_occ[2][2][qknr::kNumHeadDim][2][4];
     // host-buffer pipeline (qknr_apply_host): a host-to-device and a
     // device-to-host copy stream and the events that order them against the
     // caller's stream; made by the first such call on this device
@@ -237,12 +198,10 @@ struct Call {
 struct WorkMap {
     int kind = QKNR_KERNEL_REGISTER;
     int grid = 0, threads = 0, ctas_per_sm = 0, pdl = 1;
-    long long items = 0;  // warp items (register kernel) or tiles (bulk kernel)
+    long long items = 0;  // warp items: (token, chunk of warp passes)
     int chunks_per_token = 0;
-    int passes_per_token = 0, max_passes = 0, u_idx = 0;  // register kernel
-    int heads_per_chunk = 0, stages = 0, consumers = 0;   // bulk kernel
-    int interleave = 0;                                   // register kernel item order
-    int stage_bytes = 0, smem_bytes = 0;
+    int passes_per_token = 0, max_passes = 0, u_idx = 0;
+    int interleave = 0;   // item order
     const void *kernel = nullptr;
 };
 
@@ -316,168 +275,8 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     return QKNR_OK;
 }
 
-bool bulk_applies(const Call &c) { return (c.rope_dim % 8) == 0 && aligned(c.cache, 16); }
-
-// Bulk kernel: tiles are (token, chunk of heads) of at most `tile` bytes of
-// heads; one producer warp and `consumers` consumer warps per CTA; the ring
-// is as deep as the shared memory of the CTAs resident per SM allows (default
-// one CTA per SM), at most kMaxStages.
-int plan_bulk(DeviceState &st, const Call &c, WorkMap *wm) {
-    const int d_idx = head_dim_index(c.head_dim);
-    const int heads = c.n_qo + c.n_kv;
-    const int head_b = 2 * c.head_dim;
-    const int row_b = 4 * c.rope_dim;
-    wm->kind = QKNR_KERNEL_BULK;
-    int tile = tune(QKNR_TUNE_TILE_BYTES);
-    if (tile <= 0) tile = kDefaultTileBytes;
-    const int max_heads = std::max(1, tile / head_b);
-    wm->chunks_per_token = (heads + max_heads - 1) / max_heads;
-    wm->heads_per_chunk = (heads + wm->chunks_per_token - 1) / wm->chunks_per_token;
-    wm->stage_bytes = (wm->heads_per_chunk * head_b + row_b + 127) / 128 * 128;
-    wm->items = c.num_tokens * wm->chunks_per_token;
-
-    int ctas = tune(QKNR_TUNE_CTAS_PER_SM);
-    if (ctas <= 0) ctas = 1;
-    const int smem_cap = std::min(kMaxBulkSmem, (228 * 1024) / ctas - 1024);
-    const int fit = (smem_cap - qknr::bulk_stage_offset(kMaxStages)) / wm->stage_bytes;
-    if (fit < 1) return fail(QKNR_ERR_UNSUPPORTED, "a %d-byte tile does not fit shared memory", wm->stage_bytes);
-    // all consumer warps share each tile; by default one warp per warp pass of
-    // a tile (at least 4, at most 16)
-    const int passes = (wm->heads_per_chunk + heads_per_pass(c.head_dim) - 1) / heads_per_pass(c.head_dim);
-    int consumers = tune(QKNR_TUNE_CONSUMERS);
-    if (consumers <= 0) consumers = std::min(16, std::max(4, passes));
-    int stages = tune(QKNR_TUNE_STAGES);
-    if (stages <= 0) stages = kMaxStages;
-    stages = std::min(stages, fit);
-    wm->stages = stages;
-    wm->consumers = consumers;
-    wm->threads = qknr::kWarp * (1 + consumers);
-    wm->smem_bytes = qknr::bulk_stage_offset(stages) + stages * wm->stage_bytes;
-
-    const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
-    const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
-    const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
-    wm->kernel = dt ? qknr::bulk_kernel_fp16(pos64, d_idx, mode) : qknr::bulk_kernel_bf16(pos64, d_idx, mode);
-    if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no bulk kernel for this shape");
-    std::atomic<bool> &attr = st.bulk_attr[dt][pos64][d_idx][mode];
-    if (!attr.load(std::memory_order_acquire)) {
-        cudaError_t e =
-            cudaFuncSetAttribute(wm->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxBulkSmem);
-        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-        attr.store(true, std::memory_order_release);
-    }
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wm->kernel, wm->threads, wm->smem_bytes);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(bulk)");
-    if (occ <= 0)
-        return fail(QKNR_ERR_CUDA, "bulk kernel cannot be resident (%d bytes of shared memory)", wm->smem_bytes);
-    wm->ctas_per_sm = std::min(occ, ctas);
-    wm->grid = static_cast<int>(
-        std::max(1LL, std::min(wm->items, static_cast<long long>(wm->ctas_per_sm) * st.sm_count)));
-    return QKNR_OK;
-}
-
-// Async kernel: warps stream (token, pass) units through a private ring of S
-// stages (pass data 1 KB + cos|sin row + flag). S and the CTAs per SM are
-// chosen so that the rings of all resident warps fit the SM's shared memory.
-int plan_async(DeviceState &st, const Call &c, WorkMap *wm) {
-    const int d_idx = head_dim_index(c.head_dim);
-    const int hpw = heads_per_pass(c.head_dim);
-    wm->kind = QKNR_KERNEL_ASYNC;
-    wm->passes_per_token = (c.n_qo + c.n_kv + hpw - 1) / hpw;
-    wm->chunks_per_token = wm->passes_per_token;
-    wm->items = c.num_tokens * wm->passes_per_token;
-    wm->stage_bytes = 1024 + 4 * c.rope_dim + 16;
-    int threads = tune(QKNR_TUNE_THREADS);
-    if (threads_index(threads) < 0 || threads > 256) threads = 256;
-    wm->threads = threads;
-    const int warps = threads / qknr::kWarp;
-
-    const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
-    const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
-    const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
-    wm->kernel = dt ? qknr::async_kernel_fp16(pos64, d_idx, mode) : qknr::async_kernel_bf16(pos64, d_idx, mode);
-    if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no async kernel for this shape");
-    std::atomic<bool> &attr = st.async_attr[dt][pos64][d_idx][mode];
-    if (!attr.load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(wm->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxBulkSmem);
-        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-        attr.store(true, std::memory_order_release);
-    }
-    // CTAs per SM allowed by registers alone
-    int occ_regs = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_regs, wm->kernel, threads, 0);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(async)");
-    if (occ_regs <= 0) return fail(QKNR_ERR_CUDA, "async kernel cannot be resident with %d threads", threads);
-    const int force = tune(QKNR_TUNE_CTAS_PER_SM);
-    int ctas = force > 0 ? std::min(force, occ_regs) : occ_regs;
-    int stages = tune(QKNR_TUNE_STAGES);
-    const int per_sm = 228 * 1024 - 4096;
-    for (;;) {
-        const int fit = per_sm / ctas / (warps * wm->stage_bytes);
-        int s = stages > 0 ? std::min(stages, fit) : fit;
-        s = std::min(s, qknr::kAsyncMaxStages);
-        if (s >= 2 || ctas == 1) {
-            wm->stages = std::max(1, s);
-            break;
-        }
-        --ctas;
-    }
-    if (wm->stages < 2) return fail(QKNR_ERR_UNSUPPORTED, "async kernel: a %d-byte stage does not fit twice", wm->stage_bytes);
-    wm->smem_bytes = warps * wm->stages * wm->stage_bytes;
-    int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wm->kernel, threads, wm->smem_bytes);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(async)");
-    if (occ <= 0) return fail(QKNR_ERR_CUDA, "async kernel cannot be resident (%d bytes of shared memory)", wm->smem_bytes);
-    wm->ctas_per_sm = std::min(occ, ctas);
-    const long long needed = (wm->items + warps - 1) / warps;
-    wm->grid = static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(wm->ctas_per_sm) * st.sm_count)));
-    return QKNR_OK;
-}
-
-// Lean kernel: the register kernel's items (4 passes) with weights and the
-// cos|sin row in shared memory; at most 256 threads per CTA.
-int plan_lean(DeviceState &st, const Call &c, WorkMap *wm) {
-    const int d_idx = head_dim_index(c.head_dim);
-    const int hpw = heads_per_pass(c.head_dim);
-    wm->kind = QKNR_KERNEL_LEAN;
-    wm->passes_per_token = (c.n_qo + c.n_kv + hpw - 1) / hpw;
-    wm->chunks_per_token = (wm->passes_per_token + 3) / 4;
-    wm->max_passes = (wm->passes_per_token + wm->chunks_per_token - 1) / wm->chunks_per_token;
-    wm->u_idx = 1;
-    wm->items = c.num_tokens * wm->chunks_per_token;
-    int threads = tune(QKNR_TUNE_THREADS);
-    if (threads_index(threads) < 0 || threads > 256) threads = 256;
-    wm->threads = threads;
-    const int dt = (c.dtype & 0xff) == QKNR_FP16 ? 1 : 0;
-    const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
-    const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
-    wm->kernel = dt ? qknr::lean_kernel_fp16(pos64, d_idx, mode) : qknr::lean_kernel_bf16(pos64, d_idx, mode);
-    if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no lean kernel for this shape");
-    int occ = 0;
-    const int rc = cached_occupancy(st.lean_occ[dt][pos64][d_idx][mode][threads_index(threads)], wm->kernel, threads,
-                                    "cudaOccupancyMaxActiveBlocksPerMultiprocessor(lean)", &occ);
-    if (rc) return rc;
-    const int force = tune(QKNR_TUNE_CTAS_PER_SM);
-    if (force > 0) occ = std::min(occ, force);
-    wm->ctas_per_sm = occ;
-    wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
-    return QKNR_OK;
-}
-
 int plan(DeviceState &st, const Call &c, WorkMap *wm) {
-    const int kind = tune(QKNR_TUNE_KERNEL);
-    int rc;
-    if (kind == QKNR_KERNEL_BULK || kind == QKNR_KERNEL_ASYNC) {
-        if (!bulk_applies(c))
-            return fail(QKNR_ERR_UNSUPPORTED,
-                        "the bulk and async kernels need rope_dim %% 8 == 0 and a 16-byte aligned cos|sin table");
-        rc = kind == QKNR_KERNEL_BULK ? plan_bulk(st, c, wm) : plan_async(st, c, wm);
-    } else if (kind == QKNR_KERNEL_LEAN) {
-        rc = plan_lean(st, c, wm);
-    } else {
-        rc = plan_register(st, c, wm);
-    }
+    const int rc = plan_register(st, c, wm);
     if (rc) return rc;
     const int pdl = tune(QKNR_TUNE_PDL);
     wm->pdl = pdl < 0 ? 1 : pdl;
@@ -610,13 +409,12 @@ void log_launch(const WorkMap &wm, const Call &c) {
                                            c.dtype, wm.kind, wm.threads, wm.grid};
     std::lock_guard<std::mutex> lock(mu);
     if (!seen.insert(key).second) return;
-    static const char *const kinds[] = {"auto", "register", "bulk", "async", "lean"};
     std::fprintf(stderr,
                  "qknr: T=%lld n_qo=%d n_kv=%d head_dim=%d rope_dim=%d %s %s pos%s -> %s kernel, grid %d x %d, "
                  "%d CTAs/SM, %lld items (%d per token), %d passes per token, PDL %s\n",
                  c.num_tokens, c.n_qo, c.n_kv, c.head_dim, c.rope_dim, c.is_neox ? "neox" : "interleaved",
                  (c.dtype & 0xff) == QKNR_FP16 ? "fp16" : "bf16", (c.dtype & QKNR_POS_I64) ? "64" : "32",
-                 (wm.kind >= 0 && wm.kind <= 4) ? kinds[wm.kind] : "?", wm.grid, wm.threads, wm.ctas_per_sm,
+                 "register", wm.grid, wm.threads, wm.ctas_per_sm,
                  wm.items, wm.chunks_per_token, wm.passes_per_token, wm.pdl ? "on" : "off");
 }
 
@@ -631,91 +429,35 @@ int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = wm.pdl ? 1 : 0;
-    cudaError_t e;
-    if (wm.kind == QKNR_KERNEL_ASYNC) {
-        qknr::AsyncParams prm = {};
-        prm.q = static_cast<char *>(c.q);
-        prm.k = static_cast<char *>(c.k);
-        prm.q_w = static_cast<const uint4 *>(c.q_w);
-        prm.k_w = static_cast<const uint4 *>(c.k_w);
-        prm.cache = c.cache;
-        prm.positions = c.positions;
-        prm.status = status;
-        prm.q_stride_b = c.q_stride * 2;
-        prm.k_stride_b = c.k_stride * 2;
-        prm.head_stride_b = c.head_stride * 2;
-        prm.num_tokens = c.num_tokens;
-        prm.num_passes = wm.items;
-        prm.cache_len = c.cache_len;
-        prm.n_qo = c.n_qo;
-        prm.n_kv = c.n_kv;
-        prm.rope_dim = c.rope_dim;
-        prm.passes_per_token = wm.passes_per_token;
-        prm.stages = wm.stages;
-        prm.stage_bytes = wm.stage_bytes;
-        prm.eps = c.eps;
-        prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
-        cfg.dynamicSmemBytes = static_cast<size_t>(wm.smem_bytes);
-        void *args[] = {&prm};
-        e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
-    } else if (wm.kind == QKNR_KERNEL_BULK) {
-        BulkParams prm = {};
-        prm.q = static_cast<char *>(c.q);
-        prm.k = static_cast<char *>(c.k);
-        prm.q_w = static_cast<const uint4 *>(c.q_w);
-        prm.k_w = static_cast<const uint4 *>(c.k_w);
-        prm.cache = c.cache;
-        prm.positions = c.positions;
-        prm.status = status;
-        prm.q_stride_b = c.q_stride * 2;
-        prm.k_stride_b = c.k_stride * 2;
-        prm.head_stride_b = c.head_stride * 2;
-        prm.num_tiles = wm.items;
-        prm.cache_len = c.cache_len;
-        prm.n_qo = c.n_qo;
-        prm.n_kv = c.n_kv;
-        prm.rope_dim = c.rope_dim;
-        prm.chunks_per_token = wm.chunks_per_token;
-        prm.heads_per_chunk = wm.heads_per_chunk;
-        prm.stages = wm.stages;
-        prm.stage_bytes = wm.stage_bytes;
-        prm.heads_contig = (c.head_stride == c.head_dim) ? 1 : 0;
-        prm.eps = c.eps;
-        prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
-        cfg.dynamicSmemBytes = static_cast<size_t>(wm.smem_bytes);
-        void *args[] = {&prm};
-        e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
-    } else {
-        Params prm = {};
-        prm.q = static_cast<char *>(c.q);
-        prm.k = static_cast<char *>(c.k);
-        prm.q_w = static_cast<const uint4 *>(c.q_w);
-        prm.k_w = static_cast<const uint4 *>(c.k_w);
-        prm.cache = c.cache;
-        prm.positions = c.positions;
-        prm.status = status;
-        prm.q_stride_b = c.q_stride * 2;
-        prm.k_stride_b = c.k_stride * 2;
-        prm.head_stride_b = c.head_stride * 2;
-        prm.num_items = wm.items;
-        prm.cache_len = c.cache_len;
-        prm.n_qo = c.n_qo;
-        prm.n_kv = c.n_kv;
-        prm.rope_dim = c.rope_dim;
-        prm.chunks_per_token = wm.chunks_per_token;
-        prm.passes_per_token = wm.passes_per_token;
-        prm.cache_vec = (c.rope_dim % 8 == 0) && aligned(c.cache, 16);
-        prm.interleave = wm.interleave;
-        if (wm.chunks_per_token <= qknr::kBoundTable)
-            for (int ch = 0; ch <= wm.chunks_per_token; ++ch)
-                prm.pass_bound[ch] = static_cast<short>((static_cast<long long>(ch) * wm.passes_per_token) /
-                                                        wm.chunks_per_token);
-        prm.eps = c.eps;
-        prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
-        cfg.dynamicSmemBytes = 0;
-        void *args[] = {&prm};
-        e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
-    }
+    Params prm = {};
+    prm.q = static_cast<char *>(c.q);
+    prm.k = static_cast<char *>(c.k);
+    prm.q_w = static_cast<const uint4 *>(c.q_w);
+    prm.k_w = static_cast<const uint4 *>(c.k_w);
+    prm.cache = c.cache;
+    prm.positions = c.positions;
+    prm.status = status;
+    prm.q_stride_b = c.q_stride * 2;
+    prm.k_stride_b = c.k_stride * 2;
+    prm.head_stride_b = c.head_stride * 2;
+    prm.num_items = wm.items;
+    prm.cache_len = c.cache_len;
+    prm.n_qo = c.n_qo;
+    prm.n_kv = c.n_kv;
+    prm.rope_dim = c.rope_dim;
+    prm.chunks_per_token = wm.chunks_per_token;
+    prm.passes_per_token = wm.passes_per_token;
+    prm.cache_vec = (c.rope_dim % 8 == 0) && aligned(c.cache, 16);
+    prm.interleave = wm.interleave;
+    if (wm.chunks_per_token <= qknr::kBoundTable)
+        for (int ch = 0; ch <= wm.chunks_per_token; ++ch)
+            prm.pass_bound[ch] = static_cast<short>((static_cast<long long>(ch) * wm.passes_per_token) /
+                                                    wm.chunks_per_token);
+    prm.eps = c.eps;
+    prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
+    cfg.dynamicSmemBytes = 0;
+    void *args[] = {&prm};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return QKNR_OK;
 }
@@ -732,31 +474,12 @@ int run_checked(DeviceState &st, const WorkMap &wm, const Call &c, cudaStream_t 
                         cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail_cuda(e, "status read-back");
-    if (host_words[2]) {
-        e = cudaMemsetAsync(st.status + 2, 0, sizeof(unsigned long long), s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-        return fail(QKNR_ERR_WATCHDOG, "a kernel wait ran out (watchdog bits 0x%llx): results are incomplete",
-                    host_words[2]);
-    }
     if (host_words[0]) {
         return fail(QKNR_ERR_POSITION_OOB,
                     "%llu token(s) have positions outside [0, %lld); first bad token index %llu (left untouched)",
                     host_words[0], c.cache_len, host_words[1]);
     }
     return QKNR_OK;
-}
-
-// Watchdog self-test: one thread waits, with the bulk kernel's bounded wait,
-// on a shared-memory barrier that nothing arrives on. After the limit (about a
-// second) the wait gives up, the watchdog bit is set and the kernel returns,
-// exactly as a stalled bulk-kernel wait would; the context stays usable.
-__global__ void qknr_watchdog_selftest_kernel(unsigned long long *status) {
-    __shared__ __align__(8) unsigned long long bar;
-    if (threadIdx.x == 0) {
-        qknr::mbar_init(qknr::smem_u32(&bar), 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (!qknr::mbar_wait_bounded(qknr::smem_u32(&bar), 0u)) atomicOr(status + 2, qknr::kWatchdogBit);
-    }
 }
 
 int apply_impl(const Call &c, void *stream, bool checked) {
@@ -842,7 +565,7 @@ int apply_checked_noalloc_impl(const Call &c, void *stream) {
     rc = plan(slot.state, c, &wm);
     if (rc) return rc;
     std::lock_guard<std::mutex> lock(slot.state.checked_mu);
-    unsigned long long host_words[kStatusWords] = {0ull, 0ull, 0ull};
+    unsigned long long host_words[kStatusWords] = {0ull, 0ull};
     return run_checked(slot.state, wm, c, static_cast<cudaStream_t>(stream), host_words);
 }
 
@@ -1255,34 +978,6 @@ int qknr_apply_strided(void *q, void *k, const void *q_w, const void *k_w, const
     return apply_strided_impl(c, stream);
 }
 
-int qknr_selftest_watchdog(void *stream) {
-    DeviceState *st = current_state();
-    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
-    qknr_watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st->status);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail_cuda(e, "watchdog self-test launch");
-    return QKNR_OK;
-}
-
-int qknr_sync(void *stream) {
-    DeviceState *st = current_state();
-    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(st->checked_mu);
-    cudaError_t e = cudaMemcpyAsync(st->status_host + 2, st->status + 2, sizeof(unsigned long long),
-                                    cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return fail_cuda(e, "qknr_sync");
-    const unsigned long long bits = st->status_host[2];
-    if (bits) {
-        e = cudaMemsetAsync(st->status + 2, 0, sizeof(unsigned long long), s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-        return fail(QKNR_ERR_WATCHDOG, "a kernel wait ran out (watchdog bits 0x%llx): results are incomplete",
-                    bits);
-    }
-    return QKNR_OK;
-}
-
 int qknr_set_tuning(int key, int value) {
     std::call_once(g_env_once, read_env_tuning);
     if (key == QKNR_TUNE_RESET) {
@@ -1297,7 +992,9 @@ int qknr_set_tuning(int key, int value) {
 
 int qknr_get_tuning(int key, int *value) {
     if (!value) return fail(QKNR_ERR_INVALID_ARG, "value is null");
-    if (key <= 0 || key >= kNumTuneKeys) return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
+    if (key != QKNR_TUNE_PASSES && key != QKNR_TUNE_THREADS && key != QKNR_TUNE_CTAS_PER_SM &&
+        key != QKNR_TUNE_PDL && key != QKNR_TUNE_ORDER)
+        return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
     *value = tune(key);
     return QKNR_OK;
 }
@@ -1326,12 +1023,11 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     out[4] = wm.chunks_per_token;
     out[5] = wm.ctas_per_sm;
     out[6] = wm.pdl;
-    out[7] = wm.kind == QKNR_KERNEL_BULK ? wm.heads_per_chunk : wm.passes_per_token;
-    out[8] = (wm.kind == QKNR_KERNEL_REGISTER || wm.kind == QKNR_KERNEL_LEAN) ? qknr::kUnrollClass[wm.u_idx]
-                                                                            : wm.stages;
-    out[9] = wm.kind == QKNR_KERNEL_BULK ? wm.consumers : 0;
-    out[10] = wm.smem_bytes;
-    out[11] = wm.stage_bytes;
+    out[7] = wm.passes_per_token;
+    out[8] = qknr::kUnrollClass[wm.u_idx];
+    out[9] = wm.interleave ? 2 : 1;
+    out[10] = 0;
+    out[11] = 0;
     return QKNR_OK;
 }
 

@@ -7,9 +7,8 @@ namespace qknr {
 constexpr int kNumUnroll = 2;
 constexpr int kUnrollClass[kNumUnroll] = {2, 4};
 
-// head_dim classes
+// head_dim classes (80, 96 and 192 pad their lane groups to a power of two)
 constexpr int kNumHeadDim = 6;
-// 80, 96 and 192 (lane groups padded to a power of two): register kernel only
 constexpr int kHeadDims[kNumHeadDim] = {64, 96, 128, 192, 256, 80};
 
 // Kernel entry for (position type, head_dim class, mode, unroll class), or
@@ -20,18 +19,6 @@ const void *kernel_fp16(int pos64, int d_idx, int mode, int u_idx);
 // grid (QKNR_INPUTS_READY). Defined in qknr_inst_{bf16,fp16}_early.cu.
 const void *kernel_bf16_early(int pos64, int d_idx, int mode, int u_idx);
 const void *kernel_fp16_early(int pos64, int d_idx, int mode, int u_idx);
-
-// Bulk-copy ring kernel entry for (position type, head_dim class, mode).
-const void *bulk_kernel_bf16(int pos64, int d_idx, int mode);
-const void *bulk_kernel_fp16(int pos64, int d_idx, int mode);
-
-// Per-warp cp.async pipeline kernel entry for (position type, head_dim class, mode).
-const void *async_kernel_bf16(int pos64, int d_idx, int mode);
-const void *async_kernel_fp16(int pos64, int d_idx, int mode);
-
-// Register kernel with per-token state in shared memory, for (position type, head_dim class, mode).
-const void *lean_kernel_bf16(int pos64, int d_idx, int mode);
-const void *lean_kernel_fp16(int pos64, int d_idx, int mode);
 
 // One step of the unfused two-kernel baseline (op = kOpNorm or kOpRope), the
 // register kernel with 4 passes per item. Norm-only ignores pos64 and mode.

@@ -1,29 +1,11 @@
-// qknr_inst_bf16.cu -- explicit instantiations of the fused kernels (register and bulk-copy ring) for bf16 storage.
+// qknr_inst_bf16.cu -- explicit instantiations of the register kernel for bf16 storage: the fused op
+// (default reads) and the two steps of the unfused baseline.
 #include "qknr_dispatch.h"
-#include "qknr_async_kernel.cuh"
-#include "qknr_bulk_kernel.cuh"
 #include "qknr_kernel.cuh"
-#include "qknr_lean_kernel.cuh"
 #include "qknr_register_table.cuh"
 
 namespace qknr {
 namespace {
-
-template <class P, int D>
-const void *bulk_by_mode(int mode) {
-    return mode == kNeox ? reinterpret_cast<const void *>(&qknr_bulk_kernel<__nv_bfloat16, P, D, kNeox>)
-                         : reinterpret_cast<const void *>(&qknr_bulk_kernel<__nv_bfloat16, P, D, kInterleaved>);
-}
-
-template <class P>
-const void *bulk_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {   // head_dim 80 / 96 / 192: register kernel only
-        case 0: return bulk_by_mode<P, 64>(mode);
-        case 2: return bulk_by_mode<P, 128>(mode);
-        case 4: return bulk_by_mode<P, 256>(mode);
-        default: return nullptr;
-    }
-}
 
 template <int D>
 const void *unfused_by_op(int op, int pos64, int mode) {
@@ -38,47 +20,7 @@ const void *unfused_by_op(int op, int pos64, int mode) {
                          : reinterpret_cast<const void *>(&qknr_fused_kernel<__nv_bfloat16, int, D, kInterleaved, 4, kOpRope>);
 }
 
-template <class P, int D>
-const void *async_by_mode(int mode) {
-    return mode == kNeox ? reinterpret_cast<const void *>(&qknr_async_kernel<__nv_bfloat16, P, D, kNeox>)
-                         : reinterpret_cast<const void *>(&qknr_async_kernel<__nv_bfloat16, P, D, kInterleaved>);
-}
-
-template <class P>
-const void *async_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {   // head_dim 80 / 96 / 192: register kernel only
-        case 0: return async_by_mode<P, 64>(mode);
-        case 2: return async_by_mode<P, 128>(mode);
-        case 4: return async_by_mode<P, 256>(mode);
-        default: return nullptr;
-    }
-}
-
-template <class P, int D>
-const void *lean_by_mode(int mode) {
-    return mode == kNeox ? reinterpret_cast<const void *>(&qknr_lean_kernel<__nv_bfloat16, P, D, kNeox>)
-                         : reinterpret_cast<const void *>(&qknr_lean_kernel<__nv_bfloat16, P, D, kInterleaved>);
-}
-
-template <class P>
-const void *lean_by_head_dim(int d_idx, int mode) {
-    switch (d_idx) {   // head_dim 80 / 96 / 192: register kernel only
-        case 0: return lean_by_mode<P, 64>(mode);
-        case 2: return lean_by_mode<P, 128>(mode);
-        case 4: return lean_by_mode<P, 256>(mode);
-        default: return nullptr;
-    }
-}
-
 }  // namespace
-
-const void *lean_kernel_bf16(int pos64, int d_idx, int mode) {
-    return pos64 ? lean_by_head_dim<long long>(d_idx, mode) : lean_by_head_dim<int>(d_idx, mode);
-}
-
-const void *async_kernel_bf16(int pos64, int d_idx, int mode) {
-    return pos64 ? async_by_head_dim<long long>(d_idx, mode) : async_by_head_dim<int>(d_idx, mode);
-}
 
 const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode) {
     switch (d_idx) {
@@ -90,10 +32,6 @@ const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode) {
         case 5: return unfused_by_op<80>(op, pos64, mode);
         default: return nullptr;
     }
-}
-
-const void *bulk_kernel_bf16(int pos64, int d_idx, int mode) {
-    return pos64 ? bulk_by_head_dim<long long>(d_idx, mode) : bulk_by_head_dim<int>(d_idx, mode);
 }
 
 const void *kernel_bf16(int pos64, int d_idx, int mode, int u_idx) {

@@ -89,7 +89,7 @@ def test_can_use_contains_the_pages_set():
 def test_can_use_rejects():
     assert qknr.qknr_can_use(72, 64, 0, 0) == 0          # head_dim outside {64,80,96,128,192,256}
     assert qknr.qknr_can_use(80, 32, 1, 0) == 1          # Phi-2-like: head_dim 80, NeoX rotary 32
-    assert qknr.qknr_can_use(96, 64, 1, 0) == 1          # head_dim 96 (register kernel)
+    assert qknr.qknr_can_use(96, 64, 1, 0) == 1          # head_dim 96
     assert qknr.qknr_can_use(192, 96, 1, 0) == 1
     assert qknr.qknr_can_use(128, 0, 0, 0) == 0          # rope_dim 0
     assert qknr.qknr_can_use(128, 130, 0, 0) == 0        # rope_dim > head_dim
@@ -104,18 +104,19 @@ def test_can_use_rejects():
 
 def test_set_tuning_validation():
     K = qknr.TUNE_KEYS
-    bad = [(K["kernel"], 5), (K["passes"], 5), (K["threads"], 96), (K["ctas_per_sm"], -1),
-           (K["pdl"], 2), (K["consumers"], 17), (K["stages"], 33), (K["tile_bytes"], 100), (K["order"], 3), (99, 0)]
+    bad = [(K["passes"], 5), (K["threads"], 96), (K["ctas_per_sm"], -1), (K["ctas_per_sm"], 33),
+           (K["pdl"], 2), (K["order"], 3), (1, 1), (6, 4), (7, 8), (8, 4096), (99, 0)]
     for key, value in bad:
         assert qknr.qknr_set_tuning(key, value) == 2, (key, value)
     assert "tuning key" in qknr.qknr_last_error()
-    qknr.set_tuning(kernel=1, passes=2, threads=128, ctas_per_sm=3, pdl=0, consumers=4, stages=8,
-                    tile_bytes=4096)
-    assert qknr.get_tuning("kernel") == 1 and qknr.get_tuning("stages") == 8
-    assert qknr.get_tuning("pdl") == 0
+    v = ctypes.c_int(0)
+    assert qknr.qknr_get_tuning(7, ctypes.byref(v)) == 2      # keys of retired kernels are unknown
+    qknr.set_tuning(passes=2, threads=128, ctas_per_sm=3, pdl=0, order=1)
+    assert qknr.get_tuning("passes") == 2 and qknr.get_tuning("threads") == 128
+    assert qknr.get_tuning("pdl") == 0 and qknr.get_tuning("order") == 1
     qknr.set_tuning(reset=True)
-    assert qknr.get_tuning("kernel") == 0 and qknr.get_tuning("pdl") == -1
-    assert qknr.get_tuning("tile_bytes") == 0
+    assert qknr.get_tuning("passes") == 0 and qknr.get_tuning("pdl") == -1
+    assert qknr.get_tuning("order") == 0
 
 
 def test_apply_rejects_cpu_tensors():
@@ -151,12 +152,11 @@ print(rc, q.qknr_last_error())
 rc2 = q.qknr_apply_checked(16, 16, 16, 16, 16, 4, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 1e-6, 0, None)
 out = (ctypes.c_int64 * 12)()
 rc3 = q.qknr_query_work_map(8, 1, 1, 128, 128, 0, 0, out)
-rc4 = q.qknr_sync(None)
+rc4 = q.qknr_apply_unfused(16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 1e-6, 0, None)
 rc5 = q.qknr_apply_host(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 1e-6, 0,
                         0, 0, None)
 rc6 = q.qknr_apply_strided(16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 128, 1e-6, 0, None)
-rc7 = q.qknr_selftest_watchdog(None)
-print(rc2, rc3, rc4, rc5, rc6, rc7)
+print(rc2, rc3, rc4, rc5, rc6)
 """
 
 
@@ -168,7 +168,7 @@ def test_calls_before_init_are_refused():
     assert r.returncode == 0, r.stderr
     first, second = r.stdout.strip().splitlines()[-2:]
     assert first.startswith("1 ") and "qknr_init" in first
-    assert second.split() == ["1", "1", "1", "1", "1", "1"]
+    assert second.split() == ["1", "1", "1", "1", "1"]
 
 
 def test_four_d_inputs_view_or_refuse():

@@ -36,7 +36,7 @@ def qknr():
     q.init(0)
     q.set_tuning(reset=True)
     yield q
-    q.sync()
+    torch.cuda.synchronize()
 
 
 def _host_inputs(cpu, w, pad):

@@ -1,9 +1,10 @@
 """The PyTorch custom-op registration (torch.ops.qknr.fused_inplace_qknorm_rope).
 
 CPU: the schema declares q and k as mutated and the op returns nothing; the
-shape gate agrees with the C ABI's. GPU: the op gives the same bits as the
-direct call, eagerly and under torch.compile (aot_eager backend, one graph),
-where the mutation must be visible to the code after the op."""
+shape gate agrees with the C ABI's. GPU: the op matches the CPU oracle element
+by element and gives the same bits as the direct call, eagerly and under
+torch.compile (aot_eager backend, one graph), where the mutation must be
+visible to the code after the op."""
 import os
 import sys
 
@@ -12,8 +13,17 @@ import torch
 
 sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 
+import oracle  # noqa: E402
 import workloads  # noqa: E402
 from qk_rmsnorm_rope_gb300 import torch_op  # noqa: E402
+
+
+def _assert_oracle(got_q, got_k, cpu, w):
+    eq, ek = oracle.apply(cpu["q"], cpu["k"], cpu["q_w"], cpu["k_w"], cpu["cos_sin_cache"],
+                          cpu["positions"], is_neox=w.is_neox, eps=w.eps)
+    for got, exp, what in ((got_q, eq, "q"), (got_k, ek, "k")):
+        v = oracle.max_violation(got.reshape(exp.shape).double().cpu().numpy(), exp, w.torch_dtype)
+        assert v <= 1.0, f"{what}: max error {v:.3f} x tolerance"
 
 
 def test_schema_declares_mutation():
@@ -58,6 +68,8 @@ def test_op_matches_direct_call_eager_and_compiled():
     cq, ck = compiled(src["q"], src["k"], src["q_w"], src["k_w"], src["cos_sin_cache"],
                       src["positions"])
     torch.cuda.synchronize()
+    _assert_oracle(eager["q"], eager["k"], cpu, w)
+    _assert_oracle(cq, ck, cpu, w)
     for d in (eager,):
         assert torch.equal(d["q"], ref["q"]) and torch.equal(d["k"], ref["k"])
     assert torch.equal(cq, ref["q"]) and torch.equal(ck, ref["k"])
@@ -68,7 +80,8 @@ def test_op_matches_direct_call_eager_and_compiled():
 @pytest.mark.gpu
 def test_op_takes_model_layout_and_host_positions():
     """The registered op on [B, S, H, D] q/k and positions given on the host
-    (converted like the reference wrapper does): the bits of the 3-D call."""
+    (converted like the reference wrapper does): within the oracle's bound,
+    and the bits of the 3-D call."""
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
     import qk_rmsnorm_rope_gb300 as q
@@ -84,5 +97,6 @@ def test_op_takes_model_layout_and_host_positions():
     torch.ops.qknr.fused_inplace_qknorm_rope(q4, k4, dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
                                              cpu["positions"].to(torch.int64), False, w.eps)
     torch.cuda.synchronize()
+    _assert_oracle(q4, k4, cpu, w)
     assert torch.equal(dev["q"].view(torch.int16), ref["q"].view(torch.int16))
     assert torch.equal(dev["k"].view(torch.int16), ref["k"].view(torch.int16))
