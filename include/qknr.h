@@ -276,13 +276,16 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
 #define QKNR_TUNE_PDL 5         /* programmatic dependent launch: -1 auto (on), 0 off, 1 on */
 #define QKNR_TUNE_ORDER 9       /* item order: 0 auto (= 2), 1 a contiguous range per warp,
                                    2 interleaved (warp w takes items w, w + W, ...) */
+#define QKNR_TUNE_PREFETCH 10   /* items per warp whose q/k rows (and the first positions) are
+                                   prefetched into L2 while the kernel waits for the previous one
+                                   on the stream: -1 none, 0 auto (= 4), 1..4 */
 
 /*
  * Process-wide launch tuning, for benchmarks and tests; results do not depend
  * on it (every setting gives the same bits). Invalid values return
  * QKNR_ERR_INVALID_ARG and change nothing. The environment variable
- * QKNR_TUNE="passes=4,threads=256,ctas=2,pdl=1,order=2" sets the same keys at
- * first use.
+ * QKNR_TUNE="passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1" sets the
+ * same keys at first use.
  */
 int qknr_set_tuning(int key, int value);
 int qknr_get_tuning(int key, int *value);
@@ -297,7 +300,8 @@ int qknr_get_tuning(int key, int *value);
  *  0 kernel (QKNR_KERNEL_REGISTER)  1 grid CTAs  2 threads per CTA
  *  3 warp items  4 items per token  5 resident CTAs per SM  6 PDL on
  *  7 warp passes per token  8 unroll class (passes of loads in flight)
- *  9 item order (1 contiguous, 2 interleaved)  10, 11 reserved (0)
+ *  9 item order (1 contiguous, 2 interleaved)  10 items per warp prefetched
+ *    into L2 before the wait for the previous kernel  11 reserved (0)
  */
 int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
                         int is_neox, int dtype, int64_t *out);

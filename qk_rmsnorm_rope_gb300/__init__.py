@@ -42,9 +42,10 @@ QKNR_KERNEL_REGISTER = 1
 QKNR_HOST_AUTO, QKNR_HOST_STAGED, QKNR_HOST_DIRECT = 0, 1, 2
 HOST_MODES = {"auto": QKNR_HOST_AUTO, "staged": QKNR_HOST_STAGED, "direct": QKNR_HOST_DIRECT}
 # QKNR_TUNE_* keys (include/qknr.h)
-TUNE_KEYS = {"reset": 0, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5, "order": 9}
+TUNE_KEYS = {"reset": 0, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5, "order": 9,
+             "prefetch": 10}
 WORK_MAP_FIELDS = ["kernel", "grid", "threads", "items", "items_per_token", "ctas_per_sm", "pdl",
-                   "passes_per_token", "unroll", "order", "reserved10", "reserved11"]
+                   "passes_per_token", "unroll", "order", "prefetch_items", "reserved11"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -450,6 +451,5 @@ def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int
     d = dict(zip(WORK_MAP_FIELDS, [int(v) for v in out]))
     d["kernel"] = {QKNR_KERNEL_REGISTER: "register"}.get(d["kernel"], d["kernel"])
     d["order"] = {1: "contiguous", 2: "interleaved"}.get(d["order"], d["order"])
-    for key in ("reserved10", "reserved11"):
-        d.pop(key)
+    d.pop("reserved11")
     return d

@@ -59,10 +59,12 @@ int fail_cuda(cudaError_t e, const char *what) {
 }
 
 // ------------------------------------------------------------------ tuning
-constexpr int kNumTuneKeys = 10;  // keys 2..5 and 9 (QKNR_TUNE_*); the other slots are unused
+constexpr int kNumTuneKeys = 11;  // keys 2..5, 9 and 10 (QKNR_TUNE_*); the other slots are unused
 // the value that means "automatic" for each key
-constexpr int kTuneAuto[kNumTuneKeys] = {0, 0, 0, 0, 0, -1, 0, 0, 0, 0};
-std::atomic<int> g_tune[kNumTuneKeys] = {{0}, {0}, {0}, {0}, {0}, {-1}, {0}, {0}, {0}, {0}};
+constexpr int kTuneAuto[kNumTuneKeys] = {0, 0, 0, 0, 0, -1, 0, 0, 0, 0, 0};
+std::atomic<int> g_tune[kNumTuneKeys] = {{0}, {0}, {0}, {0}, {0}, {-1}, {0}, {0}, {0}, {0}, {0}};
+constexpr int kAutoPrefetchItems = 4;  // items per warp prefetched into L2 before the wait (automatic)
+constexpr int kMaxPrefetchItems = 4;
 std::once_flag g_env_once;
 
 int tune_check(int key, int value) {
@@ -86,12 +88,17 @@ int tune_check(int key, int value) {
             return (value >= 0 && value <= 2)
                        ? QKNR_OK
                        : fail(QKNR_ERR_INVALID_ARG, "order must be 0 (auto), 1 (contiguous) or 2 (interleaved)");
+        case QKNR_TUNE_PREFETCH:
+            return (value >= -1 && value <= kMaxPrefetchItems)
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "prefetch must be -1 (none), 0 (auto) or 1..%d items",
+                              kMaxPrefetchItems);
         default:
             return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
     }
 }
 
-// QKNR_TUNE="passes=4,threads=256,ctas=2,pdl=1,order=2"
+// QKNR_TUNE="passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1"
 void read_env_tuning() {
     const char *s = std::getenv("QKNR_TUNE");
     if (!s) return;
@@ -100,7 +107,7 @@ void read_env_tuning() {
         int key;
     } names[] = {{"passes", QKNR_TUNE_PASSES}, {"threads", QKNR_TUNE_THREADS},
                  {"ctas", QKNR_TUNE_CTAS_PER_SM}, {"pdl", QKNR_TUNE_PDL},
-                 {"order", QKNR_TUNE_ORDER}};
+                 {"order", QKNR_TUNE_ORDER},      {"prefetch", QKNR_TUNE_PREFETCH}};
     std::string spec(s);
     size_t pos = 0;
     while (pos < spec.size()) {
@@ -202,6 +209,7 @@ struct WorkMap {
     int chunks_per_token = 0;
     int passes_per_token = 0, max_passes = 0, u_idx = 0;
     int interleave = 0;   // item order
+    int prefetch_items = 0;  // items per warp prefetched into L2 before the wait
     const void *kernel = nullptr;
 };
 
@@ -272,6 +280,8 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     wm->ctas_per_sm = occ;
     wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
     wm->interleave = tune(QKNR_TUNE_ORDER) == 1 ? 0 : 1;   // interleaved unless asked otherwise
+    const int pf = tune(QKNR_TUNE_PREFETCH);
+    wm->prefetch_items = pf < 0 ? 0 : (pf == 0 ? kAutoPrefetchItems : pf);
     return QKNR_OK;
 }
 
@@ -307,6 +317,8 @@ int plan_unfused(DeviceState &st, const Call &c, int op, WorkMap *wm) {
     if (rc) return rc;
     wm->ctas_per_sm = occ;
     wm->grid = persistent_grid(wm->items, wm->threads, occ, st.sm_count);
+    const int pf = tune(QKNR_TUNE_PREFETCH);
+    wm->prefetch_items = pf < 0 ? 0 : (pf == 0 ? kAutoPrefetchItems : pf);
     const int pdl = tune(QKNR_TUNE_PDL);
     wm->pdl = pdl < 0 ? 1 : pdl;
     return QKNR_OK;
@@ -449,6 +461,7 @@ int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStr
     prm.passes_per_token = wm.passes_per_token;
     prm.cache_vec = (c.rope_dim % 8 == 0) && aligned(c.cache, 16);
     prm.interleave = wm.interleave;
+    prm.prefetch_items = wm.prefetch_items;
     if (wm.chunks_per_token <= qknr::kBoundTable)
         for (int ch = 0; ch <= wm.chunks_per_token; ++ch)
             prm.pass_bound[ch] = static_cast<short>((static_cast<long long>(ch) * wm.passes_per_token) /
@@ -993,7 +1006,7 @@ int qknr_set_tuning(int key, int value) {
 int qknr_get_tuning(int key, int *value) {
     if (!value) return fail(QKNR_ERR_INVALID_ARG, "value is null");
     if (key != QKNR_TUNE_PASSES && key != QKNR_TUNE_THREADS && key != QKNR_TUNE_CTAS_PER_SM &&
-        key != QKNR_TUNE_PDL && key != QKNR_TUNE_ORDER)
+        key != QKNR_TUNE_PDL && key != QKNR_TUNE_ORDER && key != QKNR_TUNE_PREFETCH)
         return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
     *value = tune(key);
     return QKNR_OK;
@@ -1026,7 +1039,7 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     out[7] = wm.passes_per_token;
     out[8] = qknr::kUnrollClass[wm.u_idx];
     out[9] = wm.interleave ? 2 : 1;
-    out[10] = 0;
+    out[10] = wm.prefetch_items;
     out[11] = 0;
     return QKNR_OK;
 }

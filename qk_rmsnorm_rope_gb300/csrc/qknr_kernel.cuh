@@ -26,6 +26,8 @@
 //    before any arithmetic, to keep many bytes in flight per SM.
 //  * Grid: persistent, at most one wave of resident CTAs; programmatic
 //    dependent launch lets the next kernel in the stream get resident early.
+//  * While it waits for the previous grid, each warp prefetches its first
+//    items' q/k rows and its first positions into L2 (see the kernel body).
 #pragma once
 
 #include <cstdint>
@@ -59,6 +61,7 @@ struct Params {
     int passes_per_token;         // ceil((n_qo + n_kv) / heads_per_pass)
     int cache_vec;                // 1: cos/sin rows may be read as float4
     int interleave;               // 1: warp w takes items w, w + W, ... (W warps); 0: a contiguous range
+    int prefetch_items;           // items per warp whose q/k rows are prefetched into L2 before the wait
     float eps;
     float inv_d;                  // 1 / head_dim in fp32 (exact for 64, 128 and 256; for 80, 96 and 192
                                   // the rounded reciprocal moves the mean by at most about one ulp)
@@ -68,6 +71,48 @@ struct Params {
 template <class P>
 __device__ __forceinline__ long long load_position(const void *positions, long long t) {
     return static_cast<long long>(__ldg(reinterpret_cast<const P *>(positions) + t));
+}
+
+// Pull the line holding ptr into L2 (no data comes back to the SM).
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// Before a launch waits for the previous grid in its stream, each warp pulls
+// its first p.prefetch_items items' q/k rows and the positions of its first
+// 32 items into L2. A prefetch brings nothing back to the SM, and L2 is where
+// every store of the previous grid lands, so a line it brings in cannot go
+// stale. It uses DRAM time that the previous grid's last warps leave idle, and
+// the first loads after the wait hit L2. Not inlined, so that its address
+// arithmetic does not take registers from the item loop.
+template <class P, int HPW, int UMAX, int OP>
+__device__ __noinline__ void prefetch_first_items(const Params &p, long long it_begin, long long it_end,
+                                                  long long it_step, int g, int va, int vb, bool active,
+                                                  int lane) {
+    const int chunks = p.chunks_per_token;
+    const int H = p.n_qo + p.n_kv;
+    for (int j = 0; j < p.prefetch_items; ++j) {
+        const long long itp = it_begin + j * it_step;
+        if (itp >= it_end) break;
+        const long long tp = itp / chunks;
+        const int chp = static_cast<int>(itp - tp * chunks);
+        const int pbp = (chp * p.passes_per_token) / chunks;
+        const int pep = ((chp + 1) * p.passes_per_token) / chunks;
+        const char *q_row = p.q + tp * p.q_stride_b;
+        const char *k_row = p.k + tp * p.k_stride_b - static_cast<long long>(p.n_qo) * p.head_stride_b;
+        for (int u = 0; u < UMAX; ++u) {
+            const int h = (pbp + u) * HPW + g;
+            if (pbp + u < pep && h < H && active) {
+                const char *base = (h < p.n_qo ? q_row : k_row) + static_cast<long long>(h) * p.head_stride_b;
+                prefetch_l2(base + 16 * va);
+                prefetch_l2(base + 16 * vb);
+            }
+        }
+    }
+    if (OP != kOpNorm) {
+        const long long it_j = it_begin + lane * it_step;
+        if (it_j < it_end) prefetch_l2(reinterpret_cast<const P *>(p.positions) + it_j / chunks);
+    }
 }
 
 // T: storage type (bf16/half); P: position type (int / long long);
@@ -85,15 +130,6 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     constexpr int LPH = NVH <= 1 ? 1 : NVH <= 2 ? 2 : NVH <= 4 ? 4 : NVH <= 8 ? 8 : NVH <= 16 ? 16 : 32;
     constexpr int HPW = kWarp / LPH;    // heads per warp pass
     static_assert(D % 16 == 0 && NVH >= 1 && NVH <= kWarp, "head_dim");
-
-#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 900)
-    // Programmatic dependent launch: do not touch memory before the previous
-    // grid in the stream has completed; then let the next grid get resident.
-    if (!EARLY) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        asm volatile("griddepcontrol.launch_dependents;");
-    }
-#endif
 
     const int lane = threadIdx.x & (kWarp - 1);
     const int g = lane / LPH;           // head slot within the pass
@@ -130,10 +166,6 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
         rot_lane = false;
     }
 
-    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-    const uint4 wqa = active ? __ldg(p.q_w + va) : zero4, wqb = active ? __ldg(p.q_w + vb) : zero4;
-    const uint4 wka = active ? __ldg(p.k_w + va) : zero4, wkb = active ? __ldg(p.k_w + vb) : zero4;
-
     const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long warp_id = gtid / kWarp;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) / kWarp;
@@ -143,6 +175,24 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     const long long it_begin = p.interleave ? warp_id : warp_id * p.num_items / nwarps;
     const long long it_end = p.interleave ? p.num_items : (warp_id + 1) * p.num_items / nwarps;
     const long long it_step = p.interleave ? nwarps : 1;
+
+    // Before waiting for the previous grid: pull this warp's first items' q/k
+    // rows and its first positions into L2 (prefetch_first_items).
+    if (p.prefetch_items > 0)
+        prefetch_first_items<P, HPW, UMAX, OP>(p, it_begin, it_end, it_step, g, va, vb, active, lane);
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 900)
+    // Programmatic dependent launch: read nothing before the previous grid in
+    // the stream has completed; then let the next grid get resident.
+    if (!EARLY) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;");
+    }
+#endif
+
+    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 wqa = active ? __ldg(p.q_w + va) : zero4, wqb = active ? __ldg(p.q_w + vb) : zero4;
+    const uint4 wka = active ? __ldg(p.k_w + va) : zero4, wkb = active ? __ldg(p.k_w + vb) : zero4;
 
     // cos and (sign-free) sin per owned element. Interleaved: c[m]/s[m] serve
     // pair m of vector a (m < 4) and pair m-4 of vector b (m >= 4). NeoX split:

@@ -201,6 +201,10 @@ TUNINGS = [
     dict(order=2, passes=3, threads=512),
     dict(ctas_per_sm=1),
     dict(passes=1, pdl=0, order=1),
+    dict(prefetch=-1),
+    dict(prefetch=1, order=1),
+    dict(prefetch=2, passes=1, threads=64),
+    dict(prefetch=4, pdl=0),
 ]
 
 
@@ -209,8 +213,8 @@ def test_tunings_agree_bit_for_bit(qknr, tuning):
     """Per-head results do not depend on the launch tuning: every forced setting
     gives the same bits as the automatic one, and all match the oracle. Covers
     one to four passes per item, several items per token, both item orders,
-    one or two CTAs per SM and launches with and without programmatic
-    dependent launch."""
+    one or two CTAs per SM, launches with and without programmatic dependent
+    launch, and every depth of the L2 prefetch before the wait."""
     for name, T in (("mha_neox", 97), ("fused_qkv", 41), ("tiny", 16), ("gqa", 50)):
         base = workloads.get(name)
         w = workloads.scaled(base, T, cache_len=min(base.cache_len, 4096))
@@ -240,6 +244,7 @@ def test_work_map_choice(qknr):
     assert m["kernel"] == "register" and m["order"] == "interleaved"
     assert m["unroll"] == 4 and m["passes_per_token"] == 12 and m["items_per_token"] == 3
     assert m["items"] == 4608 * 3 and m["threads"] == 256 and m["pdl"] == 1
+    assert m["prefetch_items"] == 4
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert m["grid"] <= m["ctas_per_sm"] * sms
     small = qknr.work_map(4, 4, 2, 128, 6, False, bf)
