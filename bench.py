@@ -44,8 +44,9 @@ default), and prints the same config dict as this arm.
 
 Other options: --tokens N (decode-sized calls), --graph (replays of a CUDA
 graph of calls), --inputs-ready (calls that set QKNR_INPUTS_READY), --variant
-unfused (the two-kernel chain), --ceiling (torch's own in-place elementwise
-kernel at the same bytes).
+unfused (the two-kernel chain), --tune (qknr_tune picks each configuration's
+launch first), --ceiling (torch's own in-place elementwise kernel at the same
+bytes).
 """
 from __future__ import annotations
 
@@ -393,6 +394,14 @@ def measure_config(q, args, w: workloads.Workload, rank: int, world: int, device
     torch.cuda.synchronize()
     entry = "qknr_apply_unfused" if args.variant == "unfused" else "qknr_apply"
     launches_per_step = 2 if args.variant == "unfused" else 1
+    tuned = None
+    if args.tune and args.variant == "fused":
+        # qknr_tune for this call shape (timed on the library's own scratch
+        # buffers, before and outside the warm-up and the timed region)
+        r0 = reps[0]
+        tuned = q.tune(r0["q"], r0["k"], r0["q_w"], r0["k_w"], r0["cos_sin_cache"], r0["positions"],
+                       is_neox=w.is_neox, stream=stream, inputs_ready=args.inputs_ready)
+        torch.cuda.synchronize()
     calls = [PreparedCall(q, r, w, sh, entry, args.inputs_ready) for r in reps]
     algo = workloads.algorithmic_bytes(w)
     heads = workloads.num_heads_total(w)
@@ -446,7 +455,8 @@ def measure_config(q, args, w: workloads.Workload, rank: int, world: int, device
                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                   "launch": (f"CUDA graph of {n_rep} calls, replayed" if args.graph
                              else "one C-ABI call per step from Python")
-                            + (", QKNR_INPUTS_READY" if args.inputs_ready else ""),
+                            + (", QKNR_INPUTS_READY" if args.inputs_ready else "")
+                            + (", work map chosen by qknr_tune" if tuned else ""),
                   "work_map": wm},
         "heads_per_s": world * heads * steps / secs,
         "pct_of_peak": round(100.0 * achieved / peak, 2),
@@ -836,6 +846,9 @@ def main(argv: Optional[List[str]] = None) -> int:
                     help="time replays of a CUDA graph of calls (GPU time per call, no host launch rate)")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
                     help="unfused: time the two-kernel RMSNorm-then-RoPE chain instead")
+    ap.add_argument("--tune", action="store_true",
+                    help="call qknr_tune for each configuration's shape first (the launch it picks "
+                         "on scratch buffers is then used)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

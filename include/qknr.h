@@ -293,10 +293,42 @@ int qknr_get_tuning(int key, int *value);
 /* Logging: with the environment variable QKNR_LOG=1, every distinct call shape
  * prints one line on stderr with the kernel, grid and work map chosen for it. */
 
+/*
+ * Measure the launch choices for one call shape and keep the fastest: for
+ * later calls with exactly these sizes, strides and dtype (QKNR_INPUTS_READY
+ * included) on the current device, qknr_apply, qknr_apply_checked and the
+ * host and strided entry points use the chosen passes per item and L2
+ * prefetch depth instead of the fixed rule. Explicit qknr_set_tuning values
+ * still take precedence. The op has no counterpart of this on the pages,
+ * whose kernels fix their launch at compile time.
+ *
+ * The candidates (passes per item 4, 3, 2 or 1 where they chunk a token
+ * differently; prefetch of 4, 2, 1 or no items) run on scratch buffers with
+ * the given layout, zero-filled, never on the caller's data, each timed with
+ * CUDA events over about 2 ms of launches in three alternating rounds; the
+ * one with the lowest median time per launch is kept. Input replicas rotate so
+ * that no timed launch finds its inputs in L2.
+ *
+ * Arguments as for qknr_apply (num_tokens >= 1), without pointers. The call
+ * allocates and frees its scratch (q and k at most 8 GiB, plus weights, a
+ * cos|sin table of min(num_tokens, 65536) rows and positions), so it belongs
+ * at set-up time, not on a hot path or inside a stream capture, and it waits
+ * for `stream`. out (NULL allowed): QKNR_WORK_MAP_FIELDS values, the chosen
+ * work map as qknr_query_work_map reports it, with out[11] the measured time
+ * per launch in nanoseconds. A choice is kept until qknr_shutdown; tuning the
+ * same shape again replaces it. Errors: QKNR_ERR_NOT_INITIALIZED,
+ * QKNR_ERR_INVALID_ARG / UNSUPPORTED / MISALIGNED as qknr_apply would return
+ * for the layout, QKNR_ERR_CUDA (scratch allocation or launch).
+ */
+int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim, int is_neox,
+              int64_t q_stride, int64_t k_stride, int64_t head_stride, int dtype, void *stream,
+              int64_t *out);
+
 #define QKNR_WORK_MAP_FIELDS 12
 /*
- * The launch qknr_apply would make for these sizes (no launch, no pointers;
- * assumes a 16-byte aligned cos|sin table). out[QKNR_WORK_MAP_FIELDS]:
+ * The launch qknr_apply would make for these sizes with contiguous q and k
+ * (no launch, no pointers; assumes a 16-byte aligned cos|sin table), including
+ * a choice qknr_tune made for that shape. out[QKNR_WORK_MAP_FIELDS]:
  *  0 kernel (QKNR_KERNEL_REGISTER)  1 grid CTAs  2 threads per CTA
  *  3 warp items  4 items per token  5 resident CTAs per SM  6 PDL on
  *  7 warp passes per token  8 unroll class (passes of loads in flight)

@@ -21,10 +21,10 @@ __all__ = [
     "QKNR_HOST_DIRECT", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
     "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-    "qknr_apply_host", "qknr_apply_strided",
+    "qknr_apply_host", "qknr_apply_strided", "qknr_tune",
     "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map", "TUNE_KEYS",
     "init", "apply", "apply_checked", "apply_unfused", "apply_host", "can_use", "dtype_code",
-    "work_map", "set_tuning", "get_tuning",
+    "work_map", "set_tuning", "get_tuning", "tune",
 ]
 
 QKNR_BF16 = 0x000
@@ -85,13 +85,15 @@ def _load() -> ctypes.CDLL:
                                     i64, i64, i64, f32, i32, i64, i32, vp]
     lib.qknr_apply_strided.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
                                        i64, i64, i64, i64, f32, i32, vp]
+    lib.qknr_tune.argtypes = [i64, i32, i32, i32, i32, i32, i64, i64, i64, i32, vp,
+                              ctypes.POINTER(ctypes.c_int64)]
     lib.qknr_set_tuning.argtypes = [i32, i32]
     lib.qknr_get_tuning.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
     lib.qknr_query_work_map.argtypes = [i64, i32, i32, i32, i32, i32, i32,
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
                  "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-                 "qknr_apply_host", "qknr_apply_strided", "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
+                 "qknr_apply_host", "qknr_apply_strided", "qknr_tune", "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -188,6 +190,12 @@ def qknr_apply_strided(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens, n_q
     return _get_lib().qknr_apply_strided(q, k, q_w, k_w, cos_sin_cache, positions, num_tokens,
                                          n_qo, n_kv, head_dim, rope_dim, int(is_neox), q_stride,
                                          k_stride, q_head_stride, k_head_stride, eps, dtype, stream)
+
+
+def qknr_tune(num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, q_stride, k_stride, head_stride,
+              dtype, stream, out) -> int:
+    return _get_lib().qknr_tune(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox), q_stride,
+                                k_stride, head_stride, dtype, stream, out)
 
 
 def qknr_set_tuning(key: int, value: int) -> int:
@@ -440,6 +448,36 @@ def get_tuning(name: str) -> int:
     v = ctypes.c_int(0)
     _check(qknr_get_tuning(TUNE_KEYS[name], ctypes.byref(v)))
     return v.value
+
+
+def tune(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, head_dim: int = 0,
+         rope_dim: int = 0, stream=None, inputs_ready: bool = False) -> Dict[str, int]:
+    """qknr_tune for the call apply() would make with these tensors: only their
+    shapes, strides and dtypes are read (the candidates run on scratch
+    buffers). Later apply() calls with the same shapes, strides and dtypes use
+    the launch it chose. Returns the chosen work map, with ``ns_per_launch``
+    measured. A set-up-time call: it allocates scratch and waits for the
+    stream."""
+    import torch
+    q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
+    T, n_qo, n_kv, D, R, qs, ks, hs, code = _marshal(
+        q, k, q_w, k_w, cos_sin_cache, positions, is_neox, head_dim, rope_dim, same_device=False)
+    if q.device.type != "cuda":
+        raise QknrError(2, "q must be a CUDA tensor")
+    if inputs_ready:
+        code |= QKNR_INPUTS_READY
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    out = (ctypes.c_int64 * len(WORK_MAP_FIELDS))()
+    with torch.cuda.device(q.device):
+        _check(qknr_tune(T, n_qo, n_kv, D, R, int(bool(is_neox)), qs, ks, hs, code, stream, out))
+    d = dict(zip(WORK_MAP_FIELDS, [int(v) for v in out]))
+    d["kernel"] = {QKNR_KERNEL_REGISTER: "register"}.get(d["kernel"], d["kernel"])
+    d["order"] = {1: "contiguous", 2: "interleaved"}.get(d["order"], d["order"])
+    d["ns_per_launch"] = d.pop("reserved11")
+    return d
 
 
 def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int,

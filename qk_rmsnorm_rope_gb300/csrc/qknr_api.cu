@@ -31,6 +31,8 @@
 #include <array>
 #include <set>
 #include <string>
+#include <unordered_map>
+#include <vector>
 
 namespace {
 
@@ -131,6 +133,34 @@ int tune(int key) {
 }
 
 // ------------------------------------------------------------------ devices
+// A call shape and layout that qknr_tune measured, and the work map it chose.
+struct ShapeKey {
+    long long num_tokens, q_stride, k_stride, head_stride;
+    int n_qo, n_kv, head_dim, rope_dim, is_neox, dtype;
+    bool operator==(const ShapeKey &o) const {
+        return num_tokens == o.num_tokens && q_stride == o.q_stride && k_stride == o.k_stride &&
+               head_stride == o.head_stride && n_qo == o.n_qo && n_kv == o.n_kv && head_dim == o.head_dim &&
+               rope_dim == o.rope_dim && is_neox == o.is_neox && dtype == o.dtype;
+    }
+};
+struct ShapeHash {
+    size_t operator()(const ShapeKey &k) const {
+        size_t h = std::hash<long long>()(k.num_tokens);
+        for (long long v : {k.q_stride, k.k_stride, k.head_stride, static_cast<long long>(k.n_qo),
+                            static_cast<long long>(k.n_kv), static_cast<long long>(k.head_dim),
+                            static_cast<long long>(k.rope_dim), static_cast<long long>(k.is_neox),
+                            static_cast<long long>(k.dtype)})
+            h = h * 1000003u ^ std::hash<long long>()(v);
+        return h;
+    }
+};
+// The two knobs qknr_tune chooses: warp passes per item and items per warp
+// prefetched into L2 before the wait (0: none).
+struct TunedMap {
+    int passes = 0;
+    int prefetch = 0;
+};
+
 struct DeviceState {
     std::atomic<bool> ready{false};
     int sm_count = 0;
@@ -148,6 +178,10 @@ struct DeviceState {
     bool host_ready = false;
     cudaStream_t host_in = nullptr, host_out = nullptr;
     cudaEvent_t ev_start = nullptr, ev_in = nullptr, ev_kernel = nullptr, ev_out = nullptr;
+    // work maps chosen by qknr_tune, by call shape; kept until qknr_shutdown
+    std::mutex tuned_mu;
+    std::unordered_map<ShapeKey, TunedMap, ShapeHash> tuned;
+    std::atomic<bool> has_tuned{false};
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -240,15 +274,46 @@ int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u
                             threads, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(register)", out);
 }
 
+ShapeKey shape_key(const Call &c) {
+    ShapeKey k;
+    k.num_tokens = c.num_tokens;
+    k.q_stride = c.q_stride;
+    k.k_stride = c.k_stride;
+    k.head_stride = c.head_stride;
+    k.n_qo = c.n_qo;
+    k.n_kv = c.n_kv;
+    k.head_dim = c.head_dim;
+    k.rope_dim = c.rope_dim;
+    k.is_neox = c.is_neox;
+    k.dtype = c.dtype;
+    return k;
+}
+
+// The work map qknr_tune chose for this call's shape, if any.
+bool tuned_for(DeviceState &st, const Call &c, TunedMap *out) {
+    if (!st.has_tuned.load(std::memory_order_acquire) || c.k_head_stride >= 0) return false;
+    std::lock_guard<std::mutex> lock(st.tuned_mu);
+    auto it = st.tuned.find(shape_key(c));
+    if (it == st.tuned.end()) return false;
+    *out = it->second;
+    return true;
+}
+
 // Register kernel: items are (token, chunk of warp passes); the default is the
-// largest unroll class (8 x 16-byte loads in flight per lane).
-int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
+// largest unroll class (8 x 16-byte loads in flight per lane). `force` (from
+// qknr_tune's measurements) sets the passes per item and the prefetch depth;
+// otherwise an explicit qknr_set_tuning value, then a work map that qknr_tune
+// chose for this shape, then the fixed rule decide.
+int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *force = nullptr) {
     const int d_idx = head_dim_index(c.head_dim);
     const int hpw = heads_per_pass(c.head_dim);
     const int heads = c.n_qo + c.n_kv;
     wm->kind = QKNR_KERNEL_REGISTER;
     wm->passes_per_token = (heads + hpw - 1) / hpw;
-    int ppi = tune(QKNR_TUNE_PASSES);
+    TunedMap tm;
+    const bool tuned = force ? (tm = *force, true) : tuned_for(st, c, &tm);
+    int ppi = force ? force->passes : tune(QKNR_TUNE_PASSES);
+    if (ppi <= 0 && tuned) ppi = tm.passes;
     if (ppi <= 0) {
         // a problem too small to give every SM several warps (decode-sized
         // batches) spreads its passes over as many warps as it can
@@ -275,13 +340,13 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm) {
     int occ = 0;
     int rc = resident_ctas(st, dt, pos64, d_idx, mode, wm->u_idx, threads, early, wm->kernel, &occ);
     if (rc) return rc;
-    const int force = tune(QKNR_TUNE_CTAS_PER_SM);
-    if (force > 0) occ = std::min(occ, force);
+    const int cap = tune(QKNR_TUNE_CTAS_PER_SM);
+    if (cap > 0) occ = std::min(occ, cap);
     wm->ctas_per_sm = occ;
     wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
     wm->interleave = tune(QKNR_TUNE_ORDER) == 1 ? 0 : 1;   // interleaved unless asked otherwise
-    const int pf = tune(QKNR_TUNE_PREFETCH);
-    wm->prefetch_items = pf < 0 ? 0 : (pf == 0 ? kAutoPrefetchItems : pf);
+    const int pf = force ? (force->prefetch > 0 ? force->prefetch : -1) : tune(QKNR_TUNE_PREFETCH);
+    wm->prefetch_items = pf < 0 ? 0 : (pf > 0 ? pf : (tuned ? tm.prefetch : kAutoPrefetchItems));
     return QKNR_OK;
 }
 
@@ -846,6 +911,191 @@ Call make_call(void *q, void *k, const void *q_w, const void *k_w, const float *
     return c;
 }
 
+// ---------------------------------------------------------------------------
+// Work-map tuning (qknr_tune).
+//
+// The fixed rule (4-pass items, L2 prefetch of four items) is the best single
+// choice over the measured workloads, but the best passes per item and
+// prefetch depth differ by shape by up to a few per cent. qknr_tune times the
+// candidates on scratch buffers laid out like the caller's call, never on the
+// caller's data (the op works in place), and records the fastest for that
+// shape; later calls of the same shape and layout use it.
+constexpr long long kTuneMaxScratch = 8LL << 30;   // bytes of q and k replicas at most
+constexpr int kTuneMaxReplicas = 16;
+constexpr int kTuneRounds = 3;
+
+struct Scratch {
+    std::vector<void *> ptrs;
+    ~Scratch() {
+        for (void *p : ptrs) cudaFree(p);
+    }
+    cudaError_t alloc(void **out, size_t bytes) {
+        cudaError_t e = cudaMalloc(out, bytes);
+        if (e == cudaSuccess) ptrs.push_back(*out);
+        return e;
+    }
+};
+
+int tune_impl(const Call &shape, void *stream, TunedMap *best_out, double *best_ms) {
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    if (shape.num_tokens < 1) return fail(QKNR_ERR_INVALID_ARG, "num_tokens must be >= 1 to tune");
+    // validate the layout on stand-in pointers first: aligned, and far enough
+    // apart (each extent is at most 2^56 bytes) that only a bad layout fails
+    Call probe = shape;
+    probe.q = reinterpret_cast<void *>(uintptr_t(1) << 40);
+    probe.k = reinterpret_cast<void *>(uintptr_t(1) << 58);
+    probe.q_w = probe.k_w = probe.positions = reinterpret_cast<const void *>(uintptr_t(256));
+    probe.cache = reinterpret_cast<const float *>(uintptr_t(256));
+    int rc = validate(probe);
+    if (rc) return rc;
+
+    const long long T = shape.num_tokens;
+    const long long q_bytes = ((T - 1) * shape.q_stride + static_cast<long long>(shape.n_qo - 1) * shape.head_stride +
+                               shape.head_dim) * 2;
+    const long long k_bytes = ((T - 1) * shape.k_stride + static_cast<long long>(shape.n_kv - 1) * shape.head_stride +
+                               shape.head_dim) * 2;
+    const long long rep_bytes = q_bytes + k_bytes;
+    if (rep_bytes > kTuneMaxScratch)
+        return fail(QKNR_ERR_INVALID_ARG, "qknr_tune: q and k span %lld bytes; at most %lld are tuned on scratch",
+                    rep_bytes, kTuneMaxScratch);
+    int l2 = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(L2 size)");
+    // replicas rotated between launches so that none finds its inputs in L2
+    long long n_rep = rep_bytes >= 4LL * l2 ? 1 : (4LL * l2 + rep_bytes - 1) / rep_bytes;
+    n_rep = std::min<long long>(std::min<long long>(n_rep, kTuneMaxReplicas), std::max(1LL, kTuneMaxScratch / rep_bytes));
+
+    const long long cache_len = std::min<long long>(T, 65536);
+    const bool pos64 = (shape.dtype & QKNR_POS_I64) != 0;
+    Scratch mem;
+    std::vector<Call> calls(static_cast<size_t>(n_rep), shape);
+    void *w = nullptr, *cache = nullptr, *pos = nullptr;
+    e = mem.alloc(&w, 2 * 2 * static_cast<size_t>(shape.head_dim));
+    if (e == cudaSuccess) e = mem.alloc(&cache, static_cast<size_t>(cache_len) * shape.rope_dim * sizeof(float));
+    if (e == cudaSuccess) e = mem.alloc(&pos, static_cast<size_t>(T) * (pos64 ? 8 : 4));
+    for (auto &c : calls) {
+        if (e == cudaSuccess) e = mem.alloc(&c.q, static_cast<size_t>(q_bytes));
+        if (e == cudaSuccess) e = mem.alloc(&c.k, static_cast<size_t>(k_bytes));
+    }
+    if (e != cudaSuccess) return fail_cuda(e, "qknr_tune: scratch allocation");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // zeros are a valid input (every head normalises to zero); positions walk the table
+    e = cudaMemsetAsync(w, 0, 2 * 2 * static_cast<size_t>(shape.head_dim), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(cache, 0, static_cast<size_t>(cache_len) * shape.rope_dim * sizeof(float), s);
+    for (auto &c : calls) {
+        if (e == cudaSuccess) e = cudaMemsetAsync(c.q, 0, static_cast<size_t>(q_bytes), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c.k, 0, static_cast<size_t>(k_bytes), s);
+    }
+    if (e == cudaSuccess) {
+        std::vector<long long> p64(pos64 ? static_cast<size_t>(T) : 0);
+        std::vector<int> p32(pos64 ? 0 : static_cast<size_t>(T));
+        for (long long t = 0; t < T; ++t) {
+            if (pos64) p64[static_cast<size_t>(t)] = t % cache_len;
+            else p32[static_cast<size_t>(t)] = static_cast<int>(t % cache_len);
+        }
+        e = cudaMemcpy(pos, pos64 ? static_cast<const void *>(p64.data()) : static_cast<const void *>(p32.data()),
+                       static_cast<size_t>(T) * (pos64 ? 8 : 4), cudaMemcpyHostToDevice);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "qknr_tune: scratch set-up");
+    for (auto &c : calls) {
+        c.q_w = c.k_w = w;
+        c.cache = static_cast<const float *>(cache);
+        c.positions = pos;
+        c.cache_len = 0;
+    }
+
+    // candidates: distinct (passes per item, prefetch depth) pairs
+    const int hpw = heads_per_pass(shape.head_dim);
+    const int ppt = (shape.n_qo + shape.n_kv + hpw - 1) / hpw;
+    std::vector<TunedMap> cands;
+    std::set<int> seen_chunks;
+    for (int passes : {4, 3, 2, 1}) {
+        const int chunks = (ppt + passes - 1) / passes;
+        if (!seen_chunks.insert(chunks).second) continue;
+        if (passes < 4 && cands.size() >= 6) break;
+        for (int pf : {4, 2, 1, 0}) {
+            TunedMap m;
+            m.passes = passes;
+            m.prefetch = pf;
+            cands.push_back(m);
+        }
+    }
+    std::vector<WorkMap> maps(cands.size());
+    for (size_t i = 0; i < cands.size(); ++i) {
+        rc = plan_register(*st, calls[0], &maps[i], &cands[i]);
+        if (rc) return rc;
+        const int pdl = tune(QKNR_TUNE_PDL);
+        maps[i].pdl = pdl < 0 ? 1 : pdl;
+    }
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    e = cudaEventCreate(&ev[0]);
+    if (e == cudaSuccess) e = cudaEventCreate(&ev[1]);
+    if (e != cudaSuccess) {
+        for (cudaEvent_t x : ev)
+            if (x) cudaEventDestroy(x);
+        return fail_cuda(e, "qknr_tune: events");
+    }
+    size_t next = 0;
+    auto run = [&](const WorkMap &m, int n) -> int {
+        for (int i = 0; i < n; ++i) {
+            const Call &c = calls[next++ % calls.size()];
+            const int r = launch(m, c, st->status, s);
+            if (r) return r;
+        }
+        return QKNR_OK;
+    };
+    // launches per timing: about 2 ms of work, between 5 and 200 launches
+    float ms = 0.f;
+    rc = run(maps[0], 3);
+    if (!rc) e = cudaEventRecord(ev[0], s);
+    if (!rc && e == cudaSuccess) rc = run(maps[0], 5);
+    if (!rc && e == cudaSuccess) e = cudaEventRecord(ev[1], s);
+    if (!rc && e == cudaSuccess) e = cudaEventSynchronize(ev[1]);
+    if (!rc && e == cudaSuccess) e = cudaEventElapsedTime(&ms, ev[0], ev[1]);
+    int n_iter = 5;
+    if (!rc && e == cudaSuccess) n_iter = static_cast<int>(std::min(200.0, std::max(5.0, 2.0 / std::max(1e-4, ms / 5.0))));
+    std::vector<std::vector<float>> times(cands.size());
+    for (int round = 0; round < kTuneRounds && !rc && e == cudaSuccess; ++round) {
+        for (size_t i = 0; i < cands.size() && !rc && e == cudaSuccess; ++i) {
+            rc = run(maps[i], 2);                       // settle into this work map
+            if (!rc) e = cudaEventRecord(ev[0], s);
+            if (!rc && e == cudaSuccess) rc = run(maps[i], n_iter);
+            if (!rc && e == cudaSuccess) e = cudaEventRecord(ev[1], s);
+            if (!rc && e == cudaSuccess) e = cudaEventSynchronize(ev[1]);
+            if (!rc && e == cudaSuccess) e = cudaEventElapsedTime(&ms, ev[0], ev[1]);
+            if (!rc && e == cudaSuccess) times[i].push_back(ms / n_iter);
+        }
+    }
+    cudaEventDestroy(ev[0]);
+    cudaEventDestroy(ev[1]);
+    if (rc) return rc;
+    if (e != cudaSuccess) return fail_cuda(e, "qknr_tune: timing");
+    // the candidate with the lowest median time per launch
+    size_t best = 0;
+    float best_t = 0.f;
+    for (size_t i = 0; i < cands.size(); ++i) {
+        std::vector<float> v = times[i];
+        std::sort(v.begin(), v.end());
+        const float med = v[v.size() / 2];
+        if (i == 0 || med < best_t) {
+            best = i;
+            best_t = med;
+        }
+    }
+    {
+        std::lock_guard<std::mutex> lock(st->tuned_mu);
+        st->tuned[shape_key(shape)] = cands[best];
+        st->has_tuned.store(true, std::memory_order_release);
+    }
+    *best_out = cands[best];
+    *best_ms = best_t;
+    return QKNR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -915,6 +1165,11 @@ int qknr_shutdown(void) {
             rc = fail(QKNR_ERR_CUDA, "cudaFreeHost(status) failed");
         st.status = nullptr;
         st.status_host = nullptr;
+        {
+            std::lock_guard<std::mutex> tuned_lock(st.tuned_mu);
+            st.tuned.clear();
+            st.has_tuned.store(false);
+        }
         std::lock_guard<std::mutex> host_lock(st.host_mu);
         host_pipe_release(st);
     }
@@ -991,6 +1246,35 @@ int qknr_apply_strided(void *q, void *k, const void *q_w, const void *k_w, const
     return apply_strided_impl(c, stream);
 }
 
+int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim, int is_neox, int64_t q_stride,
+              int64_t k_stride, int64_t head_stride, int dtype, void *stream, int64_t *out) {
+    const Call c = make_call(nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, num_tokens, n_qo, n_kv, head_dim,
+                             rope_dim, is_neox, q_stride, k_stride, head_stride, 1e-6f, dtype);
+    TunedMap best;
+    double ms = 0.0;
+    int rc = tune_impl(c, stream, &best, &ms);
+    if (rc || !out) return rc;
+    DeviceState *st = current_state();
+    WorkMap wm;
+    Call aligned = c;
+    aligned.cache = reinterpret_cast<const float *>(uintptr_t(256));
+    rc = plan(*st, aligned, &wm);
+    if (rc) return rc;
+    out[0] = wm.kind;
+    out[1] = wm.grid;
+    out[2] = wm.threads;
+    out[3] = wm.items;
+    out[4] = wm.chunks_per_token;
+    out[5] = wm.ctas_per_sm;
+    out[6] = wm.pdl;
+    out[7] = wm.passes_per_token;
+    out[8] = qknr::kUnrollClass[wm.u_idx];
+    out[9] = wm.interleave ? 2 : 1;
+    out[10] = wm.prefetch_items;
+    out[11] = static_cast<int64_t>(ms * 1e6);   // measured nanoseconds per launch
+    return QKNR_OK;
+}
+
 int qknr_set_tuning(int key, int value) {
     std::call_once(g_env_once, read_env_tuning);
     if (key == QKNR_TUNE_RESET) {
@@ -1022,10 +1306,12 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
         return fail(QKNR_ERR_INVALID_ARG, "bad sizes");
     if (!qknr_can_use(head_dim, rope_dim, is_neox, dtype))
         return fail(QKNR_ERR_UNSUPPORTED, "shape outside the accepted set");
-    // the plan depends on the table only through its alignment: use an aligned stand-in
+    // the plan depends on the table only through its alignment: use an aligned
+    // stand-in; q and k contiguous (the layout a tuned shape is looked up by)
     Call c = make_call(nullptr, nullptr, nullptr, nullptr, reinterpret_cast<const float *>(uintptr_t(256)), 0,
-                       nullptr, num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, 0, 0, head_dim, 1e-6f,
-                       dtype);
+                       nullptr, num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox,
+                       static_cast<long long>(n_qo) * head_dim, static_cast<long long>(n_kv) * head_dim, head_dim,
+                       1e-6f, dtype);
     WorkMap wm;
     int rc = plan(*st, c, &wm);
     if (rc) return rc;

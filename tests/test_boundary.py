@@ -158,7 +158,8 @@ rc4 = q.qknr_apply_unfused(16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 12
 rc5 = q.qknr_apply_host(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 1e-6, 0,
                         0, 0, None)
 rc6 = q.qknr_apply_strided(16, 16, 16, 16, 16, 16, 1, 1, 1, 128, 128, 0, 128, 128, 128, 128, 1e-6, 0, None)
-print(rc2, rc3, rc4, rc5, rc6)
+rc7 = q.qknr_tune(64, 4, 4, 128, 128, 0, 512, 512, 128, 0, None, None)
+print(rc2, rc3, rc4, rc5, rc6, rc7)
 """
 
 
@@ -170,7 +171,7 @@ def test_calls_before_init_are_refused():
     assert r.returncode == 0, r.stderr
     first, second = r.stdout.strip().splitlines()[-2:]
     assert first.startswith("1 ") and "qknr_init" in first
-    assert second.split() == ["1", "1", "1", "1", "1"]
+    assert second.split() == ["1", "1", "1", "1", "1", "1"]
 
 
 def test_four_d_inputs_view_or_refuse():
