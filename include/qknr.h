@@ -313,9 +313,9 @@ int qknr_get_tuning(int key, int *value);
  * allocates and frees its scratch (q and k at most 8 GiB, plus weights, a
  * cos|sin table of min(num_tokens, 65536) rows and positions), so it belongs
  * at set-up time, not on a hot path or inside a stream capture, and it waits
- * for `stream`. out (NULL allowed): QKNR_WORK_MAP_FIELDS values, the chosen
- * work map as qknr_query_work_map reports it, with out[11] the measured time
- * per launch in nanoseconds. A choice is kept until qknr_shutdown; tuning the
+ * for `stream`. out (NULL allowed): QKNR_TUNE_FIELDS values, the chosen work
+ * map as qknr_query_work_map reports it (out[0..11]), then out[12] the
+ * measured time per launch in nanoseconds. A choice is kept until qknr_shutdown; tuning the
  * same shape again replaces it. Errors: QKNR_ERR_NOT_INITIALIZED,
  * QKNR_ERR_INVALID_ARG / UNSUPPORTED / MISALIGNED as qknr_apply would return
  * for the layout, QKNR_ERR_CUDA (scratch allocation or launch).
@@ -325,6 +325,7 @@ int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim
               int64_t *out);
 
 #define QKNR_WORK_MAP_FIELDS 12
+#define QKNR_TUNE_FIELDS 13
 /*
  * The launch qknr_apply would make for these sizes with contiguous q and k
  * (no launch, no pointers; assumes a 16-byte aligned cos|sin table), including
@@ -333,7 +334,10 @@ int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim
  *  3 warp items  4 items per token  5 resident CTAs per SM  6 PDL on
  *  7 warp passes per token  8 unroll class (passes of loads in flight)
  *  9 item order (1 contiguous, 2 interleaved)  10 items per warp prefetched
- *    into L2 before the wait for the previous kernel  11 reserved (0)
+ *    into L2 before the wait for the previous kernel  11 rope_dim compiled
+ *    into the instantiation (0: read at run time; interleaved pairing with
+ *    4-pass items has instantiations for rope_dim = head_dim and head_dim / 2
+ *    at head_dim 64, 128 and 256)
  */
 int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
                         int is_neox, int dtype, int64_t *out);

@@ -45,7 +45,7 @@ HOST_MODES = {"auto": QKNR_HOST_AUTO, "staged": QKNR_HOST_STAGED, "direct": QKNR
 TUNE_KEYS = {"reset": 0, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5, "order": 9,
              "prefetch": 10}
 WORK_MAP_FIELDS = ["kernel", "grid", "threads", "items", "items_per_token", "ctas_per_sm", "pdl",
-                   "passes_per_token", "unroll", "order", "prefetch_items", "reserved11"]
+                   "passes_per_token", "unroll", "order", "prefetch_items", "rope_dim_compiled"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -470,13 +470,12 @@ def tune(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, head_dim: i
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif not isinstance(stream, int):
         stream = stream.cuda_stream
-    out = (ctypes.c_int64 * len(WORK_MAP_FIELDS))()
+    out = (ctypes.c_int64 * (len(WORK_MAP_FIELDS) + 1))()
     with torch.cuda.device(q.device):
         _check(qknr_tune(T, n_qo, n_kv, D, R, int(bool(is_neox)), qs, ks, hs, code, stream, out))
-    d = dict(zip(WORK_MAP_FIELDS, [int(v) for v in out]))
+    d = dict(zip(WORK_MAP_FIELDS + ["ns_per_launch"], [int(v) for v in out]))
     d["kernel"] = {QKNR_KERNEL_REGISTER: "register"}.get(d["kernel"], d["kernel"])
     d["order"] = {1: "contiguous", 2: "interleaved"}.get(d["order"], d["order"])
-    d["ns_per_launch"] = d.pop("reserved11")
     return d
 
 
@@ -489,5 +488,4 @@ def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int
     d = dict(zip(WORK_MAP_FIELDS, [int(v) for v in out]))
     d["kernel"] = {QKNR_KERNEL_REGISTER: "register"}.get(d["kernel"], d["kernel"])
     d["order"] = {1: "contiguous", 2: "interleaved"}.get(d["order"], d["order"])
-    d.pop("reserved11")
     return d

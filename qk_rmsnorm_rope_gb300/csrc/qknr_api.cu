@@ -167,8 +167,9 @@ struct DeviceState {
     unsigned long long *status = nullptr;       // device: kStatusWords words
     unsigned long long *status_host = nullptr;  // pinned host copy (qknr_init) or nullptr
     std::mutex checked_mu;                      // serialises status read-backs on this device
-    // resident CTAs per SM for the register kernel, by (dtype, pos64, d_idx, mode, u_idx, threads class)
-    std::atomic<int> occupancy[2][2][2][qknr::kNumHeadDim][2][qknr::kNumUnroll][4];  // [early][dt]...
+    // resident CTAs per SM for the register kernel, by (early, dtype, pos64, d_idx, mode, u_idx,
+    // rope_dim class, threads class)
+    std::atomic<int> occupancy[2][2][2][qknr::kNumHeadDim][2][qknr::kNumUnroll][qknr::kNumRope][4];
     // resident CTAs per SM of the unfused-baseline kernels, by (dtype, op-1, pos64, d_idx, mode)
     std::atomic<int> unfused_occ[2][2][2][qknr::kNumHeadDim][2];
     // host-buffer pipeline (qknr_apply_host): a host-to-device and a
@@ -242,6 +243,7 @@ struct WorkMap {
     long long items = 0;  // warp items: (token, chunk of warp passes)
     int chunks_per_token = 0;
     int passes_per_token = 0, max_passes = 0, u_idx = 0;
+    int r_idx = 0;        // rope_dim class of the instantiation (qknr::kRope*)
     int interleave = 0;   // item order
     int prefetch_items = 0;  // items per warp prefetched into L2 before the wait
     const void *kernel = nullptr;
@@ -268,10 +270,17 @@ int persistent_grid(long long items, int threads, int ctas_per_sm, int sm_count)
     return static_cast<int>(std::max(1LL, std::min(needed, static_cast<long long>(ctas_per_sm) * sm_count)));
 }
 
-int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u_idx, int threads, int early,
-                  const void *kernel, int *out) {
-    return cached_occupancy(st.occupancy[early][dt][pos64][d_idx][mode][u_idx][threads_index(threads)], kernel,
-                            threads, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(register)", out);
+int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u_idx, int r_idx, int threads,
+                  int early, const void *kernel, int *out) {
+    return cached_occupancy(st.occupancy[early][dt][pos64][d_idx][mode][u_idx][r_idx][threads_index(threads)],
+                            kernel, threads, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(register)", out);
+}
+
+const void *register_kernel(int dt, int early, int pos64, int d_idx, int mode, int u_idx, int r_idx) {
+    return early ? (dt ? qknr::kernel_fp16_early(pos64, d_idx, mode, u_idx, r_idx)
+                       : qknr::kernel_bf16_early(pos64, d_idx, mode, u_idx, r_idx))
+                 : (dt ? qknr::kernel_fp16(pos64, d_idx, mode, u_idx, r_idx)
+                       : qknr::kernel_bf16(pos64, d_idx, mode, u_idx, r_idx));
 }
 
 ShapeKey shape_key(const Call &c) {
@@ -332,13 +341,21 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *f
     const int pos64 = (c.dtype & QKNR_POS_I64) ? 1 : 0;
     const int mode = c.is_neox ? qknr::kNeox : qknr::kInterleaved;
     const int early = (c.dtype & QKNR_INPUTS_READY) ? 1 : 0;
-    wm->kernel = early ? (dt ? qknr::kernel_fp16_early(pos64, d_idx, mode, wm->u_idx)
-                             : qknr::kernel_bf16_early(pos64, d_idx, mode, wm->u_idx))
-                       : (dt ? qknr::kernel_fp16(pos64, d_idx, mode, wm->u_idx)
-                             : qknr::kernel_bf16(pos64, d_idx, mode, wm->u_idx));
+    // rope_dim fixed at compile time where it measured faster (interleaved
+    // pairing, 4-pass items, rope_dim = head_dim or head_dim / 2); the table has
+    // no such instantiation elsewhere, and then the run-time rope_dim kernel runs
+    wm->r_idx = qknr::kRopeRuntime;
+    if (mode == qknr::kInterleaved && wm->u_idx == 1)
+        wm->r_idx = c.rope_dim == c.head_dim ? qknr::kRopeFull
+                    : (2 * c.rope_dim == c.head_dim ? qknr::kRopeHalf : qknr::kRopeRuntime);
+    wm->kernel = register_kernel(dt, early, pos64, d_idx, mode, wm->u_idx, wm->r_idx);
+    if (!wm->kernel && wm->r_idx != qknr::kRopeRuntime) {
+        wm->r_idx = qknr::kRopeRuntime;
+        wm->kernel = register_kernel(dt, early, pos64, d_idx, mode, wm->u_idx, wm->r_idx);
+    }
     if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no kernel for this shape");
     int occ = 0;
-    int rc = resident_ctas(st, dt, pos64, d_idx, mode, wm->u_idx, threads, early, wm->kernel, &occ);
+    int rc = resident_ctas(st, dt, pos64, d_idx, mode, wm->u_idx, wm->r_idx, threads, early, wm->kernel, &occ);
     if (rc) return rc;
     const int cap = tune(QKNR_TUNE_CTAS_PER_SM);
     if (cap > 0) occ = std::min(occ, cap);
@@ -488,11 +505,12 @@ void log_launch(const WorkMap &wm, const Call &c) {
     if (!seen.insert(key).second) return;
     std::fprintf(stderr,
                  "qknr: T=%lld n_qo=%d n_kv=%d head_dim=%d rope_dim=%d %s %s pos%s -> %s kernel, grid %d x %d, "
-                 "%d CTAs/SM, %lld items (%d per token), %d passes per token, PDL %s\n",
+                 "%d CTAs/SM, %lld items (%d per token), %d passes per token, rope_dim %s, PDL %s\n",
                  c.num_tokens, c.n_qo, c.n_kv, c.head_dim, c.rope_dim, c.is_neox ? "neox" : "interleaved",
                  (c.dtype & 0xff) == QKNR_FP16 ? "fp16" : "bf16", (c.dtype & QKNR_POS_I64) ? "64" : "32",
                  "register", wm.grid, wm.threads, wm.ctas_per_sm,
-                 wm.items, wm.chunks_per_token, wm.passes_per_token, wm.pdl ? "on" : "off");
+                 wm.items, wm.chunks_per_token, wm.passes_per_token,
+                 wm.r_idx == qknr::kRopeRuntime ? "at run time" : "compiled in", wm.pdl ? "on" : "off");
 }
 
 int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStream_t stream) {
@@ -1138,7 +1156,8 @@ int qknr_init(int device) {
                     for (auto &c : b)
                         for (auto &d : c)
                             for (auto &u : d)
-                                for (auto &x : u) x.store(0);
+                                for (auto &r : u)
+                                    for (auto &x : r) x.store(0);
         st.ready.store(true, std::memory_order_release);
     } else {
         if (st.status) cudaFree(st.status);
@@ -1271,7 +1290,8 @@ int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim
     out[8] = qknr::kUnrollClass[wm.u_idx];
     out[9] = wm.interleave ? 2 : 1;
     out[10] = wm.prefetch_items;
-    out[11] = static_cast<int64_t>(ms * 1e6);   // measured nanoseconds per launch
+    out[11] = wm.r_idx == qknr::kRopeFull ? c.head_dim : (wm.r_idx == qknr::kRopeHalf ? c.head_dim / 2 : 0);
+    out[12] = static_cast<int64_t>(ms * 1e6);   // measured nanoseconds per launch
     return QKNR_OK;
 }
 
@@ -1326,7 +1346,7 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     out[8] = qknr::kUnrollClass[wm.u_idx];
     out[9] = wm.interleave ? 2 : 1;
     out[10] = wm.prefetch_items;
-    out[11] = 0;
+    out[11] = wm.r_idx == qknr::kRopeFull ? head_dim : (wm.r_idx == qknr::kRopeHalf ? head_dim / 2 : 0);
     return QKNR_OK;
 }
 

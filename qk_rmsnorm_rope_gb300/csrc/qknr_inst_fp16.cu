@@ -34,8 +34,8 @@ const void *unfused_kernel_fp16(int op, int pos64, int d_idx, int mode) {
     }
 }
 
-const void *kernel_fp16(int pos64, int d_idx, int mode, int u_idx) {
-    return RegisterTable<__half, false>::get(pos64, d_idx, mode, u_idx);
+const void *kernel_fp16(int pos64, int d_idx, int mode, int u_idx, int r_idx) {
+    return RegisterTable<__half, false>::get(pos64, d_idx, mode, u_idx, r_idx);
 }
 
 }  // namespace qknr

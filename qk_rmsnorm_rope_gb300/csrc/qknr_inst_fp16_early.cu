@@ -6,8 +6,8 @@
 
 namespace qknr {
 
-const void *kernel_fp16_early(int pos64, int d_idx, int mode, int u_idx) {
-    return RegisterTable<__half, true>::get(pos64, d_idx, mode, u_idx);
+const void *kernel_fp16_early(int pos64, int d_idx, int mode, int u_idx, int r_idx) {
+    return RegisterTable<__half, true>::get(pos64, d_idx, mode, u_idx, r_idx);
 }
 
 }  // namespace qknr

@@ -244,7 +244,7 @@ def test_work_map_choice(qknr):
     assert m["kernel"] == "register" and m["order"] == "interleaved"
     assert m["unroll"] == 4 and m["passes_per_token"] == 12 and m["items_per_token"] == 3
     assert m["items"] == 4608 * 3 and m["threads"] == 256 and m["pdl"] == 1
-    assert m["prefetch_items"] == 4
+    assert m["prefetch_items"] == 4 and m["rope_dim_compiled"] == 128
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert m["grid"] <= m["ctas_per_sm"] * sms
     small = qknr.work_map(4, 4, 2, 128, 6, False, bf)
@@ -917,3 +917,43 @@ def test_split_rope_pair_mapping(qknr):
     torch.cuda.synchronize()
     _assert_close(dq.view(B * S, H, D).double().cpu().numpy(), eq, torch.bfloat16, "q")
     _assert_close(dk.view(B * S, H, D).double().cpu().numpy(), ek, torch.bfloat16, "k")
+
+
+COMPILED_R = [(D, R, dt, pos) for D in (64, 128, 256) for R in (D, D // 2)
+              for dt, pos in (("bf16", "i32"), ("fp16", "i64"))]
+
+
+@pytest.mark.parametrize("D,R,dtype,pos", COMPILED_R, ids=[f"D{c[0]}-R{c[1]}-{c[2]}-{c[3]}" for c in COMPILED_R])
+def test_compiled_rope_dim_kernels(qknr, D, R, dtype, pos):
+    """Interleaved pairing with 4-pass items runs an instantiation with
+    rope_dim compiled in when rope_dim is head_dim or head_dim / 2; 2-pass
+    items run the one that reads rope_dim at run time. Same bits, and the
+    oracle's bound; other rope_dims keep the run-time kernel."""
+    # 32 heads: at least 4 warp passes per token for every head_dim here, so
+    # that 4-pass items take the 4-pass class
+    w = _make(D, R, False, pos, 131, 20, 12, dtype=dtype, seed=D + R)
+    code = qknr.dtype_code(w.torch_dtype, w.pos_torch_dtype)
+    cpu = workloads.make_inputs(w)
+    eq, ek = _expected(cpu, w)
+    outs = {}
+    for passes in (4, 2):
+        qknr.set_tuning(reset=True, passes=passes)
+        try:
+            m = qknr.work_map(w.num_tokens, w.n_qo, w.n_kv, D, R, False, code)
+            assert m["rope_dim_compiled"] == (R if passes == 4 else 0), m
+            dev = workloads.to_device(cpu, w, "cuda")
+            _run_gpu(qknr, dev, w)
+        finally:
+            qknr.set_tuning(reset=True)
+        _assert_close(dev["q"].double().cpu().numpy(), eq, w.torch_dtype, f"q passes={passes}")
+        _assert_close(dev["k"].double().cpu().numpy(), ek, w.torch_dtype, f"k passes={passes}")
+        outs[passes] = dev
+    assert torch.equal(outs[4]["q"].view(torch.int16), outs[2]["q"].view(torch.int16))
+    assert torch.equal(outs[4]["k"].view(torch.int16), outs[2]["k"].view(torch.int16))
+    qknr.set_tuning(reset=True, passes=4)
+    try:
+        other = qknr.work_map(w.num_tokens, w.n_qo, w.n_kv, D, R - 2, False, code)
+        neox = qknr.work_map(w.num_tokens, w.n_qo, w.n_kv, D, D, True, code)
+    finally:
+        qknr.set_tuning(reset=True)
+    assert other["rope_dim_compiled"] == 0 and neox["rope_dim_compiled"] == 0
