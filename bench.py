@@ -45,8 +45,9 @@ default), and prints the same config dict as this arm.
 Other options: --tokens N (decode-sized calls), --graph (replays of a CUDA
 graph of calls), --inputs-ready (calls that set QKNR_INPUTS_READY), --variant
 unfused (the two-kernel chain), --tune (qknr_tune picks each configuration's
-launch first), --ceiling (torch's own in-place elementwise kernel at the same
-bytes).
+launch first), --kernel register|ring (force one of the two kernels instead
+of the library's rule), --ceiling (torch's own in-place elementwise kernel at
+the same bytes).
 """
 from __future__ import annotations
 
@@ -72,7 +73,7 @@ import workloads  # noqa: E402
 METRIC = "fused QK-RMSNorm+RoPE effective HBM GB/s (% of GB300 peak) and heads/sec"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_NAMES = {"register": "qknr_fused_kernel"}
+KERNEL_NAMES = {"register": "qknr_fused_kernel", "ring": "qknr_ring_kernel"}
 # every configuration of the benchmark, small to large; the headline is the
 # largest one that fits one GPU
 CONFIGS = ["tiny", "dit", "mha_neox", "gqa", "fused_qkv"]
@@ -122,6 +123,7 @@ def measured_peaks() -> Dict:
 # while these are unchanged)
 KERNEL_SOURCES = {
     "qknr_fused_kernel": ["qknr_math.cuh", "qknr_kernel.cuh"],
+    "qknr_ring_kernel": ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_ring_kernel.cuh"],
 }
 
 
@@ -494,6 +496,8 @@ def run_ours(args, names: List[str], rank: int, world: int, local: int) -> Optio
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     q.init(local)
+    if args.kernel != "auto":
+        q.set_tuning(kernel=args.kernel)
     stream = torch.cuda.current_stream(device)
     head = HEADLINE if HEADLINE in names else names[-1]
     results = {}
@@ -846,6 +850,8 @@ def main(argv: Optional[List[str]] = None) -> int:
                     help="time replays of a CUDA graph of calls (GPU time per call, no host launch rate)")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
                     help="unfused: time the two-kernel RMSNorm-then-RoPE chain instead")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "register", "ring"],
+                    help="force one of the two kernels (default: the library's measured rule)")
     ap.add_argument("--tune", action="store_true",
                     help="call qknr_tune for each configuration's shape first (the launch it picks "
                          "on scratch buffers is then used)")

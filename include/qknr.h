@@ -50,8 +50,8 @@ extern "C" {
  * and positions were not written by the kernel enqueued just before this call
  * on the stream (for example: weights loaded at start-up, positions computed
  * at the start of the forward pass, and a GEMM producing q and k just before).
- * With it, the register kernel reads the weights and positions while that
- * kernel finishes (programmatic dependent launch), and reads q, k and the
+ * With it, the kernels read the weights and positions while that
+ * kernel finishes (programmatic dependent launch), and read q, k and the
  * cos|sin table only after it has completed: about 17% less latency per
  * decode-sized call and 3% more bandwidth on a 4608-token DiT call, with the
  * same results. Breaking the promise is a data race. The unfused baseline and
@@ -67,11 +67,12 @@ extern "C" {
 #define QKNR_ERR_MISALIGNED 4      /* pointer or stride breaks the 16-byte vector rule */
 #define QKNR_ERR_CUDA 5            /* a CUDA runtime call failed; message has the CUDA error */
 #define QKNR_ERR_POSITION_OOB 6    /* qknr_apply_checked: a position outside [0, cache_len) */
+#define QKNR_ERR_WATCHDOG 7        /* a bounded wait inside a kernel ran out; that call's output is incomplete */
 
 /*
  * Prepare the library for CUDA device `device`: reads the SM count and other
- * limits, and allocates a 16-byte status block (the position-check counters
- * of qknr_apply_checked).
+ * limits, and allocates a 24-byte status block (the position-check counters
+ * of qknr_apply_checked and the ring kernel's watchdog word, see qknr_sync).
  * Idempotent; safe to call from several threads. Restores the caller's
  * current device before returning. Returns QKNR_OK or QKNR_ERR_CUDA /
  * QKNR_ERR_INVALID_ARG (no such device).
@@ -131,6 +132,15 @@ int qknr_can_use(int head_dim, int rope_dim, int is_neox, int dtype);
  * are fine). Neither q nor k may span more than 2^56 bytes, and no size or
  * stride may exceed 2^56 (QKNR_ERR_INVALID_ARG), so that no byte offset can
  * wrap. The caller owns every buffer; nothing is retained after return.
+ *
+ * Kernels: the library has two kernels with identical results, chosen per
+ * call by a measured rule (or by qknr_tune / qknr_set_tuning): the register
+ * kernel, which loads each warp item straight into registers, and the ring
+ * kernel, which double-buffers each warp's items in shared memory with bulk
+ * copies (TMA) and takes NeoX calls and interleaved calls of up to 256 MiB of
+ * q and k. The ring kernel's waits are bounded; one that runs out (never in
+ * normal operation) sets a watchdog word that qknr_sync and the checked entry
+ * points report as QKNR_ERR_WATCHDOG.
  */
 int qknr_apply(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
                const void *positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim,
@@ -142,8 +152,10 @@ int qknr_apply(void *q, void *k, const void *q_w, const void *k_w, const float *
  * whose position is outside are left untouched; all others are computed as by
  * qknr_apply. SYNCHRONOUS: waits for `stream` before returning. Returns
  * QKNR_ERR_POSITION_OOB (message: count and first bad token) if any position
- * was out of range. Uses the status word that qknr_init allocated, so calls
- * on one device must not overlap on the GPU (they serialise on the host).
+ * was out of range, and QKNR_ERR_WATCHDOG (clearing the word) if a kernel
+ * wait on this device ran out since the word was last read. Uses the status
+ * words that qknr_init allocated, so calls on one device must not overlap on
+ * the GPU (they serialise on the host).
  */
 int qknr_apply_checked(void *q, void *k, const void *q_w, const void *k_w,
                        const float *cos_sin_cache, int64_t cache_len, const void *positions,
@@ -177,9 +189,9 @@ int qknr_apply_unfused(void *q, void *k, const void *q_w, const void *k_w,
  *
  * Same arguments, results and QKNR_ERR_POSITION_OOB report as
  * qknr_apply_checked, but qknr_init is not needed and nothing is allocated:
- * the 16-byte status block lives in a 256-byte file-scope __device__ array
+ * the 24-byte status block lives in a 256-byte file-scope __device__ array
  * of the library, which every GPU that loads the library holds until the
- * process exits. A call needs those 16 bytes whatever its num_tokens, so no
+ * process exits. A call needs those 24 bytes whatever its num_tokens, so no
  * problem size exceeds the array. The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture. That set-up is kept for
@@ -204,8 +216,8 @@ int qknr_apply_checked_noalloc(void *q, void *k, const void *q_w, const void *k_
  * deep-dive's contract (§3, §4.7) has one shared head stride; this entry
  * point lifts that restriction. Same results, bit for bit, as qknr_apply on
  * the same values. With equal strides, or one head on a side, it is
- * qknr_apply's single launch; otherwise two launches of the register kernel
- * on `stream`, q's heads then k's. Arguments, ownership and errors as
+ * qknr_apply's single launch; otherwise two launches on `stream`, q's heads
+ * then k's, each with the kernel the rule picks for that side. Arguments, ownership and errors as
  * qknr_apply (each side's stride is checked on its own; a negative stride is
  * QKNR_ERR_INVALID_ARG). Asynchronous on `stream`.
  */
@@ -264,11 +276,36 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
                     int64_t head_stride, float eps, int dtype, int64_t chunk_tokens, int flags,
                     void *stream);
 
-/* kernel (qknr_query_work_map out[0]) */
-#define QKNR_KERNEL_REGISTER 1 /* the register kernel: loads straight into registers; every accepted shape */
+/*
+ * Reports whether a bounded wait inside a kernel ran out on the current
+ * device since the last report (the ring kernel bounds each wait at one
+ * second of GPU time; it never runs out in normal operation, and a warp whose
+ * wait ran out stops, leaving the rest of its items unprocessed). qknr_apply
+ * is asynchronous, so this is how its caller learns of it; the checked entry
+ * points report it themselves. Waits for `stream`, then returns QKNR_OK or
+ * QKNR_ERR_WATCHDOG and clears the word. Not part of the op on the pages.
+ */
+int qknr_sync(void *stream);
 
-/* tuning keys for qknr_set_tuning / qknr_get_tuning (1, 6, 7 and 8 are not used) */
+/*
+ * Exercises the watchdog path for tests of a caller's error handling: on
+ * `stream`, one warp waits, with the ring kernel's bounded wait, on an
+ * mbarrier that nothing arrives on. After about a second the wait gives up
+ * and sets the watchdog word, as a stalled ring-kernel wait would; the next
+ * qknr_sync (or checked call) on the device reports QKNR_ERR_WATCHDOG. No
+ * fault and no unbounded wait: the context stays usable. Not part of the op.
+ */
+int qknr_selftest_watchdog(void *stream);
+
+/* kernels (QKNR_TUNE_KERNEL values and qknr_query_work_map out[0]) */
+#define QKNR_KERNEL_AUTO 0     /* the measured rule (QKNR_TUNE_KERNEL only) */
+#define QKNR_KERNEL_REGISTER 1 /* loads each warp item straight into registers */
+#define QKNR_KERNEL_RING 2     /* double-buffers each warp's items in shared memory (bulk copies) */
+
+/* tuning keys for qknr_set_tuning / qknr_get_tuning (6, 7 and 8 are not used) */
 #define QKNR_TUNE_RESET 0       /* qknr_set_tuning(QKNR_TUNE_RESET, 0): every key back to automatic */
+#define QKNR_TUNE_KERNEL 1      /* 0 auto (the rule: ring for NeoX and for interleaved calls with at most
+                                   256 MiB of q and k, items of 3-4 passes; else register), 1, 2 */
 #define QKNR_TUNE_PASSES 2      /* warp passes per item, 1..4 (0 auto: 4, or 1 when the whole call has
                                    at most 16 warp passes per SM) */
 #define QKNR_TUNE_THREADS 3     /* threads per CTA, 64/128/256/512 (0 auto = 256) */
@@ -284,8 +321,8 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
  * Process-wide launch tuning, for benchmarks and tests; results do not depend
  * on it (every setting gives the same bits). Invalid values return
  * QKNR_ERR_INVALID_ARG and change nothing. The environment variable
- * QKNR_TUNE="passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1" sets the
- * same keys at first use.
+ * QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1"
+ * sets the same keys at first use.
  */
 int qknr_set_tuning(int key, int value);
 int qknr_get_tuning(int key, int *value);
@@ -297,13 +334,13 @@ int qknr_get_tuning(int key, int *value);
  * Measure the launch choices for one call shape and keep the fastest: for
  * later calls with exactly these sizes, strides and dtype (QKNR_INPUTS_READY
  * included) on the current device, qknr_apply, qknr_apply_checked and the
- * host and strided entry points use the chosen passes per item and L2
- * prefetch depth instead of the fixed rule. Explicit qknr_set_tuning values
+ * host and strided entry points use the chosen kernel, passes per item and
+ * L2 prefetch depth instead of the fixed rule. Explicit qknr_set_tuning values
  * still take precedence. The op has no counterpart of this on the pages,
  * whose kernels fix their launch at compile time.
  *
- * The candidates (passes per item 4, 3, 2 or 1 where they chunk a token
- * differently; prefetch of 4, 2, 1 or no items) run on scratch buffers with
+ * The candidates (both kernels; passes per item 4, 3, 2 or 1 where they chunk
+ * a token differently; prefetch of 4, 2, 1 or no items) run on scratch buffers with
  * the given layout, zero-filled, never on the caller's data, each timed with
  * CUDA events over about 2 ms of launches in three alternating rounds; the
  * one with the lowest median time per launch is kept. Input replicas rotate so
@@ -330,9 +367,10 @@ int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim
  * The launch qknr_apply would make for these sizes with contiguous q and k
  * (no launch, no pointers; assumes a 16-byte aligned cos|sin table), including
  * a choice qknr_tune made for that shape. out[QKNR_WORK_MAP_FIELDS]:
- *  0 kernel (QKNR_KERNEL_REGISTER)  1 grid CTAs  2 threads per CTA
- *  3 warp items  4 items per token  5 resident CTAs per SM  6 PDL on
- *  7 warp passes per token  8 unroll class (passes of loads in flight)
+ *  0 kernel (QKNR_KERNEL_REGISTER or QKNR_KERNEL_RING)  1 grid CTAs
+ *  2 threads per CTA  3 warp items  4 items per token  5 resident CTAs per
+ *  SM  6 PDL on  7 warp passes per token  8 unroll class (most passes per
+ *  item the instantiation holds: 2 or 4; the ring kernel's stage holds 4)
  *  9 item order (1 contiguous, 2 interleaved)  10 items per warp prefetched
  *    into L2 before the wait for the previous kernel  11 rope_dim compiled
  *    into the instantiation (0: read at run time; interleaved pairing with

@@ -21,10 +21,10 @@ __all__ = [
     "QKNR_HOST_DIRECT", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
     "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-    "qknr_apply_host", "qknr_apply_strided", "qknr_tune",
+    "qknr_apply_host", "qknr_apply_strided", "qknr_tune", "qknr_sync", "qknr_selftest_watchdog",
     "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map", "TUNE_KEYS",
     "init", "apply", "apply_checked", "apply_unfused", "apply_host", "can_use", "dtype_code",
-    "work_map", "set_tuning", "get_tuning", "tune",
+    "work_map", "set_tuning", "get_tuning", "tune", "sync",
 ]
 
 QKNR_BF16 = 0x000
@@ -35,15 +35,16 @@ QKNR_INPUTS_READY = 0x200   # caller's promise: weights and positions are not wr
 STATUS_NAMES = {
     0: "QKNR_OK", 1: "QKNR_ERR_NOT_INITIALIZED", 2: "QKNR_ERR_INVALID_ARG",
     3: "QKNR_ERR_UNSUPPORTED", 4: "QKNR_ERR_MISALIGNED", 5: "QKNR_ERR_CUDA",
-    6: "QKNR_ERR_POSITION_OOB",
+    6: "QKNR_ERR_POSITION_OOB", 7: "QKNR_ERR_WATCHDOG",
 }
 
-QKNR_KERNEL_REGISTER = 1
+QKNR_KERNEL_AUTO, QKNR_KERNEL_REGISTER, QKNR_KERNEL_RING = 0, 1, 2
+KERNEL_NAMES = {QKNR_KERNEL_REGISTER: "register", QKNR_KERNEL_RING: "ring"}
 QKNR_HOST_AUTO, QKNR_HOST_STAGED, QKNR_HOST_DIRECT = 0, 1, 2
 HOST_MODES = {"auto": QKNR_HOST_AUTO, "staged": QKNR_HOST_STAGED, "direct": QKNR_HOST_DIRECT}
 # QKNR_TUNE_* keys (include/qknr.h)
-TUNE_KEYS = {"reset": 0, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5, "order": 9,
-             "prefetch": 10}
+TUNE_KEYS = {"reset": 0, "kernel": 1, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5,
+             "order": 9, "prefetch": 10}
 WORK_MAP_FIELDS = ["kernel", "grid", "threads", "items", "items_per_token", "ctas_per_sm", "pdl",
                    "passes_per_token", "unroll", "order", "prefetch_items", "rope_dim_compiled"]
 
@@ -87,13 +88,16 @@ def _load() -> ctypes.CDLL:
                                        i64, i64, i64, i64, f32, i32, vp]
     lib.qknr_tune.argtypes = [i64, i32, i32, i32, i32, i32, i64, i64, i64, i32, vp,
                               ctypes.POINTER(ctypes.c_int64)]
+    lib.qknr_sync.argtypes = [vp]
+    lib.qknr_selftest_watchdog.argtypes = [vp]
     lib.qknr_set_tuning.argtypes = [i32, i32]
     lib.qknr_get_tuning.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
     lib.qknr_query_work_map.argtypes = [i64, i32, i32, i32, i32, i32, i32,
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
                  "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-                 "qknr_apply_host", "qknr_apply_strided", "qknr_tune", "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
+                 "qknr_apply_host", "qknr_apply_strided", "qknr_tune", "qknr_sync", "qknr_selftest_watchdog",
+                 "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -196,6 +200,14 @@ def qknr_tune(num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, q_stride, k_s
               dtype, stream, out) -> int:
     return _get_lib().qknr_tune(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox), q_stride,
                                 k_stride, head_stride, dtype, stream, out)
+
+
+def qknr_sync(stream) -> int:
+    return _get_lib().qknr_sync(stream)
+
+
+def qknr_selftest_watchdog(stream) -> int:
+    return _get_lib().qknr_selftest_watchdog(stream)
 
 
 def qknr_set_tuning(key: int, value: int) -> int:
@@ -437,11 +449,28 @@ def apply_host(h_q, h_k, q_w, k_w, cos_sin_cache, h_positions, d_q=None, d_k=Non
 
 def set_tuning(**kw) -> None:
     """Set launch tuning keys by name (see TUNE_KEYS); ``reset=True`` first
-    returns every key to automatic."""
+    returns every key to automatic. ``kernel`` also takes "auto", "register"
+    or "ring"."""
     if kw.pop("reset", False):
         _check(qknr_set_tuning(0, 0))
     for name, value in kw.items():
+        if name == "kernel" and isinstance(value, str):
+            value = {"auto": QKNR_KERNEL_AUTO, "register": QKNR_KERNEL_REGISTER, "ring": QKNR_KERNEL_RING}[value]
         _check(qknr_set_tuning(TUNE_KEYS[name], int(value)))
+
+
+def sync(stream=None, device=None) -> None:
+    """qknr_sync: wait for ``stream`` (default: torch's current stream) and
+    raise QknrError(QKNR_ERR_WATCHDOG) if a kernel wait ran out since the
+    last report."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    with torch.cuda.device(dev):
+        _check(qknr_sync(stream))
 
 
 def get_tuning(name: str) -> int:
@@ -474,7 +503,7 @@ def tune(q, k, q_w, k_w, cos_sin_cache, positions, *, is_neox: bool, head_dim: i
     with torch.cuda.device(q.device):
         _check(qknr_tune(T, n_qo, n_kv, D, R, int(bool(is_neox)), qs, ks, hs, code, stream, out))
     d = dict(zip(WORK_MAP_FIELDS + ["ns_per_launch"], [int(v) for v in out]))
-    d["kernel"] = {QKNR_KERNEL_REGISTER: "register"}.get(d["kernel"], d["kernel"])
+    d["kernel"] = KERNEL_NAMES.get(d["kernel"], d["kernel"])
     d["order"] = {1: "contiguous", 2: "interleaved"}.get(d["order"], d["order"])
     return d
 
@@ -486,6 +515,6 @@ def work_map(num_tokens: int, n_qo: int, n_kv: int, head_dim: int, rope_dim: int
     _check(qknr_query_work_map(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox), dtype,
                                out))
     d = dict(zip(WORK_MAP_FIELDS, [int(v) for v in out]))
-    d["kernel"] = {QKNR_KERNEL_REGISTER: "register"}.get(d["kernel"], d["kernel"])
+    d["kernel"] = KERNEL_NAMES.get(d["kernel"], d["kernel"])
     d["order"] = {1: "contiguous", 2: "interleaved"}.get(d["order"], d["order"])
     return d

@@ -21,8 +21,10 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libqknr.so")
 SOURCES = ["qknr_api.cu", "qknr_inst_bf16.cu", "qknr_inst_fp16.cu", "qknr_inst_bf16_early.cu",
-           "qknr_inst_fp16_early.cu"]
-HEADERS = ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_register_table.cuh", "qknr_dispatch.h"]
+           "qknr_inst_fp16_early.cu", "qknr_inst_ring_bf16.cu", "qknr_inst_ring_fp16.cu",
+           "qknr_inst_ring_bf16_early.cu", "qknr_inst_ring_fp16_early.cu"]
+HEADERS = ["qknr_math.cuh", "qknr_kernel.cuh", "qknr_register_table.cuh", "qknr_ring_kernel.cuh",
+           "qknr_ring_table.cuh", "qknr_dispatch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

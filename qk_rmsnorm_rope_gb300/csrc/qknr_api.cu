@@ -5,9 +5,11 @@
 // launch, int32 or int64 positions, grid sized from occupancy x SM count, the
 // CUDA launch error checked), restated for this library's kernels.
 //
-// One kernel computes the op: the register kernel qknr_fused_kernel
-// (qknr_kernel.cuh), which loads straight into registers and takes any
-// accepted shape and alignment.
+// Two kernels compute the op, with the same bits: the register kernel
+// qknr_fused_kernel (qknr_kernel.cuh), which loads straight into registers,
+// and the ring kernel qknr_ring_kernel (qknr_ring_kernel.cuh), which
+// double-buffers each warp's items in shared memory with bulk copies. The
+// work map picks one per call by a measured rule (plan_register).
 //
 // Entry points beyond the op itself: the position-checked variants (one with
 // no allocation), the unfused two-kernel baseline, the host-buffer variant
@@ -15,6 +17,7 @@
 #include "../../include/qknr.h"
 #include "qknr_dispatch.h"
 #include "qknr_kernel.cuh"
+#include "qknr_ring_kernel.cuh"
 
 #include <cuda_runtime.h>
 
@@ -39,8 +42,8 @@ namespace {
 using qknr::Params;
 
 constexpr int kMaxDevices = 64;
-constexpr int kVersion = 10300;             // 1.3.0: the register kernel alone
-constexpr int kStatusWords = 2;             // {bad-token count, first bad token}
+constexpr int kVersion = 10400;             // 1.4.0: the ring kernel
+constexpr int kStatusWords = 3;             // {bad-token count, first bad token, watchdog}
 constexpr int kMaxHeads = 1 << 24;                // largest n_qo + n_kv accepted
 constexpr long long kMaxExtentBytes = 1LL << 56;  // largest q or k extent accepted (far above any GPU's memory)
 
@@ -61,7 +64,7 @@ int fail_cuda(cudaError_t e, const char *what) {
 }
 
 // ------------------------------------------------------------------ tuning
-constexpr int kNumTuneKeys = 11;  // keys 2..5, 9 and 10 (QKNR_TUNE_*); the other slots are unused
+constexpr int kNumTuneKeys = 11;  // keys 1..5, 9 and 10 (QKNR_TUNE_*); the other slots are unused
 // the value that means "automatic" for each key
 constexpr int kTuneAuto[kNumTuneKeys] = {0, 0, 0, 0, 0, -1, 0, 0, 0, 0, 0};
 std::atomic<int> g_tune[kNumTuneKeys] = {{0}, {0}, {0}, {0}, {0}, {-1}, {0}, {0}, {0}, {0}, {0}};
@@ -71,6 +74,10 @@ std::once_flag g_env_once;
 
 int tune_check(int key, int value) {
     switch (key) {
+        case QKNR_TUNE_KERNEL:
+            return (value >= 0 && value <= QKNR_KERNEL_RING)
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "kernel must be 0 (auto), 1 (register) or 2 (ring)");
         case QKNR_TUNE_PASSES:
             return (value >= 0 && value <= qknr::kUnrollClass[qknr::kNumUnroll - 1])
                        ? QKNR_OK
@@ -100,14 +107,14 @@ int tune_check(int key, int value) {
     }
 }
 
-// QKNR_TUNE="passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1"
+// QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1"
 void read_env_tuning() {
     const char *s = std::getenv("QKNR_TUNE");
     if (!s) return;
     static const struct {
         const char *name;
         int key;
-    } names[] = {{"passes", QKNR_TUNE_PASSES}, {"threads", QKNR_TUNE_THREADS},
+    } names[] = {{"kernel", QKNR_TUNE_KERNEL}, {"passes", QKNR_TUNE_PASSES}, {"threads", QKNR_TUNE_THREADS},
                  {"ctas", QKNR_TUNE_CTAS_PER_SM}, {"pdl", QKNR_TUNE_PDL},
                  {"order", QKNR_TUNE_ORDER},      {"prefetch", QKNR_TUNE_PREFETCH}};
     std::string spec(s);
@@ -154,9 +161,10 @@ struct ShapeHash {
         return h;
     }
 };
-// The two knobs qknr_tune chooses: warp passes per item and items per warp
-// prefetched into L2 before the wait (0: none).
+// The knobs qknr_tune chooses: the kernel, warp passes per item and items per
+// warp prefetched into L2 before the wait (0: none).
 struct TunedMap {
+    int kernel = QKNR_KERNEL_REGISTER;
     int passes = 0;
     int prefetch = 0;
 };
@@ -164,12 +172,14 @@ struct TunedMap {
 struct DeviceState {
     std::atomic<bool> ready{false};
     int sm_count = 0;
-    unsigned long long *status = nullptr;       // device: kStatusWords words
+    unsigned long long *status = nullptr;       // device: kStatusWords words (position check, watchdog)
     unsigned long long *status_host = nullptr;  // pinned host copy (qknr_init) or nullptr
     std::mutex checked_mu;                      // serialises status read-backs on this device
     // resident CTAs per SM for the register kernel, by (early, dtype, pos64, d_idx, mode, u_idx,
     // rope_dim class, threads class)
     std::atomic<int> occupancy[2][2][2][qknr::kNumHeadDim][2][qknr::kNumUnroll][qknr::kNumRope][4];
+    // the same for the ring kernel, by (early, dtype, pos64, d_idx, mode, rope_dim class, threads class)
+    std::atomic<int> ring_occ[2][2][2][qknr::kNumHeadDim][2][qknr::kNumRope][4];
     // resident CTAs per SM of the unfused-baseline kernels, by (dtype, op-1, pos64, d_idx, mode)
     std::atomic<int> unfused_occ[2][2][2][qknr::kNumHeadDim][2];
     // host-buffer pipeline (qknr_apply_host): a host-to-device and a
@@ -246,15 +256,23 @@ struct WorkMap {
     int r_idx = 0;        // rope_dim class of the instantiation (qknr::kRope*)
     int interleave = 0;   // item order
     int prefetch_items = 0;  // items per warp prefetched into L2 before the wait
+    int smem = 0;            // dynamic shared memory per CTA (ring kernel)
     const void *kernel = nullptr;
 };
 
-// Resident CTAs per SM of `kernel` at `threads` threads and no dynamic shared
-// memory: asked of the occupancy API once, then cached in `slot`.
-int cached_occupancy(std::atomic<int> &slot, const void *kernel, int threads, const char *what, int *out) {
+// Resident CTAs per SM of `kernel` at `threads` threads and `smem` bytes of
+// dynamic shared memory: asked of the occupancy API once, then cached in
+// `slot`. A kernel with dynamic shared memory first gets its limit raised to
+// what the largest CTA (512 threads) would need, once per kernel; that limit
+// is an attribute of the kernel, not of a launch.
+int cached_occupancy(std::atomic<int> &slot, const void *kernel, int threads, const char *what, int *out,
+                     int smem = 0) {
     int v = slot.load(std::memory_order_relaxed);
     if (v == 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, 0);
+        cudaError_t e = cudaSuccess;
+        if (smem > 0)
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, qknr::ring_smem_bytes(512));
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, smem);
         if (e != cudaSuccess) return fail_cuda(e, what);
         if (v <= 0) return fail(QKNR_ERR_CUDA, "%s: the kernel cannot be resident with %d threads", what, threads);
         slot.store(v, std::memory_order_relaxed);
@@ -274,6 +292,13 @@ int resident_ctas(DeviceState &st, int dt, int pos64, int d_idx, int mode, int u
                   int early, const void *kernel, int *out) {
     return cached_occupancy(st.occupancy[early][dt][pos64][d_idx][mode][u_idx][r_idx][threads_index(threads)],
                             kernel, threads, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(register)", out);
+}
+
+const void *ring_kernel(int dt, int early, int pos64, int d_idx, int mode, int r_idx) {
+    return early ? (dt ? qknr::ring_kernel_fp16_early(pos64, d_idx, mode, r_idx)
+                       : qknr::ring_kernel_bf16_early(pos64, d_idx, mode, r_idx))
+                 : (dt ? qknr::ring_kernel_fp16(pos64, d_idx, mode, r_idx)
+                       : qknr::ring_kernel_bf16(pos64, d_idx, mode, r_idx));
 }
 
 const void *register_kernel(int dt, int early, int pos64, int d_idx, int mode, int u_idx, int r_idx) {
@@ -308,16 +333,29 @@ bool tuned_for(DeviceState &st, const Call &c, TunedMap *out) {
     return true;
 }
 
-// Register kernel: items are (token, chunk of warp passes); the default is the
-// largest unroll class (8 x 16-byte loads in flight per lane). `force` (from
-// qknr_tune's measurements) sets the passes per item and the prefetch depth;
-// otherwise an explicit qknr_set_tuning value, then a work map that qknr_tune
-// chose for this shape, then the fixed rule decide.
+// The ring kernel's measured territory (GB300, same-box A/B against the
+// register kernel): NeoX pairing at every size tried (+2 to +10%), and
+// interleaved calls that move at most this many bytes of q and k (+2.5% on
+// a 4608-token DiT call); larger interleaved calls sustain more bandwidth
+// with the register kernel.
+constexpr long long kRingInterleavedMaxBytes = 256LL << 20;
+
+bool ring_by_rule(const Call &c, const WorkMap &wm) {
+    if (wm.u_idx != 1) return false;   // decode-sized calls (items of one or two passes)
+    if (c.is_neox) return true;
+    const long long qk_bytes = 4LL * (c.n_qo + c.n_kv) * c.head_dim * c.num_tokens;
+    return qk_bytes <= kRingInterleavedMaxBytes;
+}
+
+// Items are (token, chunk of warp passes); the default is the largest unroll
+// class (8 x 16-byte loads in flight per lane, or four passes per ring stage).
+// `force` (from qknr_tune's measurements) sets the kernel, the passes per item
+// and the prefetch depth; otherwise an explicit qknr_set_tuning value, then a
+// work map that qknr_tune chose for this shape, then the fixed rule decide.
 int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *force = nullptr) {
     const int d_idx = head_dim_index(c.head_dim);
     const int hpw = heads_per_pass(c.head_dim);
     const int heads = c.n_qo + c.n_kv;
-    wm->kind = QKNR_KERNEL_REGISTER;
     wm->passes_per_token = (heads + hpw - 1) / hpw;
     TunedMap tm;
     const bool tuned = force ? (tm = *force, true) : tuned_for(st, c, &tm);
@@ -348,14 +386,33 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *f
     if (mode == qknr::kInterleaved && wm->u_idx == 1)
         wm->r_idx = c.rope_dim == c.head_dim ? qknr::kRopeFull
                     : (2 * c.rope_dim == c.head_dim ? qknr::kRopeHalf : qknr::kRopeRuntime);
-    wm->kernel = register_kernel(dt, early, pos64, d_idx, mode, wm->u_idx, wm->r_idx);
-    if (!wm->kernel && wm->r_idx != qknr::kRopeRuntime) {
-        wm->r_idx = qknr::kRopeRuntime;
-        wm->kernel = register_kernel(dt, early, pos64, d_idx, mode, wm->u_idx, wm->r_idx);
-    }
-    if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no kernel for this shape");
+    int kind = force ? force->kernel : tune(QKNR_TUNE_KERNEL);
+    if (kind == QKNR_KERNEL_AUTO && tuned) kind = tm.kernel;
+    if (kind == QKNR_KERNEL_AUTO) kind = ring_by_rule(c, *wm) ? QKNR_KERNEL_RING : QKNR_KERNEL_REGISTER;
+    wm->kind = kind;
     int occ = 0;
-    int rc = resident_ctas(st, dt, pos64, d_idx, mode, wm->u_idx, wm->r_idx, threads, early, wm->kernel, &occ);
+    int rc = QKNR_OK;
+    if (kind == QKNR_KERNEL_RING) {
+        wm->kernel = ring_kernel(dt, early, pos64, d_idx, mode, wm->r_idx);
+        if (!wm->kernel && wm->r_idx != qknr::kRopeRuntime) {
+            wm->r_idx = qknr::kRopeRuntime;
+            wm->kernel = ring_kernel(dt, early, pos64, d_idx, mode, wm->r_idx);
+        }
+        if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no ring kernel for this shape");
+        wm->smem = qknr::ring_smem_bytes(threads);
+        rc = cached_occupancy(st.ring_occ[early][dt][pos64][d_idx][mode][wm->r_idx][threads_index(threads)],
+                              wm->kernel, threads, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ring)", &occ,
+                              wm->smem);
+    } else {
+        wm->kernel = register_kernel(dt, early, pos64, d_idx, mode, wm->u_idx, wm->r_idx);
+        if (!wm->kernel && wm->r_idx != qknr::kRopeRuntime) {
+            wm->r_idx = qknr::kRopeRuntime;
+            wm->kernel = register_kernel(dt, early, pos64, d_idx, mode, wm->u_idx, wm->r_idx);
+        }
+        if (!wm->kernel) return fail(QKNR_ERR_UNSUPPORTED, "no kernel for this shape");
+        wm->smem = 0;
+        rc = resident_ctas(st, dt, pos64, d_idx, mode, wm->u_idx, wm->r_idx, threads, early, wm->kernel, &occ);
+    }
     if (rc) return rc;
     const int cap = tune(QKNR_TUNE_CTAS_PER_SM);
     if (cap > 0) occ = std::min(occ, cap);
@@ -508,7 +565,7 @@ void log_launch(const WorkMap &wm, const Call &c) {
                  "%d CTAs/SM, %lld items (%d per token), %d passes per token, rope_dim %s, PDL %s\n",
                  c.num_tokens, c.n_qo, c.n_kv, c.head_dim, c.rope_dim, c.is_neox ? "neox" : "interleaved",
                  (c.dtype & 0xff) == QKNR_FP16 ? "fp16" : "bf16", (c.dtype & QKNR_POS_I64) ? "64" : "32",
-                 "register", wm.grid, wm.threads, wm.ctas_per_sm,
+                 wm.kind == QKNR_KERNEL_RING ? "ring" : "register", wm.grid, wm.threads, wm.ctas_per_sm,
                  wm.items, wm.chunks_per_token, wm.passes_per_token,
                  wm.r_idx == qknr::kRopeRuntime ? "at run time" : "compiled in", wm.pdl ? "on" : "off");
 }
@@ -551,7 +608,7 @@ int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStr
                                                     wm.chunks_per_token);
     prm.eps = c.eps;
     prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = static_cast<size_t>(wm.smem);
     void *args[] = {&prm};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
@@ -570,12 +627,33 @@ int run_checked(DeviceState &st, const WorkMap &wm, const Call &c, cudaStream_t 
                         cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail_cuda(e, "status read-back");
+    if (host_words[qknr::kStatusWatchdog]) {
+        e = cudaMemsetAsync(st.status + qknr::kStatusWatchdog, 0, sizeof(unsigned long long), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return fail_cuda(e, "watchdog reset");
+        return fail(QKNR_ERR_WATCHDOG,
+                    "a bounded wait in a kernel on this device ran out (this call or an earlier "
+                    "unchecked one); that call's output is incomplete");
+    }
     if (host_words[0]) {
         return fail(QKNR_ERR_POSITION_OOB,
                     "%llu token(s) have positions outside [0, %lld); first bad token index %llu (left untouched)",
                     host_words[0], c.cache_len, host_words[1]);
     }
     return QKNR_OK;
+}
+
+// The watchdog's run-out path, on purpose: one warp waits, with the ring
+// kernel's bounded wait, on an mbarrier that nothing arrives on. After the
+// limit the wait gives up and the watchdog word is set, as a stalled
+// ring-kernel wait would set it; nothing faults and the context stays usable.
+__global__ void qknr_watchdog_selftest_kernel(unsigned long long *status) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x == 0) {
+        qknr::mbar_init(qknr::smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!qknr::mbar_wait(qknr::smem_u32(&bar), 0u)) atomicOr(status + qknr::kStatusWatchdog, 1ull);
+    }
 }
 
 int apply_impl(const Call &c, void *stream, bool checked) {
@@ -661,7 +739,7 @@ int apply_checked_noalloc_impl(const Call &c, void *stream) {
     rc = plan(slot.state, c, &wm);
     if (rc) return rc;
     std::lock_guard<std::mutex> lock(slot.state.checked_mu);
-    unsigned long long host_words[kStatusWords] = {0ull, 0ull};
+    unsigned long long host_words[kStatusWords] = {0ull, 0ull, 0ull};
     return run_checked(slot.state, wm, c, static_cast<cudaStream_t>(stream), host_words);
 }
 
@@ -1026,7 +1104,7 @@ int tune_impl(const Call &shape, void *stream, TunedMap *best_out, double *best_
         c.cache_len = 0;
     }
 
-    // candidates: distinct (passes per item, prefetch depth) pairs
+    // candidates: distinct (kernel, passes per item, prefetch depth) triples
     const int hpw = heads_per_pass(shape.head_dim);
     const int ppt = (shape.n_qo + shape.n_kv + hpw - 1) / hpw;
     std::vector<TunedMap> cands;
@@ -1034,13 +1112,15 @@ int tune_impl(const Call &shape, void *stream, TunedMap *best_out, double *best_
     for (int passes : {4, 3, 2, 1}) {
         const int chunks = (ppt + passes - 1) / passes;
         if (!seen_chunks.insert(chunks).second) continue;
-        if (passes < 4 && cands.size() >= 6) break;
-        for (int pf : {4, 2, 1, 0}) {
-            TunedMap m;
-            m.passes = passes;
-            m.prefetch = pf;
-            cands.push_back(m);
-        }
+        if (passes < 4 && cands.size() >= 12) break;
+        for (int kernel : {QKNR_KERNEL_REGISTER, QKNR_KERNEL_RING})
+            for (int pf : {4, 2, 1, 0}) {
+                TunedMap m;
+                m.kernel = kernel;
+                m.passes = passes;
+                m.prefetch = pf;
+                cands.push_back(m);
+            }
     }
     std::vector<WorkMap> maps(cands.size());
     for (size_t i = 0; i < cands.size(); ++i) {
@@ -1158,6 +1238,10 @@ int qknr_init(int device) {
                             for (auto &u : d)
                                 for (auto &r : u)
                                     for (auto &x : r) x.store(0);
+        // the ring kernels' cached occupancy goes with the limit on their
+        // dynamic shared memory, which a new context no longer has
+        std::atomic<int> *ring = &st.ring_occ[0][0][0][0][0][0][0];
+        for (size_t i = 0; i < sizeof(st.ring_occ) / sizeof(st.ring_occ[0][0][0][0][0][0][0]); ++i) ring[i].store(0);
         st.ready.store(true, std::memory_order_release);
     } else {
         if (st.status) cudaFree(st.status);
@@ -1265,6 +1349,33 @@ int qknr_apply_strided(void *q, void *k, const void *q_w, const void *k_w, const
     return apply_strided_impl(c, stream);
 }
 
+int qknr_sync(void *stream) {
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(st->checked_mu);
+    unsigned long long *word = st->status_host + qknr::kStatusWatchdog;
+    cudaError_t e = cudaMemcpyAsync(word, st->status + qknr::kStatusWatchdog, sizeof(unsigned long long),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "watchdog read-back");
+    if (*word == 0) return QKNR_OK;
+    e = cudaMemsetAsync(st->status + qknr::kStatusWatchdog, 0, sizeof(unsigned long long), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "watchdog reset");
+    return fail(QKNR_ERR_WATCHDOG, "a bounded wait in a kernel on this device ran out; the output of the call "
+                                   "it belonged to is incomplete");
+}
+
+int qknr_selftest_watchdog(void *stream) {
+    DeviceState *st = current_state();
+    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
+    qknr_watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st->status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "watchdog self-test launch");
+    return QKNR_OK;
+}
+
 int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim, int is_neox, int64_t q_stride,
               int64_t k_stride, int64_t head_stride, int dtype, void *stream, int64_t *out) {
     const Call c = make_call(nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, num_tokens, n_qo, n_kv, head_dim,
@@ -1287,7 +1398,7 @@ int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim
     out[5] = wm.ctas_per_sm;
     out[6] = wm.pdl;
     out[7] = wm.passes_per_token;
-    out[8] = qknr::kUnrollClass[wm.u_idx];
+    out[8] = wm.kind == QKNR_KERNEL_RING ? qknr::kRingMaxPasses : qknr::kUnrollClass[wm.u_idx];
     out[9] = wm.interleave ? 2 : 1;
     out[10] = wm.prefetch_items;
     out[11] = wm.r_idx == qknr::kRopeFull ? c.head_dim : (wm.r_idx == qknr::kRopeHalf ? c.head_dim / 2 : 0);
@@ -1309,7 +1420,7 @@ int qknr_set_tuning(int key, int value) {
 
 int qknr_get_tuning(int key, int *value) {
     if (!value) return fail(QKNR_ERR_INVALID_ARG, "value is null");
-    if (key != QKNR_TUNE_PASSES && key != QKNR_TUNE_THREADS && key != QKNR_TUNE_CTAS_PER_SM &&
+    if (key != QKNR_TUNE_KERNEL && key != QKNR_TUNE_PASSES && key != QKNR_TUNE_THREADS && key != QKNR_TUNE_CTAS_PER_SM &&
         key != QKNR_TUNE_PDL && key != QKNR_TUNE_ORDER && key != QKNR_TUNE_PREFETCH)
         return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
     *value = tune(key);
@@ -1343,7 +1454,7 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     out[5] = wm.ctas_per_sm;
     out[6] = wm.pdl;
     out[7] = wm.passes_per_token;
-    out[8] = qknr::kUnrollClass[wm.u_idx];
+    out[8] = wm.kind == QKNR_KERNEL_RING ? qknr::kRingMaxPasses : qknr::kUnrollClass[wm.u_idx];
     out[9] = wm.interleave ? 2 : 1;
     out[10] = wm.prefetch_items;
     out[11] = wm.r_idx == qknr::kRopeFull ? head_dim : (wm.r_idx == qknr::kRopeHalf ? head_dim / 2 : 0);

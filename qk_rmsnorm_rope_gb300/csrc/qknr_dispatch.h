@@ -25,6 +25,14 @@ const void *kernel_fp16(int pos64, int d_idx, int mode, int u_idx, int r_idx);
 const void *kernel_bf16_early(int pos64, int d_idx, int mode, int u_idx, int r_idx);
 const void *kernel_fp16_early(int pos64, int d_idx, int mode, int u_idx, int r_idx);
 
+// Ring kernel entry for (position type, head_dim class, mode, rope_dim class),
+// or nullptr; items of at most four warp passes. Defined in
+// qknr_inst_ring_{bf16,fp16}[_early].cu.
+const void *ring_kernel_bf16(int pos64, int d_idx, int mode, int r_idx);
+const void *ring_kernel_fp16(int pos64, int d_idx, int mode, int r_idx);
+const void *ring_kernel_bf16_early(int pos64, int d_idx, int mode, int r_idx);
+const void *ring_kernel_fp16_early(int pos64, int d_idx, int mode, int r_idx);
+
 // One step of the unfused two-kernel baseline (op = kOpNorm or kOpRope), the
 // register kernel with 4 passes per item. Norm-only ignores pos64 and mode.
 const void *unfused_kernel_bf16(int op, int pos64, int d_idx, int mode);

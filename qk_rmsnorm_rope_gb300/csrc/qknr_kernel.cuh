@@ -115,6 +115,152 @@ __device__ __noinline__ void prefetch_first_items(const Params &p, long long it_
     }
 }
 
+// Lane geometry of a head: a head's data takes NVH lanes (two 16-byte
+// vectors each); its lane group is LPH lanes, NVH rounded up to a power of two
+// (head_dim 80, 96 and 192 leave 2 and 4 lanes of the group idle: no loads, no
+// stores, zero in the sum); a warp pass covers HPW heads.
+template <int D>
+struct HeadGeom {
+    static constexpr int NVH = D / 16;
+    static constexpr int LPH = NVH <= 1 ? 1 : NVH <= 2 ? 2 : NVH <= 4 ? 4 : NVH <= 8 ? 8 : NVH <= 16 ? 16 : 32;
+    static constexpr int HPW = kWarp / LPH;
+    static_assert(D % 16 == 0 && NVH >= 1 && NVH <= kWarp, "head_dim");
+};
+
+// What one lane owns of its head: the two 16-byte vectors (vector v = dims
+// [8v, 8v+8)) and their role in the rotation.
+struct LaneMap {
+    int va, vb;
+    bool split;      // NeoX rope_dim % 16 == 0 layout
+    bool rot_lane;   // this lane holds rotated dims
+    bool active;     // this lane holds data (l < NVH)
+};
+
+// Interleaved pairs (2j, 2j+1) sit inside one vector. NeoX with rope_dim % 16
+// == 0: a rotating lane owns dims [8a, 8a+8) and [8a+R/2, 8a+R/2+8), both
+// halves of eight rotation pairs; lanes past the rotated span own one vector
+// from each half of the tail. NeoX with rope_dim <= 8: all of it in vector 0.
+template <int D, int MODE>
+__device__ __forceinline__ LaneMap lane_map(int l, int R) {
+    constexpr int NVH = HeadGeom<D>::NVH;
+    LaneMap m;
+    m.split = false;
+    if (MODE == kNeox && (R & 15) == 0) {
+        m.split = true;
+        const int rl = R >> 4;          // lanes holding rotation pairs
+        if (l < rl) {
+            m.va = l;
+            m.vb = l + rl;
+            m.rot_lane = true;
+        } else {
+            m.va = (R >> 3) + (l - rl);
+            m.vb = m.va + ((D - R) >> 4);
+            m.rot_lane = false;
+        }
+    } else {
+        m.va = l;
+        m.vb = l + NVH;
+        m.rot_lane = (MODE == kNeox) ? (l == 0) : (8 * m.va < R);
+    }
+    m.active = l < NVH;
+    if (!m.active) {
+        m.va = 0;
+        m.vb = 0;
+        m.rot_lane = false;
+    }
+    return m;
+}
+
+// First and end pass of chunk `ch` of a token: from the host's table, or by
+// division. An integer division costs about twenty instructions and the
+// kernels run their items back to back, so the table is worth 1-2%
+// (interleaved); the NeoX instantiations keep the division, which measured
+// faster there.
+template <int MODE>
+__device__ __forceinline__ void item_passes(const Params &p, int chunks, int ch, int &pb, int &pe) {
+    if (MODE == kInterleaved && chunks <= kBoundTable) {
+        pb = p.pass_bound[ch];
+        pe = p.pass_bound[ch + 1];
+    } else {
+        pb = chunks == 1 ? 0 : (ch * p.passes_per_token) / chunks;
+        pe = chunks == 1 ? p.passes_per_token : ((ch + 1) * p.passes_per_token) / chunks;
+    }
+}
+
+// A new token's position, checked against the cache when the call asks for it
+// (cache_len > 0): `ok` becomes false for a position outside the cache, and the
+// first chunk's lane 0 counts the bad token once. Otherwise `ok` is left as it is.
+__device__ __forceinline__ void check_position(const Params &p, long long pos, long long t, int ch, int lane,
+                                               bool &ok) {
+    if (p.cache_len > 0) {
+        ok = pos >= 0 && pos < p.cache_len;
+        if (!ok && ch == 0 && lane == 0) {
+            atomicAdd(p.status, 1ull);
+            atomicMin(p.status + 1, static_cast<unsigned long long>(t));
+        }
+    }
+}
+
+// The token's cos and (sign-free) sin per owned element. Interleaved:
+// c[m]/s[m] serve pair m of vector a (m < 4) and pair m-4 of vector b (m >=
+// 4). NeoX split: c[e]/s[e] serve element e of both vectors. NeoX small:
+// element e < R/2 of vector 0. Identity (1, 0) wherever nothing rotates.
+template <int MODE>
+__device__ __forceinline__ void token_cos_sin(const Params &p, long long pos, bool load, int va, int vb, bool split,
+                                              int R, int half, float (&c)[8], float (&s)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) { c[e] = 1.f; s[e] = 0.f; }
+    if (load) {
+        const float *row = p.cache + pos * R;
+        if (MODE == kInterleaved) {
+            if (p.cache_vec && 8 * va + 8 <= R) {
+                const float4 ca = __ldg(reinterpret_cast<const float4 *>(row + 4 * va));
+                const float4 sa = __ldg(reinterpret_cast<const float4 *>(row + half + 4 * va));
+                c[0] = ca.x; c[1] = ca.y; c[2] = ca.z; c[3] = ca.w;
+                s[0] = sa.x; s[1] = sa.y; s[2] = sa.z; s[3] = sa.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = 4 * va + q;
+                    if (2 * j < R) { c[q] = __ldg(row + j); s[q] = __ldg(row + half + j); }
+                }
+            }
+            if (p.cache_vec && 8 * vb + 8 <= R) {
+                const float4 cb = __ldg(reinterpret_cast<const float4 *>(row + 4 * vb));
+                const float4 sb = __ldg(reinterpret_cast<const float4 *>(row + half + 4 * vb));
+                c[4] = cb.x; c[5] = cb.y; c[6] = cb.z; c[7] = cb.w;
+                s[4] = sb.x; s[5] = sb.y; s[6] = sb.z; s[7] = sb.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = 4 * vb + q;
+                    if (2 * j < R) { c[4 + q] = __ldg(row + j); s[4 + q] = __ldg(row + half + j); }
+                }
+            }
+        } else if (split) {
+            const int j0 = 8 * va;      // dims [j0, j0+8) of the first half
+            if (p.cache_vec) {
+                const float4 c0 = __ldg(reinterpret_cast<const float4 *>(row + j0));
+                const float4 c1 = __ldg(reinterpret_cast<const float4 *>(row + j0 + 4));
+                const float4 s0 = __ldg(reinterpret_cast<const float4 *>(row + half + j0));
+                const float4 s1 = __ldg(reinterpret_cast<const float4 *>(row + half + j0 + 4));
+                c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+                c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+                s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+                s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { c[e] = __ldg(row + j0 + e); s[e] = __ldg(row + half + j0 + e); }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (e < half) { c[e] = __ldg(row + e); s[e] = __ldg(row + half + e); }
+            }
+        }
+    }
+}
+
 // T: storage type (bf16/half); P: position type (int / long long);
 // D: head_dim; MODE: pairing; UMAX: max warp passes per item (loads in flight);
 // OP: fused (the product) or one step of the unfused baseline;
@@ -127,48 +273,17 @@ __device__ __noinline__ void prefetch_first_items(const Params &p, long long it_
 // pairing it measured slower (the compiler's schedule of the split layout).
 template <class T, class P, int D, int MODE, int UMAX, int OP = kOpFused, bool EARLY = false, int RC = 0>
 __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__ Params p) {
-    // A head's data takes NVH lanes (two 16-byte vectors each); its lane group
-    // is LPH lanes, NVH rounded up to a power of two (head_dim 80, 96 and 192 leave
-    // 2 and 4 lanes of the group idle: no loads, no stores, zero in the sum).
-    constexpr int NVH = D / 16;
-    constexpr int LPH = NVH <= 1 ? 1 : NVH <= 2 ? 2 : NVH <= 4 ? 4 : NVH <= 8 ? 8 : NVH <= 16 ? 16 : 32;
-    constexpr int HPW = kWarp / LPH;    // heads per warp pass
-    static_assert(D % 16 == 0 && NVH >= 1 && NVH <= kWarp, "head_dim");
+    constexpr int LPH = HeadGeom<D>::LPH;
+    constexpr int HPW = HeadGeom<D>::HPW;    // heads per warp pass
 
     const int lane = threadIdx.x & (kWarp - 1);
     const int g = lane / LPH;           // head slot within the pass
-    const int l = lane % LPH;           // lane within the head
     const int R = RC > 0 ? RC : p.rope_dim;
     const int half = R >> 1;
     const int H = p.n_qo + p.n_kv;
-
-    // The two 16-byte vectors (vector v = dims [8v, 8v+8)) this lane owns.
-    int va, vb;
-    bool split = false;                 // NeoX rope_dim % 16 == 0 layout
-    bool rot_lane;                      // this lane holds rotated dims
-    if (MODE == kNeox && (R & 15) == 0) {
-        split = true;
-        const int rl = R >> 4;          // lanes holding rotation pairs
-        if (l < rl) {
-            va = l;
-            vb = l + rl;
-            rot_lane = true;
-        } else {
-            va = (R >> 3) + (l - rl);
-            vb = va + ((D - R) >> 4);
-            rot_lane = false;
-        }
-    } else {
-        va = l;
-        vb = l + NVH;
-        rot_lane = (MODE == kNeox) ? (l == 0) : (8 * va < R);
-    }
-    const bool active = l < NVH;
-    if (!active) {
-        va = 0;
-        vb = 0;
-        rot_lane = false;
-    }
+    const LaneMap lm = lane_map<D, MODE>(lane % LPH, R);
+    const int va = lm.va, vb = lm.vb;
+    const bool split = lm.split, rot_lane = lm.rot_lane, active = lm.active;
 
     const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long warp_id = gtid / kWarp;
@@ -243,18 +358,8 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
             ch += step_c;
             if (ch >= chunks) { ch -= chunks; ++t; }
         }
-        // The item's passes [pb, pe): from the host's table, or by division. An
-        // integer division costs about twenty instructions and the kernel runs
-        // its items back to back, so the table is worth 1-2% (interleaved); the
-        // NeoX instantiations keep the division, which measured faster there.
-        int pb, pe;
-        if (MODE == kInterleaved && chunks <= kBoundTable) {
-            pb = p.pass_bound[ch];
-            pe = p.pass_bound[ch + 1];
-        } else {
-            pb = chunks == 1 ? 0 : (ch * p.passes_per_token) / chunks;
-            pe = chunks == 1 ? p.passes_per_token : ((ch + 1) * p.passes_per_token) / chunks;
-        }
+        int pb, pe;                     // the item's passes [pb, pe)
+        item_passes<MODE>(p, chunks, ch, pb, pe);
 
         // this token's rows; k's is shifted back by n_qo heads so that head h
         // (q heads first, then k heads) is row + h * head_stride for both
@@ -283,13 +388,10 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
         if (OP != kOpNorm && t != cur_t) {
             cur_t = t;
             const long long pos = __shfl_sync(0xffffffffu, my_pos, jb);
-            if (p.cache_len > 0) {
-                tok_ok = pos >= 0 && pos < p.cache_len;
-                if (!tok_ok && ch == 0 && lane == 0) {
-                    atomicAdd(p.status, 1ull);
-                    atomicMin(p.status + 1, static_cast<unsigned long long>(t));
-                }
-            }
+            check_position(p, pos, t, ch, lane, tok_ok);
+            // token_cos_sin, written out: as a call it changed this kernel's
+            // register allocation and spills (ptxas), and this close to the
+            // bandwidth limit such changes move its time
 #pragma unroll
             for (int e = 0; e < 8; ++e) { c[e] = 1.f; s[e] = 0.f; }
             if (tok_ok && rot_lane) {

@@ -20,8 +20,11 @@ struct RegisterTable {
     template <class P, int D, int MODE>
     static const void *by_unroll(int u_idx, int r_idx) {
         if (r_idx != kRopeRuntime) {
-            if (MODE != kInterleaved || u_idx != 1 || (D != 64 && D != 128 && D != 256)) return nullptr;
-            return r_idx == kRopeFull ? entry<P, D, MODE, 4, D>() : entry<P, D, MODE, 4, D / 2>();
+            if constexpr (MODE == kInterleaved && (D == 64 || D == 128 || D == 256)) {
+                if (u_idx != 1) return nullptr;
+                return r_idx == kRopeFull ? entry<P, D, MODE, 4, D>() : entry<P, D, MODE, 4, D / 2>();
+            }
+            return nullptr;
         }
         switch (u_idx) {
             case 0: return entry<P, D, MODE, 2>();

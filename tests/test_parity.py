@@ -143,6 +143,58 @@ def test_workload_full_size_every_element(qknr, name):
                            cpu["buffer"][:, lo:, :].view(torch.int16))
 
 
+@pytest.mark.parametrize("name", ["dit", "mha_neox", "gqa", "fused_qkv"])
+def test_kernels_agree_at_full_size(qknr, name):
+    """Full size: the register kernel and the ring kernel, each forced, give the
+    same bits on copies of one input (the default launch of each workload is
+    compared with the oracle element by element above, so both kernels are
+    pinned to it at the sizes the benchmark runs)."""
+    w = workloads.get(name)
+    cpu = workloads.make_inputs(w)
+    outs = []
+    for kernel in ("register", "ring"):
+        dev = workloads.to_device(cpu, w, "cuda")
+        qknr.set_tuning(reset=True, kernel=kernel)
+        try:
+            _run_gpu(qknr, dev, w)
+        finally:
+            qknr.set_tuning(reset=True)
+        key = "buffer" if w.fused_total_heads else None
+        outs.append([dev[key].view(torch.int16)] if key else [dev["q"].view(torch.int16),
+                                                              dev["k"].view(torch.int16)])
+        del dev
+    for a, b in zip(*outs):
+        assert torch.equal(a, b), name
+
+
+def test_watchdog_selftest_reports_once(qknr):
+    """The ring kernel's bounded wait, run out on purpose (a barrier nothing
+    arrives on): qknr_sync reports QKNR_ERR_WATCHDOG once and clears it, the
+    context stays usable, and a checked call reports a run-out that happened
+    before it."""
+    stream = torch.cuda.current_stream().cuda_stream
+    assert qknr.qknr_sync(stream) == 0
+    assert qknr.qknr_selftest_watchdog(stream) == 0
+    assert qknr.qknr_sync(stream) == 7, qknr.qknr_last_error()
+    assert "ran out" in qknr.qknr_last_error()
+    assert qknr.qknr_sync(stream) == 0
+    # the context is still usable: a normal call matches the oracle
+    w = workloads.scaled(workloads.get("gqa"), 333, cache_len=4096)
+    qknr.set_tuning(reset=True, kernel="ring")
+    try:
+        _check_workload(qknr, w)
+        assert qknr.qknr_selftest_watchdog(stream) == 0
+        cpu = workloads.make_inputs(w)
+        dev = workloads.to_device(cpu, w, "cuda")
+        with pytest.raises(qknr.QknrError) as ei:
+            qknr.apply_checked(dev["q"], dev["k"], dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
+                               dev["positions"], is_neox=w.is_neox, eps=w.eps)
+        assert ei.value.code == 7
+    finally:
+        qknr.set_tuning(reset=True)
+    assert qknr.qknr_sync(stream) == 0
+
+
 def _rope_dims(D, neox):
     if neox:
         return sorted({r for r in (4, 8, 16, 32, 64, D // 2, D) if r <= D and (r % 16 == 0 or r <= 8)})
@@ -164,14 +216,16 @@ def _make(D, R, neox, pos, T, n_qo, n_kv, dtype="bf16", seed=0, cache_len=300, b
                               seed=seed)
 
 
-@pytest.mark.parametrize("order", ["interleaved", "contiguous"])
+@pytest.mark.parametrize("kernel,order", [("register", "interleaved"), ("register", "contiguous"),
+                                          ("ring", "interleaved"), ("ring", "contiguous")])
 @pytest.mark.parametrize("D,R,neox,pos,T", GRID,
                          ids=[f"D{g[0]}-R{g[1]}-{'neox' if g[2] else 'inter'}-{g[3]}-T{g[4]}"
                               for g in GRID])
-def test_shape_grid(qknr, D, R, neox, pos, T, order):
-    """The grid in both item orders (interleaved is the automatic one)."""
+def test_shape_grid(qknr, D, R, neox, pos, T, kernel, order):
+    """The grid with both kernels forced, in both item orders (interleaved is
+    the automatic one)."""
     w = _make(D, R, neox, pos, T, 4, 2, dtype="bf16" if (D + R + T) % 2 == 0 else "fp16")
-    qknr.set_tuning(reset=True, order=2 if order == "interleaved" else 1)
+    qknr.set_tuning(reset=True, kernel=kernel, order=2 if order == "interleaved" else 1)
     try:
         _check_workload(qknr, w)
     finally:
@@ -205,6 +259,14 @@ TUNINGS = [
     dict(prefetch=1, order=1),
     dict(prefetch=2, passes=1, threads=64),
     dict(prefetch=4, pdl=0),
+    dict(kernel=1),
+    dict(kernel=2),
+    dict(kernel=2, passes=1, threads=64, ctas_per_sm=1),
+    dict(kernel=2, passes=2, threads=128),
+    dict(kernel=2, passes=3, threads=512),
+    dict(kernel=2, order=1, prefetch=-1),
+    dict(kernel=2, pdl=0, prefetch=1),
+    dict(kernel=2, threads=64, ctas_per_sm=2, prefetch=2),
 ]
 
 
@@ -214,7 +276,8 @@ def test_tunings_agree_bit_for_bit(qknr, tuning):
     gives the same bits as the automatic one, and all match the oracle. Covers
     one to four passes per item, several items per token, both item orders,
     one or two CTAs per SM, launches with and without programmatic dependent
-    launch, and every depth of the L2 prefetch before the wait."""
+    launch, every depth of the L2 prefetch before the wait, and both kernels
+    (register and ring) under each kind of setting."""
     for name, T in (("mha_neox", 97), ("fused_qkv", 41), ("tiny", 16), ("gqa", 50)):
         base = workloads.get(name)
         w = workloads.scaled(base, T, cache_len=min(base.cache_len, 4096))
@@ -236,19 +299,28 @@ def test_tunings_agree_bit_for_bit(qknr, tuning):
 
 
 def test_work_map_choice(qknr):
-    """The automatic launch: the register kernel, 4-pass items interleaved over
-    a persistent grid of at most one wave of resident CTAs; 1-pass items for a
-    call too small to give every SM several warps."""
-    bf = qknr.QKNR_BF16
-    m = qknr.work_map(4608, 24, 24, 128, 128, False, bf)
-    assert m["kernel"] == "register" and m["order"] == "interleaved"
+    """The automatic launch: 4-pass items interleaved over a persistent grid of
+    at most one wave of resident CTAs, with the ring kernel for NeoX pairing and
+    for interleaved calls of at most 256 MiB of q and k, the register kernel for
+    larger interleaved calls; 1-pass items on the register kernel for a call
+    too small to give every SM several warps."""
+    bf, fp = qknr.QKNR_BF16, qknr.QKNR_FP16 | qknr.QKNR_POS_I64
+    m = qknr.work_map(4608, 24, 24, 128, 128, False, bf)           # DiT: 113 MB of q and k
+    assert m["kernel"] == "ring" and m["order"] == "interleaved"
     assert m["unroll"] == 4 and m["passes_per_token"] == 12 and m["items_per_token"] == 3
     assert m["items"] == 4608 * 3 and m["threads"] == 256 and m["pdl"] == 1
     assert m["prefetch_items"] == 4 and m["rope_dim_compiled"] == 128
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert m["grid"] <= m["ctas_per_sm"] * sms
+    assert m["grid"] <= m["ctas_per_sm"] * sms and m["ctas_per_sm"] == 2
+    assert qknr.work_map(65536, 16, 4, 256, 128, False, bf)["kernel"] == "register"   # 1.3 GB
+    assert qknr.work_map(16384, 32, 8, 128, 64, True, fp)["kernel"] == "ring"
+    assert qknr.work_map(65536, 32, 8, 128, 64, True, fp)["kernel"] == "ring"         # NeoX: any size
+    limit = (256 << 20) // (4 * 48 * 128)                            # tokens of 48 heads in 256 MiB
+    assert qknr.work_map(limit, 24, 24, 128, 128, False, bf)["kernel"] == "ring"
+    assert qknr.work_map(limit + 1, 24, 24, 128, 128, False, bf)["kernel"] == "register"
     small = qknr.work_map(4, 4, 2, 128, 6, False, bf)
     assert small["kernel"] == "register" and small["items_per_token"] == small["passes_per_token"]
+    assert qknr.work_map(4, 4, 2, 128, 64, True, fp)["kernel"] == "register"
 
 
 def test_separate_strides_and_padded_heads(qknr):
@@ -340,14 +412,16 @@ def test_independent_head_strides_errors(qknr):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("kernel", ["register", "ring"])
 @pytest.mark.parametrize("pdl", [-1, 0])
-def test_cuda_graph_capture_and_replay(qknr, pdl):
+def test_cuda_graph_capture_and_replay(qknr, pdl, kernel):
     """Calls captured into a CUDA graph (two calls on different buffers, with
-    programmatic dependent launch on or off) replay to the same bits as eager
-    calls, on new values written into the captured buffers."""
+    programmatic dependent launch on or off, either kernel forced) replay to
+    the same bits as eager calls, on new values written into the captured
+    buffers."""
     base = workloads.get("gqa")
     ws = [workloads.scaled(base, 70, cache_len=4096), workloads.scaled(workloads.get("dit"), 33)]
-    qknr.set_tuning(pdl=pdl)
+    qknr.set_tuning(pdl=pdl, kernel=kernel)
     try:
         devs = [workloads.to_device(workloads.make_inputs(w), w, "cuda") for w in ws]
         s = torch.cuda.Stream()

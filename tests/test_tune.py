@@ -56,12 +56,13 @@ def test_tune_records_a_candidate_and_later_calls_use_it(qknr, name, T):
     assert torch.equal(dev["q"], before_q)                      # tuning ran on scratch only
     passes_item = -(-m["passes_per_token"] // m["items_per_token"])
     assert passes_item in (1, 2, 3, 4) and m["prefetch_items"] in (0, 1, 2, 4), m
-    assert m["ns_per_launch"] > 0
+    assert m["kernel"] in ("register", "ring") and m["ns_per_launch"] > 0
     if not w.fused_total_heads:
         # the work map of the (contiguous) shape reports the tuned choice
         wm = qknr.work_map(w.num_tokens, w.n_qo, w.n_kv, w.head_dim, w.rope_dim, w.is_neox,
                            qknr.dtype_code(w.torch_dtype, w.pos_torch_dtype))
-        assert (wm["items_per_token"], wm["prefetch_items"]) == (m["items_per_token"], m["prefetch_items"])
+        assert (wm["kernel"], wm["items_per_token"], wm["prefetch_items"]) == (
+            m["kernel"], m["items_per_token"], m["prefetch_items"])
     _apply(qknr, dev, w)
     assert torch.equal(dev["q"].view(torch.int16), untuned["q"].view(torch.int16))
     assert torch.equal(dev["k"].view(torch.int16), untuned["k"].view(torch.int16))
@@ -85,15 +86,16 @@ def test_explicit_tuning_wins_and_shutdown_forgets(qknr):
         qknr.set_tuning(reset=True)
     assert forced["items_per_token"] == forced["passes_per_token"] and forced["prefetch_items"] == 0
     tuned = qknr.work_map(w.num_tokens, w.n_qo, w.n_kv, w.head_dim, w.rope_dim, False, code)
-    assert (tuned["items_per_token"], tuned["prefetch_items"]) == (m["items_per_token"], m["prefetch_items"])
+    assert (tuned["kernel"], tuned["items_per_token"], tuned["prefetch_items"]) == (
+        m["kernel"], m["items_per_token"], m["prefetch_items"])
     # another token count is another shape: the fixed rule
     other = qknr.work_map(w.num_tokens + 1, w.n_qo, w.n_kv, w.head_dim, w.rope_dim, False, code)
     assert other["prefetch_items"] == rule["prefetch_items"]
     assert qknr.qknr_shutdown() == 0
     qknr.init(0)
     again = qknr.work_map(w.num_tokens, w.n_qo, w.n_kv, w.head_dim, w.rope_dim, False, code)
-    assert (again["items_per_token"], again["prefetch_items"]) == (rule["items_per_token"],
-                                                                  rule["prefetch_items"])
+    assert (again["kernel"], again["items_per_token"], again["prefetch_items"]) == (
+        rule["kernel"], rule["items_per_token"], rule["prefetch_items"])
 
 
 def test_tune_refuses_bad_layouts(qknr):
