@@ -67,12 +67,11 @@ extern "C" {
 #define QKNR_ERR_MISALIGNED 4      /* pointer or stride breaks the 16-byte vector rule */
 #define QKNR_ERR_CUDA 5            /* a CUDA runtime call failed; message has the CUDA error */
 #define QKNR_ERR_POSITION_OOB 6    /* qknr_apply_checked: a position outside [0, cache_len) */
-#define QKNR_ERR_WATCHDOG 7        /* a bounded wait inside a kernel ran out; that call's output is incomplete */
 
 /*
  * Prepare the library for CUDA device `device`: reads the SM count and other
- * limits, and allocates a 24-byte status block (the position-check counters
- * of qknr_apply_checked and the ring kernel's watchdog word, see qknr_sync).
+ * limits, and allocates a 16-byte status block (the position-check counters
+ * of qknr_apply_checked).
  * Idempotent; safe to call from several threads. Restores the caller's
  * current device before returning. Returns QKNR_OK or QKNR_ERR_CUDA /
  * QKNR_ERR_INVALID_ARG (no such device).
@@ -135,12 +134,10 @@ int qknr_can_use(int head_dim, int rope_dim, int is_neox, int dtype);
  *
  * Kernels: the library has two kernels with identical results, chosen per
  * call by a measured rule (or by qknr_tune / qknr_set_tuning): the register
- * kernel, which loads each warp item straight into registers, and the ring
- * kernel, which double-buffers each warp's items in shared memory with bulk
- * copies (TMA) and takes NeoX calls and interleaved calls of up to 256 MiB of
- * q and k. The ring kernel's waits are bounded; one that runs out (never in
- * normal operation) sets a watchdog word that qknr_sync and the checked entry
- * points report as QKNR_ERR_WATCHDOG.
+ * kernel, which loads each warp item straight into registers (decode-sized
+ * calls), and the ring kernel, which double-buffers each warp's items in
+ * shared memory with asynchronous copies (every larger call), in one of two
+ * issue orders (QKNR_TUNE_RING_ORDER).
  */
 int qknr_apply(void *q, void *k, const void *q_w, const void *k_w, const float *cos_sin_cache,
                const void *positions, int64_t num_tokens, int n_qo, int n_kv, int head_dim,
@@ -152,10 +149,8 @@ int qknr_apply(void *q, void *k, const void *q_w, const void *k_w, const float *
  * whose position is outside are left untouched; all others are computed as by
  * qknr_apply. SYNCHRONOUS: waits for `stream` before returning. Returns
  * QKNR_ERR_POSITION_OOB (message: count and first bad token) if any position
- * was out of range, and QKNR_ERR_WATCHDOG (clearing the word) if a kernel
- * wait on this device ran out since the word was last read. Uses the status
- * words that qknr_init allocated, so calls on one device must not overlap on
- * the GPU (they serialise on the host).
+ * was out of range. Uses the status word that qknr_init allocated, so calls
+ * on one device must not overlap on the GPU (they serialise on the host).
  */
 int qknr_apply_checked(void *q, void *k, const void *q_w, const void *k_w,
                        const float *cos_sin_cache, int64_t cache_len, const void *positions,
@@ -189,9 +184,9 @@ int qknr_apply_unfused(void *q, void *k, const void *q_w, const void *k_w,
  *
  * Same arguments, results and QKNR_ERR_POSITION_OOB report as
  * qknr_apply_checked, but qknr_init is not needed and nothing is allocated:
- * the 24-byte status block lives in a 256-byte file-scope __device__ array
+ * the 16-byte status block lives in a 256-byte file-scope __device__ array
  * of the library, which every GPU that loads the library holds until the
- * process exits. A call needs those 24 bytes whatever its num_tokens, so no
+ * process exits. A call needs those 16 bytes whatever its num_tokens, so no
  * problem size exceeds the array. The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture. That set-up is kept for
@@ -276,52 +271,35 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
                     int64_t head_stride, float eps, int dtype, int64_t chunk_tokens, int flags,
                     void *stream);
 
-/*
- * Reports whether a bounded wait inside a kernel ran out on the current
- * device since the last report (the ring kernel bounds each wait at one
- * second of GPU time; it never runs out in normal operation, and a warp whose
- * wait ran out stops, leaving the rest of its items unprocessed). qknr_apply
- * is asynchronous, so this is how its caller learns of it; the checked entry
- * points report it themselves. Waits for `stream`, then returns QKNR_OK or
- * QKNR_ERR_WATCHDOG and clears the word. Not part of the op on the pages.
- */
-int qknr_sync(void *stream);
-
-/*
- * Exercises the watchdog path for tests of a caller's error handling: on
- * `stream`, one warp waits, with the ring kernel's bounded wait, on an
- * mbarrier that nothing arrives on. After about a second the wait gives up
- * and sets the watchdog word, as a stalled ring-kernel wait would; the next
- * qknr_sync (or checked call) on the device reports QKNR_ERR_WATCHDOG. No
- * fault and no unbounded wait: the context stays usable. Not part of the op.
- */
-int qknr_selftest_watchdog(void *stream);
-
 /* kernels (QKNR_TUNE_KERNEL values and qknr_query_work_map out[0]) */
 #define QKNR_KERNEL_AUTO 0     /* the measured rule (QKNR_TUNE_KERNEL only) */
 #define QKNR_KERNEL_REGISTER 1 /* loads each warp item straight into registers */
-#define QKNR_KERNEL_RING 2     /* double-buffers each warp's items in shared memory (bulk copies) */
+#define QKNR_KERNEL_RING 2     /* double-buffers each warp's items in shared memory (cp.async) */
 
-/* tuning keys for qknr_set_tuning / qknr_get_tuning (6, 7 and 8 are not used) */
+/* tuning keys for qknr_set_tuning / qknr_get_tuning (7 and 8 are not used) */
 #define QKNR_TUNE_RESET 0       /* qknr_set_tuning(QKNR_TUNE_RESET, 0): every key back to automatic */
-#define QKNR_TUNE_KERNEL 1      /* 0 auto (the rule: ring for NeoX and for interleaved calls with at most
-                                   256 MiB of q and k, items of 3-4 passes; else register), 1, 2 */
+#define QKNR_TUNE_KERNEL 1      /* 0 auto (the rule: the ring kernel when items have 3 or 4 passes, the
+                                   register kernel for decode-sized calls), 1 register, 2 ring */
 #define QKNR_TUNE_PASSES 2      /* warp passes per item, 1..4 (0 auto: 4, or 1 when the whole call has
                                    at most 16 warp passes per SM) */
 #define QKNR_TUNE_THREADS 3     /* threads per CTA, 64/128/256/512 (0 auto = 256) */
 #define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy) */
 #define QKNR_TUNE_PDL 5         /* programmatic dependent launch: -1 auto (on), 0 off, 1 on */
+#define QKNR_TUNE_RING_ORDER 6  /* ring kernel's issue order: 0 auto (2 for interleaved calls with more
+                                   than 256 MiB of q and k, else 1), 1 each item's successor issued as
+                                   soon as the item's bytes land, 2 two items ahead after the first */
 #define QKNR_TUNE_ORDER 9       /* item order: 0 auto (= 2), 1 a contiguous range per warp,
                                    2 interleaved (warp w takes items w, w + W, ...) */
 #define QKNR_TUNE_PREFETCH 10   /* items per warp whose q/k rows (and the first positions) are
                                    prefetched into L2 while the kernel waits for the previous one
-                                   on the stream: -1 none, 0 auto (= 4), 1..4 */
+                                   on the stream: -1 none, 0 auto (4 for the register kernel, 1 for
+                                   the ring kernel), 1..4 */
 
 /*
  * Process-wide launch tuning, for benchmarks and tests; results do not depend
  * on it (every setting gives the same bits). Invalid values return
  * QKNR_ERR_INVALID_ARG and change nothing. The environment variable
- * QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1"
+ * QKNR_TUNE="kernel=2,ring_order=1,passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1"
  * sets the same keys at first use.
  */
 int qknr_set_tuning(int key, int value);
@@ -339,8 +317,9 @@ int qknr_get_tuning(int key, int *value);
  * still take precedence. The op has no counterpart of this on the pages,
  * whose kernels fix their launch at compile time.
  *
- * The candidates (both kernels; passes per item 4, 3, 2 or 1 where they chunk
- * a token differently; prefetch of 4, 2, 1 or no items) run on scratch buffers with
+ * The candidates (the register kernel and both orders of the ring kernel;
+ * passes per item 4, 3, 2 or 1 where they chunk a token differently; prefetch
+ * of 4, 2, 1 or no items) run on scratch buffers with
  * the given layout, zero-filled, never on the caller's data, each timed with
  * CUDA events over about 2 ms of launches in three alternating rounds; the
  * one with the lowest median time per launch is kept. Input replicas rotate so
@@ -351,7 +330,7 @@ int qknr_get_tuning(int key, int *value);
  * cos|sin table of min(num_tokens, 65536) rows and positions), so it belongs
  * at set-up time, not on a hot path or inside a stream capture, and it waits
  * for `stream`. out (NULL allowed): QKNR_TUNE_FIELDS values, the chosen work
- * map as qknr_query_work_map reports it (out[0..11]), then out[12] the
+ * map as qknr_query_work_map reports it (out[0..12]), then out[13] the
  * measured time per launch in nanoseconds. A choice is kept until qknr_shutdown; tuning the
  * same shape again replaces it. Errors: QKNR_ERR_NOT_INITIALIZED,
  * QKNR_ERR_INVALID_ARG / UNSUPPORTED / MISALIGNED as qknr_apply would return
@@ -361,8 +340,8 @@ int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim
               int64_t q_stride, int64_t k_stride, int64_t head_stride, int dtype, void *stream,
               int64_t *out);
 
-#define QKNR_WORK_MAP_FIELDS 12
-#define QKNR_TUNE_FIELDS 13
+#define QKNR_WORK_MAP_FIELDS 13
+#define QKNR_TUNE_FIELDS 14
 /*
  * The launch qknr_apply would make for these sizes with contiguous q and k
  * (no launch, no pointers; assumes a 16-byte aligned cos|sin table), including
@@ -375,7 +354,8 @@ int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim
  *    into L2 before the wait for the previous kernel  11 rope_dim compiled
  *    into the instantiation (0: read at run time; interleaved pairing with
  *    4-pass items has instantiations for rope_dim = head_dim and head_dim / 2
- *    at head_dim 64, 128 and 256)
+ *    at head_dim 64, 128 and 256)  12 ring kernel's issue order (1 or 2;
+ *    0 for the register kernel)
  */
 int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim,
                         int is_neox, int dtype, int64_t *out);

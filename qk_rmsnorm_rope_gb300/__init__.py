@@ -21,10 +21,10 @@ __all__ = [
     "QKNR_HOST_DIRECT", "QknrError", "library_path",
     "qknr_init", "qknr_shutdown", "qknr_last_error", "qknr_version", "qknr_can_use",
     "qknr_apply", "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-    "qknr_apply_host", "qknr_apply_strided", "qknr_tune", "qknr_sync", "qknr_selftest_watchdog",
+    "qknr_apply_host", "qknr_apply_strided", "qknr_tune",
     "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map", "TUNE_KEYS",
     "init", "apply", "apply_checked", "apply_unfused", "apply_host", "can_use", "dtype_code",
-    "work_map", "set_tuning", "get_tuning", "tune", "sync",
+    "work_map", "set_tuning", "get_tuning", "tune",
 ]
 
 QKNR_BF16 = 0x000
@@ -35,7 +35,7 @@ QKNR_INPUTS_READY = 0x200   # caller's promise: weights and positions are not wr
 STATUS_NAMES = {
     0: "QKNR_OK", 1: "QKNR_ERR_NOT_INITIALIZED", 2: "QKNR_ERR_INVALID_ARG",
     3: "QKNR_ERR_UNSUPPORTED", 4: "QKNR_ERR_MISALIGNED", 5: "QKNR_ERR_CUDA",
-    6: "QKNR_ERR_POSITION_OOB", 7: "QKNR_ERR_WATCHDOG",
+    6: "QKNR_ERR_POSITION_OOB",
 }
 
 QKNR_KERNEL_AUTO, QKNR_KERNEL_REGISTER, QKNR_KERNEL_RING = 0, 1, 2
@@ -44,9 +44,10 @@ QKNR_HOST_AUTO, QKNR_HOST_STAGED, QKNR_HOST_DIRECT = 0, 1, 2
 HOST_MODES = {"auto": QKNR_HOST_AUTO, "staged": QKNR_HOST_STAGED, "direct": QKNR_HOST_DIRECT}
 # QKNR_TUNE_* keys (include/qknr.h)
 TUNE_KEYS = {"reset": 0, "kernel": 1, "passes": 2, "threads": 3, "ctas_per_sm": 4, "pdl": 5,
-             "order": 9, "prefetch": 10}
+             "ring_order": 6, "order": 9, "prefetch": 10}
 WORK_MAP_FIELDS = ["kernel", "grid", "threads", "items", "items_per_token", "ctas_per_sm", "pdl",
-                   "passes_per_token", "unroll", "order", "prefetch_items", "rope_dim_compiled"]
+                   "passes_per_token", "unroll", "order", "prefetch_items", "rope_dim_compiled",
+                   "ring_order"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -88,16 +89,14 @@ def _load() -> ctypes.CDLL:
                                        i64, i64, i64, i64, f32, i32, vp]
     lib.qknr_tune.argtypes = [i64, i32, i32, i32, i32, i32, i64, i64, i64, i32, vp,
                               ctypes.POINTER(ctypes.c_int64)]
-    lib.qknr_sync.argtypes = [vp]
-    lib.qknr_selftest_watchdog.argtypes = [vp]
     lib.qknr_set_tuning.argtypes = [i32, i32]
     lib.qknr_get_tuning.argtypes = [i32, ctypes.POINTER(ctypes.c_int)]
     lib.qknr_query_work_map.argtypes = [i64, i32, i32, i32, i32, i32, i32,
                                         ctypes.POINTER(ctypes.c_int64)]
     for name in ("qknr_init", "qknr_shutdown", "qknr_version", "qknr_can_use", "qknr_apply",
                  "qknr_apply_checked", "qknr_apply_checked_noalloc", "qknr_apply_unfused",
-                 "qknr_apply_host", "qknr_apply_strided", "qknr_tune", "qknr_sync", "qknr_selftest_watchdog",
-                 "qknr_set_tuning", "qknr_get_tuning", "qknr_query_work_map"):
+                 "qknr_apply_host", "qknr_apply_strided", "qknr_tune", "qknr_set_tuning", "qknr_get_tuning",
+                 "qknr_query_work_map"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -200,14 +199,6 @@ def qknr_tune(num_tokens, n_qo, n_kv, head_dim, rope_dim, is_neox, q_stride, k_s
               dtype, stream, out) -> int:
     return _get_lib().qknr_tune(num_tokens, n_qo, n_kv, head_dim, rope_dim, int(is_neox), q_stride,
                                 k_stride, head_stride, dtype, stream, out)
-
-
-def qknr_sync(stream) -> int:
-    return _get_lib().qknr_sync(stream)
-
-
-def qknr_selftest_watchdog(stream) -> int:
-    return _get_lib().qknr_selftest_watchdog(stream)
 
 
 def qknr_set_tuning(key: int, value: int) -> int:
@@ -457,20 +448,6 @@ def set_tuning(**kw) -> None:
         if name == "kernel" and isinstance(value, str):
             value = {"auto": QKNR_KERNEL_AUTO, "register": QKNR_KERNEL_REGISTER, "ring": QKNR_KERNEL_RING}[value]
         _check(qknr_set_tuning(TUNE_KEYS[name], int(value)))
-
-
-def sync(stream=None, device=None) -> None:
-    """qknr_sync: wait for ``stream`` (default: torch's current stream) and
-    raise QknrError(QKNR_ERR_WATCHDOG) if a kernel wait ran out since the
-    last report."""
-    import torch
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    if stream is None:
-        stream = torch.cuda.current_stream(dev).cuda_stream
-    elif not isinstance(stream, int):
-        stream = stream.cuda_stream
-    with torch.cuda.device(dev):
-        _check(qknr_sync(stream))
 
 
 def get_tuning(name: str) -> int:

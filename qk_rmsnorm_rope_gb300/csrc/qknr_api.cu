@@ -8,8 +8,8 @@
 // Two kernels compute the op, with the same bits: the register kernel
 // qknr_fused_kernel (qknr_kernel.cuh), which loads straight into registers,
 // and the ring kernel qknr_ring_kernel (qknr_ring_kernel.cuh), which
-// double-buffers each warp's items in shared memory with bulk copies. The
-// work map picks one per call by a measured rule (plan_register).
+// double-buffers each warp's items in shared memory with asynchronous
+// copies. The work map picks one per call by a measured rule (plan_register).
 //
 // Entry points beyond the op itself: the position-checked variants (one with
 // no allocation), the unfused two-kernel baseline, the host-buffer variant
@@ -43,7 +43,7 @@ using qknr::Params;
 
 constexpr int kMaxDevices = 64;
 constexpr int kVersion = 10400;             // 1.4.0: the ring kernel
-constexpr int kStatusWords = 3;             // {bad-token count, first bad token, watchdog}
+constexpr int kStatusWords = 2;             // {bad-token count, first bad token}
 constexpr int kMaxHeads = 1 << 24;                // largest n_qo + n_kv accepted
 constexpr long long kMaxExtentBytes = 1LL << 56;  // largest q or k extent accepted (far above any GPU's memory)
 
@@ -64,11 +64,16 @@ int fail_cuda(cudaError_t e, const char *what) {
 }
 
 // ------------------------------------------------------------------ tuning
-constexpr int kNumTuneKeys = 11;  // keys 1..5, 9 and 10 (QKNR_TUNE_*); the other slots are unused
+constexpr int kNumTuneKeys = 11;  // keys 1..6, 9 and 10 (QKNR_TUNE_*); the other slots are unused
 // the value that means "automatic" for each key
 constexpr int kTuneAuto[kNumTuneKeys] = {0, 0, 0, 0, 0, -1, 0, 0, 0, 0, 0};
 std::atomic<int> g_tune[kNumTuneKeys] = {{0}, {0}, {0}, {0}, {0}, {-1}, {0}, {0}, {0}, {0}, {0}};
-constexpr int kAutoPrefetchItems = 4;  // items per warp prefetched into L2 before the wait (automatic)
+// items per warp prefetched into L2 before the wait (automatic): the register
+// kernel's first loads all wait on DRAM, the ring kernel's first copy goes out
+// right after the wait and competes with more prefetches (measured: 1 item
+// +0.8% on dit and mha_neox and +2.2% on gqa against 4)
+constexpr int kAutoPrefetchItems = 4;
+constexpr int kAutoPrefetchRing = 1;
 constexpr int kMaxPrefetchItems = 4;
 std::once_flag g_env_once;
 
@@ -78,6 +83,10 @@ int tune_check(int key, int value) {
             return (value >= 0 && value <= QKNR_KERNEL_RING)
                        ? QKNR_OK
                        : fail(QKNR_ERR_INVALID_ARG, "kernel must be 0 (auto), 1 (register) or 2 (ring)");
+        case QKNR_TUNE_RING_ORDER:
+            return (value >= 0 && value <= 2)
+                       ? QKNR_OK
+                       : fail(QKNR_ERR_INVALID_ARG, "ring order must be 0 (auto), 1 (next after the wait) or 2 (two ahead)");
         case QKNR_TUNE_PASSES:
             return (value >= 0 && value <= qknr::kUnrollClass[qknr::kNumUnroll - 1])
                        ? QKNR_OK
@@ -107,14 +116,15 @@ int tune_check(int key, int value) {
     }
 }
 
-// QKNR_TUNE="kernel=2,passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1"
+// QKNR_TUNE="kernel=2,ring_order=1,passes=4,threads=256,ctas=2,pdl=1,order=2,prefetch=1"
 void read_env_tuning() {
     const char *s = std::getenv("QKNR_TUNE");
     if (!s) return;
     static const struct {
         const char *name;
         int key;
-    } names[] = {{"kernel", QKNR_TUNE_KERNEL}, {"passes", QKNR_TUNE_PASSES}, {"threads", QKNR_TUNE_THREADS},
+    } names[] = {{"kernel", QKNR_TUNE_KERNEL}, {"ring_order", QKNR_TUNE_RING_ORDER},
+                 {"passes", QKNR_TUNE_PASSES}, {"threads", QKNR_TUNE_THREADS},
                  {"ctas", QKNR_TUNE_CTAS_PER_SM}, {"pdl", QKNR_TUNE_PDL},
                  {"order", QKNR_TUNE_ORDER},      {"prefetch", QKNR_TUNE_PREFETCH}};
     std::string spec(s);
@@ -161,10 +171,12 @@ struct ShapeHash {
         return h;
     }
 };
-// The knobs qknr_tune chooses: the kernel, warp passes per item and items per
-// warp prefetched into L2 before the wait (0: none).
+// The knobs qknr_tune chooses: the kernel (and the ring kernel's issue order,
+// 1 or 2 as QKNR_TUNE_RING_ORDER), warp passes per item and items per warp
+// prefetched into L2 before the wait (0: none).
 struct TunedMap {
     int kernel = QKNR_KERNEL_REGISTER;
+    int ring_order = 0;
     int passes = 0;
     int prefetch = 0;
 };
@@ -172,7 +184,7 @@ struct TunedMap {
 struct DeviceState {
     std::atomic<bool> ready{false};
     int sm_count = 0;
-    unsigned long long *status = nullptr;       // device: kStatusWords words (position check, watchdog)
+    unsigned long long *status = nullptr;       // device: kStatusWords words
     unsigned long long *status_host = nullptr;  // pinned host copy (qknr_init) or nullptr
     std::mutex checked_mu;                      // serialises status read-backs on this device
     // resident CTAs per SM for the register kernel, by (early, dtype, pos64, d_idx, mode, u_idx,
@@ -257,6 +269,7 @@ struct WorkMap {
     int interleave = 0;   // item order
     int prefetch_items = 0;  // items per warp prefetched into L2 before the wait
     int smem = 0;            // dynamic shared memory per CTA (ring kernel)
+    int ring_ahead = 0;      // ring kernel's issue order (Params::ring_ahead)
     const void *kernel = nullptr;
 };
 
@@ -333,18 +346,20 @@ bool tuned_for(DeviceState &st, const Call &c, TunedMap *out) {
     return true;
 }
 
-// The ring kernel's measured territory (GB300, same-box A/B against the
-// register kernel): NeoX pairing at every size tried (+2 to +10%), and
-// interleaved calls that move at most this many bytes of q and k (+2.5% on
-// a 4608-token DiT call); larger interleaved calls sustain more bandwidth
-// with the register kernel.
-constexpr long long kRingInterleavedMaxBytes = 256LL << 20;
+// The measured rule (GB300, same-box sweeps of both kernels and both ring
+// orders over call sizes): the ring kernel for every call whose items have
+// three or four passes (+4% to +13% over the register kernel at the
+// benchmark's sizes), the register kernel for decode-sized calls; the ring's
+// order 1 (two items ahead) for interleaved calls of more than this many
+// bytes of q and k, order 0 (next item after the wait) below it and for NeoX
+// pairing.
+constexpr long long kRingAheadMinBytes = 256LL << 20;
 
-bool ring_by_rule(const Call &c, const WorkMap &wm) {
-    if (wm.u_idx != 1) return false;   // decode-sized calls (items of one or two passes)
-    if (c.is_neox) return true;
+bool ring_by_rule(const WorkMap &wm) { return wm.u_idx == 1; }
+
+int ring_ahead_by_rule(const Call &c) {
     const long long qk_bytes = 4LL * (c.n_qo + c.n_kv) * c.head_dim * c.num_tokens;
-    return qk_bytes <= kRingInterleavedMaxBytes;
+    return (!c.is_neox && qk_bytes > kRingAheadMinBytes) ? 1 : 0;
 }
 
 // Items are (token, chunk of warp passes); the default is the largest unroll
@@ -388,8 +403,11 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *f
                     : (2 * c.rope_dim == c.head_dim ? qknr::kRopeHalf : qknr::kRopeRuntime);
     int kind = force ? force->kernel : tune(QKNR_TUNE_KERNEL);
     if (kind == QKNR_KERNEL_AUTO && tuned) kind = tm.kernel;
-    if (kind == QKNR_KERNEL_AUTO) kind = ring_by_rule(c, *wm) ? QKNR_KERNEL_RING : QKNR_KERNEL_REGISTER;
+    if (kind == QKNR_KERNEL_AUTO) kind = ring_by_rule(*wm) ? QKNR_KERNEL_RING : QKNR_KERNEL_REGISTER;
     wm->kind = kind;
+    int order = force ? force->ring_order : tune(QKNR_TUNE_RING_ORDER);
+    if (order == 0 && tuned) order = tm.ring_order;
+    wm->ring_ahead = kind != QKNR_KERNEL_RING ? 0 : (order == 0 ? ring_ahead_by_rule(c) : order - 1);
     int occ = 0;
     int rc = QKNR_OK;
     if (kind == QKNR_KERNEL_RING) {
@@ -420,7 +438,8 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *f
     wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
     wm->interleave = tune(QKNR_TUNE_ORDER) == 1 ? 0 : 1;   // interleaved unless asked otherwise
     const int pf = force ? (force->prefetch > 0 ? force->prefetch : -1) : tune(QKNR_TUNE_PREFETCH);
-    wm->prefetch_items = pf < 0 ? 0 : (pf > 0 ? pf : (tuned ? tm.prefetch : kAutoPrefetchItems));
+    const int auto_pf = kind == QKNR_KERNEL_RING ? kAutoPrefetchRing : kAutoPrefetchItems;
+    wm->prefetch_items = pf < 0 ? 0 : (pf > 0 ? pf : (tuned ? tm.prefetch : auto_pf));
     return QKNR_OK;
 }
 
@@ -608,6 +627,7 @@ int launch(const WorkMap &wm, const Call &c, unsigned long long *status, cudaStr
                                                     wm.chunks_per_token);
     prm.eps = c.eps;
     prm.inv_d = 1.0f / static_cast<float>(c.head_dim);
+    prm.ring_ahead = wm.ring_ahead;
     cfg.dynamicSmemBytes = static_cast<size_t>(wm.smem);
     void *args[] = {&prm};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, wm.kernel, args);
@@ -627,33 +647,12 @@ int run_checked(DeviceState &st, const WorkMap &wm, const Call &c, cudaStream_t 
                         cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail_cuda(e, "status read-back");
-    if (host_words[qknr::kStatusWatchdog]) {
-        e = cudaMemsetAsync(st.status + qknr::kStatusWatchdog, 0, sizeof(unsigned long long), s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-        if (e != cudaSuccess) return fail_cuda(e, "watchdog reset");
-        return fail(QKNR_ERR_WATCHDOG,
-                    "a bounded wait in a kernel on this device ran out (this call or an earlier "
-                    "unchecked one); that call's output is incomplete");
-    }
     if (host_words[0]) {
         return fail(QKNR_ERR_POSITION_OOB,
                     "%llu token(s) have positions outside [0, %lld); first bad token index %llu (left untouched)",
                     host_words[0], c.cache_len, host_words[1]);
     }
     return QKNR_OK;
-}
-
-// The watchdog's run-out path, on purpose: one warp waits, with the ring
-// kernel's bounded wait, on an mbarrier that nothing arrives on. After the
-// limit the wait gives up and the watchdog word is set, as a stalled
-// ring-kernel wait would set it; nothing faults and the context stays usable.
-__global__ void qknr_watchdog_selftest_kernel(unsigned long long *status) {
-    __shared__ __align__(8) unsigned long long bar;
-    if (threadIdx.x == 0) {
-        qknr::mbar_init(qknr::smem_u32(&bar), 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (!qknr::mbar_wait(qknr::smem_u32(&bar), 0u)) atomicOr(status + qknr::kStatusWatchdog, 1ull);
-    }
 }
 
 int apply_impl(const Call &c, void *stream, bool checked) {
@@ -739,7 +738,7 @@ int apply_checked_noalloc_impl(const Call &c, void *stream) {
     rc = plan(slot.state, c, &wm);
     if (rc) return rc;
     std::lock_guard<std::mutex> lock(slot.state.checked_mu);
-    unsigned long long host_words[kStatusWords] = {0ull, 0ull, 0ull};
+    unsigned long long host_words[kStatusWords] = {0ull, 0ull};
     return run_checked(slot.state, wm, c, static_cast<cudaStream_t>(stream), host_words);
 }
 
@@ -1112,11 +1111,12 @@ int tune_impl(const Call &shape, void *stream, TunedMap *best_out, double *best_
     for (int passes : {4, 3, 2, 1}) {
         const int chunks = (ppt + passes - 1) / passes;
         if (!seen_chunks.insert(chunks).second) continue;
-        if (passes < 4 && cands.size() >= 12) break;
-        for (int kernel : {QKNR_KERNEL_REGISTER, QKNR_KERNEL_RING})
+        if (passes < 4 && cands.size() >= 24) break;
+        for (int variant : {0, 1, 2})    // register; ring, next after the wait; ring, two ahead
             for (int pf : {4, 2, 1, 0}) {
                 TunedMap m;
-                m.kernel = kernel;
+                m.kernel = variant == 0 ? QKNR_KERNEL_REGISTER : QKNR_KERNEL_RING;
+                m.ring_order = variant;
                 m.passes = passes;
                 m.prefetch = pf;
                 cands.push_back(m);
@@ -1349,33 +1349,6 @@ int qknr_apply_strided(void *q, void *k, const void *q_w, const void *k_w, const
     return apply_strided_impl(c, stream);
 }
 
-int qknr_sync(void *stream) {
-    DeviceState *st = current_state();
-    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(st->checked_mu);
-    unsigned long long *word = st->status_host + qknr::kStatusWatchdog;
-    cudaError_t e = cudaMemcpyAsync(word, st->status + qknr::kStatusWatchdog, sizeof(unsigned long long),
-                                    cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return fail_cuda(e, "watchdog read-back");
-    if (*word == 0) return QKNR_OK;
-    e = cudaMemsetAsync(st->status + qknr::kStatusWatchdog, 0, sizeof(unsigned long long), s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return fail_cuda(e, "watchdog reset");
-    return fail(QKNR_ERR_WATCHDOG, "a bounded wait in a kernel on this device ran out; the output of the call "
-                                   "it belonged to is incomplete");
-}
-
-int qknr_selftest_watchdog(void *stream) {
-    DeviceState *st = current_state();
-    if (!st) return fail(QKNR_ERR_NOT_INITIALIZED, "qknr_init was not called for the current device");
-    qknr_watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st->status);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail_cuda(e, "watchdog self-test launch");
-    return QKNR_OK;
-}
-
 int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim, int is_neox, int64_t q_stride,
               int64_t k_stride, int64_t head_stride, int dtype, void *stream, int64_t *out) {
     const Call c = make_call(nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, num_tokens, n_qo, n_kv, head_dim,
@@ -1402,7 +1375,8 @@ int qknr_tune(int64_t num_tokens, int n_qo, int n_kv, int head_dim, int rope_dim
     out[9] = wm.interleave ? 2 : 1;
     out[10] = wm.prefetch_items;
     out[11] = wm.r_idx == qknr::kRopeFull ? c.head_dim : (wm.r_idx == qknr::kRopeHalf ? c.head_dim / 2 : 0);
-    out[12] = static_cast<int64_t>(ms * 1e6);   // measured nanoseconds per launch
+    out[12] = wm.kind == QKNR_KERNEL_RING ? wm.ring_ahead + 1 : 0;
+    out[13] = static_cast<int64_t>(ms * 1e6);   // measured nanoseconds per launch
     return QKNR_OK;
 }
 
@@ -1420,7 +1394,8 @@ int qknr_set_tuning(int key, int value) {
 
 int qknr_get_tuning(int key, int *value) {
     if (!value) return fail(QKNR_ERR_INVALID_ARG, "value is null");
-    if (key != QKNR_TUNE_KERNEL && key != QKNR_TUNE_PASSES && key != QKNR_TUNE_THREADS && key != QKNR_TUNE_CTAS_PER_SM &&
+    if (key != QKNR_TUNE_KERNEL && key != QKNR_TUNE_RING_ORDER && key != QKNR_TUNE_PASSES &&
+        key != QKNR_TUNE_THREADS && key != QKNR_TUNE_CTAS_PER_SM &&
         key != QKNR_TUNE_PDL && key != QKNR_TUNE_ORDER && key != QKNR_TUNE_PREFETCH)
         return fail(QKNR_ERR_INVALID_ARG, "unknown tuning key %d", key);
     *value = tune(key);
@@ -1458,6 +1433,7 @@ int qknr_query_work_map(int64_t num_tokens, int n_qo, int n_kv, int head_dim, in
     out[9] = wm.interleave ? 2 : 1;
     out[10] = wm.prefetch_items;
     out[11] = wm.r_idx == qknr::kRopeFull ? head_dim : (wm.r_idx == qknr::kRopeHalf ? head_dim / 2 : 0);
+    out[12] = wm.kind == QKNR_KERNEL_RING ? wm.ring_ahead + 1 : 0;
     return QKNR_OK;
 }
 

@@ -66,6 +66,7 @@ struct Params {
     float inv_d;                  // 1 / head_dim in fp32 (exact for 64, 128 and 256; for 80, 96 and 192
                                   // the rounded reciprocal moves the mean by at most about one ulp)
     short pass_bound[kBoundTable + 1];  // first pass of chunk c, c <= chunks_per_token <= kBoundTable
+    int ring_ahead;               // ring kernel's issue order: 0 next item after the wait, 1 two ahead
 };
 
 template <class P>

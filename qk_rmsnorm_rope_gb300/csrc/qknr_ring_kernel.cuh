@@ -1,32 +1,25 @@
 // qknr_ring_kernel.cuh -- the fused op with each warp's items double-buffered
-// in shared memory by bulk asynchronous copies (TMA), for sm_103a.
+// in shared memory by asynchronous copies, for sm_103a.
 //
-// Same op, lane mapping and arithmetic (qknr_head) as the register kernel in
-// qknr_kernel.cuh, so both give the same bits; only the way q and k reach the
-// lanes differs. The register kernel holds an item's loads in registers, so a
-// warp has nothing in flight while it computes. Here each warp owns two 4 KB
-// stages of shared memory and one mbarrier per stage:
-//  * one lane issues the item's q/k bytes as one or two cp.async.bulk copies
-//    (one per side when the item spans the q/k boundary; one per head when
-//    heads are not contiguous) into a stage, with the byte count armed on the
-//    stage's mbarrier;
-//  * the warp waits for the item's bytes, then at once issues its next item
-//    into the other stage, so that item's copy is in flight while this one is
-//    computed: per pass each lane reads its two 16-byte vectors from shared
-//    memory, runs qknr_head and stores the result straight to global memory;
-//  * the first item alone is issued before the loop, so a launch requests no
-//    more at its start than the register kernel does.
-// There is no synchronisation between warps: stages, barriers and items are
-// private to a warp, and items are dealt to warps as in the register kernel.
-// Measured on GB300 it is faster than the register kernel on NeoX pairing at
-// every size tried and on interleaved calls of up to a few hundred MB; on
-// larger interleaved calls the register kernel sustains more bandwidth.
+// Same op, items, lane mapping and arithmetic (qknr_head) as the register
+// kernel in qknr_kernel.cuh, so both give the same bits; only the way q and k
+// reach the lanes differs. The register kernel holds an item's loads in
+// registers, so a warp has nothing in flight while it computes. Here each
+// warp owns two 4 KB stages of shared memory, and every lane copies its own
+// 16-byte vectors of an item into its own slots of a stage with cp.async
+// (global -> shared, no registers). A lane later reads back only what it
+// copied itself, so completion is the lane's own cp.async group: no mbarrier,
+// no spin-wait and no synchronisation between lanes or warps.
 //
-// Every mbarrier wait is bounded (kRingWaitNs of %globaltimer). A wait that
-// runs out sets the watchdog word of the status block, waits (bounded again)
-// for the copy it was waiting on, and the warp returns, leaving its remaining
-// items untouched; the host reports it (QKNR_ERR_WATCHDOG) from the checked
-// entry points and qknr_sync.
+// Two issue orders (Params::ring_ahead), both measured on GB300:
+//  0  the next item is issued right after this item's bytes have landed, so
+//     it is in flight while this one is computed; a launch asks for no more
+//     at its start than the register kernel does. Best on calls of up to a
+//     few hundred MB and on NeoX pairing.
+//  1  after the first item, the item two ahead is issued once this item's
+//     stores are out, so two items can be in flight. More bytes in flight
+//     sustain more bandwidth on large interleaved calls (fused_qkv: 99.8% of
+//     the measured copy peak); the start is slower.
 #pragma once
 
 #include <cstdint>
@@ -36,64 +29,29 @@
 namespace qknr {
 
 constexpr int kRingStages = 2;                // per warp
-constexpr int kRingStageBytes = 4096;         // up to 4 warp passes of at most 1 KB
+constexpr int kRingStageBytes = 4096;         // up to 4 warp passes of 1 KB
 constexpr int kRingMaxPasses = 4;             // warp passes per item
-constexpr int kRingWarpBytes = kRingStages * (kRingStageBytes + 8);  // stages + mbarriers
-constexpr unsigned long long kRingWaitNs = 1000000000ull;            // 1 s per wait
-constexpr int kStatusWatchdog = 2;            // status word set when a wait ran out
 
 // Dynamic shared memory of a CTA of `threads` threads.
-__host__ __device__ constexpr int ring_smem_bytes(int threads) { return (threads / kWarp) * kRingWarpBytes; }
+__host__ __device__ constexpr int ring_smem_bytes(int threads) {
+    return (threads / kWarp) * kRingStages * kRingStageBytes;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+// 16-byte global -> shared copy that bypasses L1 (both addresses 16-byte aligned)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// Arrive once on `bar` and add `bytes` to the bytes its phase waits for.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
-// Global -> shared bulk copy; its bytes complete on `bar`. dst, src and bytes
-// are multiples of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n}\n"
-                 : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// The slow path of mbar_wait: poll until the phase completes or kRingWaitNs
-// have passed (false).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kRingWaitNs) return false;
-    }
-}
-
-// Wait for the phase of `bar` with parity `parity`; false if it did not
-// complete within kRingWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
+// Wait until at most N of this thread's committed groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -110,8 +68,7 @@ template <class T, class P, int D, int MODE, bool EARLY = false, int RC = 0>
 __global__ void __launch_bounds__(512) qknr_ring_kernel(const __grid_constant__ Params p) {
     constexpr int LPH = HeadGeom<D>::LPH;
     constexpr int HPW = HeadGeom<D>::HPW;   // heads per warp pass
-    constexpr int HB = D * static_cast<int>(sizeof(T));   // bytes of one head
-    static_assert(kRingMaxPasses * HPW * HB <= kRingStageBytes, "an item must fit its stage");
+    static_assert(2 * kRingMaxPasses * kWarp * 16 <= kRingStageBytes, "an item's slots must fit a stage");
 
     const int lane = threadIdx.x & (kWarp - 1);
     const int g = lane / LPH;
@@ -122,18 +79,11 @@ __global__ void __launch_bounds__(512) qknr_ring_kernel(const __grid_constant__ 
     const int va = lm.va, vb = lm.vb;
     const bool active = lm.active;
 
-    // this warp's stages and their mbarriers (one arrival: the issuing lane's)
+    // This lane's slots: vector j of pass u of an item sits at
+    // ((2u + j) * 32 + lane) * 16 within the stage, so a warp's 16-byte
+    // accesses to one slot row cover 512 consecutive bytes (no bank conflict).
     extern __shared__ __align__(128) unsigned char ring_smem[];
-    const int wib = threadIdx.x >> 5;
-    const uint32_t data_s = smem_u32(ring_smem) + wib * (kRingStages * kRingStageBytes);
-    const uint32_t bar_s =
-        smem_u32(ring_smem) + (blockDim.x >> 5) * (kRingStages * kRingStageBytes) + wib * (kRingStages * 8);
-    if (lane == 0) {
-#pragma unroll
-        for (int s_ = 0; s_ < kRingStages; ++s_) mbar_init(bar_s + 8 * s_, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
+    const uint32_t slots = smem_u32(ring_smem) + (threadIdx.x >> 5) * (kRingStages * kRingStageBytes) + lane * 16;
 
     const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long warp_id = gtid / kWarp;
@@ -174,37 +124,26 @@ __global__ void __launch_bounds__(512) qknr_ring_kernel(const __grid_constant__ 
     int ch = static_cast<int>(it_begin - t * chunks);
     const long long step_t = it_step / chunks;
     const int step_c = static_cast<int>(it_step - step_t * chunks);
-    const bool contig = p.head_stride_b == HB;
 
-    // Issue cursor: the next item to copy in, advanced by every lane alike;
-    // lane 0 issues the copies.
+    // Issue cursor: the next item to copy in.
     long long ti = t, it_i = it_begin;
     int chi = ch;
     auto issue = [&](int stage_) {
-        if (lane == 0) {
-            int b0, b1;
-            item_passes<MODE>(p, chunks, chi, b0, b1);
-            const int h0 = b0 * HPW;
-            const int h1 = min(b1 * HPW, H);
-            const uint32_t dst = data_s + stage_ * kRingStageBytes;
-            const uint32_t bar = bar_s + 8 * stage_;
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>((h1 - h0) * HB));
-            const char *q_row = p.q + ti * p.q_stride_b;
-            const char *k_row = p.k + ti * p.k_stride_b - static_cast<long long>(p.n_qo) * p.head_stride_b;
-            if (contig) {
-                if (h0 < p.n_qo) {
-                    const int he = min(h1, p.n_qo);
-                    bulk_load(dst, q_row + static_cast<long long>(h0) * HB, (he - h0) * HB, bar);
-                }
-                if (h1 > p.n_qo) {
-                    const int hk = max(h0, p.n_qo);
-                    bulk_load(dst + (hk - h0) * HB, k_row + static_cast<long long>(hk) * HB, (h1 - hk) * HB, bar);
-                }
-            } else {
-                for (int h = h0; h < h1; ++h)
-                    bulk_load(dst + (h - h0) * HB, (h < p.n_qo ? q_row : k_row) + h * p.head_stride_b, HB, bar);
+        int b0, b1;
+        item_passes<MODE>(p, chunks, chi, b0, b1);
+        const uint32_t dst = slots + stage_ * kRingStageBytes;
+        const char *q_row = p.q + ti * p.q_stride_b;
+        const char *k_row = p.k + ti * p.k_stride_b - static_cast<long long>(p.n_qo) * p.head_stride_b;
+#pragma unroll
+        for (int u = 0; u < kRingMaxPasses; ++u) {
+            const int h = (b0 + u) * HPW + g;
+            if (b0 + u < b1 && h < H && active) {
+                const char *base = (h < p.n_qo ? q_row : k_row) + static_cast<long long>(h) * p.head_stride_b;
+                cp_async16(dst + (2 * u) * (kWarp * 16), base + 16 * va);
+                cp_async16(dst + (2 * u + 1) * (kWarp * 16), base + 16 * vb);
             }
         }
+        cp_async_commit();
         it_i += it_step;
         ti += step_t;
         chi += step_c;
@@ -212,8 +151,9 @@ __global__ void __launch_bounds__(512) qknr_ring_kernel(const __grid_constant__ 
     };
     if (it_i < it_end) issue(0);
 
+    const bool ahead2 = p.ring_ahead != 0;
+    bool next_pending = false;   // the item after this one was already issued (order 1)
     int stage = 0;
-    uint32_t parity = 0;
     for (long long it = it_begin; it < it_end; it += it_step, ++jb) {
         if (jb == kWarp) {   // next batch of 32 items' positions
             jb = 0;
@@ -234,25 +174,16 @@ __global__ void __launch_bounds__(512) qknr_ring_kernel(const __grid_constant__ 
             check_position(p, pos, t, ch, lane, tok_ok);
             token_cos_sin<MODE>(p, pos, tok_ok && lm.rot_lane, va, vb, lm.split, R, half, c, s);
         }
+        if (next_pending) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        // order 0: the next item into the other stage (it held the previous
+        // item, whose slots this lane has read); order 1 does this once
+        if ((!ahead2 || it == it_begin) && it_i < it_end) issue(stage ^ 1);
 
-        const uint32_t sbase = data_s + stage * kRingStageBytes;
-        if (!mbar_wait(bar_s + 8 * stage, parity)) {
-            // the only copy this warp has in flight is this item's (the next
-            // one is issued after this wait): give it one more bounded wait
-            if (lane == 0) atomicOr(p.status + kStatusWatchdog, 1ull);
-            mbar_wait(bar_s + 8 * stage, parity);
-            return;
-        }
-        // the other stage held the previous item, whose reads ended at the
-        // last __syncwarp: order them before the async proxy writes it again
-        if (it_i < it_end) {
-            if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(stage ^ 1);
-        }
         if (tok_ok) {
+            const uint32_t sbase = slots + stage * kRingStageBytes;
             char *const q_row = p.q + t * p.q_stride_b;
             char *const k_row = p.k + t * p.k_stride_b - static_cast<long long>(p.n_qo) * p.head_stride_b;
-            const int h0 = pb * HPW;
 #pragma unroll
             for (int u = 0; u < kRingMaxPasses; ++u) {
                 if (pb + u >= pe) break;    // warp-uniform
@@ -260,9 +191,8 @@ __global__ void __launch_bounds__(512) qknr_ring_kernel(const __grid_constant__ 
                 const bool ok = (h < H) && active;
                 uint4 xa = zero4, xb = zero4;
                 if (ok) {
-                    const uint32_t a = sbase + (h - h0) * HB;
-                    xa = lds128(a + 16 * va);
-                    xb = lds128(a + 16 * vb);
+                    xa = lds128(sbase + (2 * u) * (kWarp * 16));
+                    xb = lds128(sbase + (2 * u + 1) * (kWarp * 16));
                 }
                 const bool is_q = h < p.n_qo;
                 qknr_head<T, MODE, LPH, kOpFused>(xa, xb, is_q ? wqa : wka, is_q ? wqb : wkb, c, s, lm.split,
@@ -274,10 +204,15 @@ __global__ void __launch_bounds__(512) qknr_ring_kernel(const __grid_constant__ 
                 }
             }
         }
-        __syncwarp();
+        // order 1: the item two ahead into this stage, once its slots are read
+        next_pending = false;
+        if (ahead2 && it_i < it_end) {
+            issue(stage);
+            next_pending = true;
+        }
         stage ^= 1;
-        parity ^= static_cast<uint32_t>(stage == 0);
     }
+    cp_async_wait<0>();
 }
 
 }  // namespace qknr

@@ -106,13 +106,15 @@ def test_set_tuning_validation():
     K = qknr.TUNE_KEYS
     bad = [(K["passes"], 5), (K["threads"], 96), (K["ctas_per_sm"], -1), (K["ctas_per_sm"], 33),
            (K["pdl"], 2), (K["order"], 3), (K["prefetch"], -2), (K["prefetch"], 5), (K["kernel"], 3),
-           (K["kernel"], -1), (6, 4), (7, 8), (8, 4096), (99, 0)]
+           (K["kernel"], -1), (K["ring_order"], 3), (K["ring_order"], -1), (7, 8), (8, 4096), (99, 0)]
     for key, value in bad:
         assert qknr.qknr_set_tuning(key, value) == 2, (key, value)
     assert "tuning key" in qknr.qknr_last_error()
     v = ctypes.c_int(0)
     assert qknr.qknr_get_tuning(7, ctypes.byref(v)) == 2      # keys of retired kernels are unknown
-    qknr.set_tuning(passes=2, threads=128, ctas_per_sm=3, pdl=0, order=1, prefetch=-1, kernel="ring")
+    qknr.set_tuning(passes=2, threads=128, ctas_per_sm=3, pdl=0, order=1, prefetch=-1, kernel="ring",
+                    ring_order=2)
+    assert qknr.get_tuning("ring_order") == 2
     assert qknr.get_tuning("passes") == 2 and qknr.get_tuning("threads") == 128
     assert qknr.get_tuning("pdl") == 0 and qknr.get_tuning("order") == 1
     assert qknr.get_tuning("prefetch") == -1 and qknr.get_tuning("kernel") == qknr.QKNR_KERNEL_RING
@@ -121,7 +123,7 @@ def test_set_tuning_validation():
     qknr.set_tuning(reset=True)
     assert qknr.get_tuning("passes") == 0 and qknr.get_tuning("pdl") == -1
     assert qknr.get_tuning("order") == 0 and qknr.get_tuning("prefetch") == 0
-    assert qknr.get_tuning("kernel") == qknr.QKNR_KERNEL_AUTO
+    assert qknr.get_tuning("kernel") == qknr.QKNR_KERNEL_AUTO and qknr.get_tuning("ring_order") == 0
 
 
 def test_apply_rejects_cpu_tensors():

@@ -145,16 +145,16 @@ def test_workload_full_size_every_element(qknr, name):
 
 @pytest.mark.parametrize("name", ["dit", "mha_neox", "gqa", "fused_qkv"])
 def test_kernels_agree_at_full_size(qknr, name):
-    """Full size: the register kernel and the ring kernel, each forced, give the
-    same bits on copies of one input (the default launch of each workload is
-    compared with the oracle element by element above, so both kernels are
-    pinned to it at the sizes the benchmark runs)."""
+    """Full size: the register kernel and the ring kernel in both issue orders,
+    each forced, give the same bits on copies of one input (the default launch
+    of each workload is compared with the oracle element by element above, so
+    every kernel is pinned to it at the sizes the benchmark runs)."""
     w = workloads.get(name)
     cpu = workloads.make_inputs(w)
     outs = []
-    for kernel in ("register", "ring"):
+    for kernel, ring_order in (("register", 0), ("ring", 1), ("ring", 2)):
         dev = workloads.to_device(cpu, w, "cuda")
-        qknr.set_tuning(reset=True, kernel=kernel)
+        qknr.set_tuning(reset=True, kernel=kernel, ring_order=ring_order)
         try:
             _run_gpu(qknr, dev, w)
         finally:
@@ -163,36 +163,9 @@ def test_kernels_agree_at_full_size(qknr, name):
         outs.append([dev[key].view(torch.int16)] if key else [dev["q"].view(torch.int16),
                                                               dev["k"].view(torch.int16)])
         del dev
-    for a, b in zip(*outs):
-        assert torch.equal(a, b), name
-
-
-def test_watchdog_selftest_reports_once(qknr):
-    """The ring kernel's bounded wait, run out on purpose (a barrier nothing
-    arrives on): qknr_sync reports QKNR_ERR_WATCHDOG once and clears it, the
-    context stays usable, and a checked call reports a run-out that happened
-    before it."""
-    stream = torch.cuda.current_stream().cuda_stream
-    assert qknr.qknr_sync(stream) == 0
-    assert qknr.qknr_selftest_watchdog(stream) == 0
-    assert qknr.qknr_sync(stream) == 7, qknr.qknr_last_error()
-    assert "ran out" in qknr.qknr_last_error()
-    assert qknr.qknr_sync(stream) == 0
-    # the context is still usable: a normal call matches the oracle
-    w = workloads.scaled(workloads.get("gqa"), 333, cache_len=4096)
-    qknr.set_tuning(reset=True, kernel="ring")
-    try:
-        _check_workload(qknr, w)
-        assert qknr.qknr_selftest_watchdog(stream) == 0
-        cpu = workloads.make_inputs(w)
-        dev = workloads.to_device(cpu, w, "cuda")
-        with pytest.raises(qknr.QknrError) as ei:
-            qknr.apply_checked(dev["q"], dev["k"], dev["q_w"], dev["k_w"], dev["cos_sin_cache"],
-                               dev["positions"], is_neox=w.is_neox, eps=w.eps)
-        assert ei.value.code == 7
-    finally:
-        qknr.set_tuning(reset=True)
-    assert qknr.qknr_sync(stream) == 0
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a, b), name
 
 
 def _rope_dims(D, neox):
@@ -217,15 +190,17 @@ def _make(D, R, neox, pos, T, n_qo, n_kv, dtype="bf16", seed=0, cache_len=300, b
 
 
 @pytest.mark.parametrize("kernel,order", [("register", "interleaved"), ("register", "contiguous"),
-                                          ("ring", "interleaved"), ("ring", "contiguous")])
+                                          ("ring", "interleaved"), ("ring", "contiguous"),
+                                          ("ring2", "interleaved")])
 @pytest.mark.parametrize("D,R,neox,pos,T", GRID,
                          ids=[f"D{g[0]}-R{g[1]}-{'neox' if g[2] else 'inter'}-{g[3]}-T{g[4]}"
                               for g in GRID])
 def test_shape_grid(qknr, D, R, neox, pos, T, kernel, order):
     """The grid with both kernels forced, in both item orders (interleaved is
-    the automatic one)."""
+    the automatic one), and the ring kernel's second issue order ("ring2")."""
     w = _make(D, R, neox, pos, T, 4, 2, dtype="bf16" if (D + R + T) % 2 == 0 else "fp16")
-    qknr.set_tuning(reset=True, kernel=kernel, order=2 if order == "interleaved" else 1)
+    qknr.set_tuning(reset=True, kernel=kernel.rstrip("2"), ring_order=2 if kernel == "ring2" else 0,
+                    order=2 if order == "interleaved" else 1)
     try:
         _check_workload(qknr, w)
     finally:
@@ -267,6 +242,11 @@ TUNINGS = [
     dict(kernel=2, order=1, prefetch=-1),
     dict(kernel=2, pdl=0, prefetch=1),
     dict(kernel=2, threads=64, ctas_per_sm=2, prefetch=2),
+    dict(kernel=2, ring_order=1, passes=4, threads=512),
+    dict(kernel=2, ring_order=2),
+    dict(kernel=2, ring_order=2, passes=1, threads=64, ctas_per_sm=1),
+    dict(kernel=2, ring_order=2, passes=3, order=1, prefetch=-1),
+    dict(kernel=2, ring_order=2, pdl=0, threads=128),
 ]
 
 
@@ -300,26 +280,30 @@ def test_tunings_agree_bit_for_bit(qknr, tuning):
 
 def test_work_map_choice(qknr):
     """The automatic launch: 4-pass items interleaved over a persistent grid of
-    at most one wave of resident CTAs, with the ring kernel for NeoX pairing and
-    for interleaved calls of at most 256 MiB of q and k, the register kernel for
-    larger interleaved calls; 1-pass items on the register kernel for a call
-    too small to give every SM several warps."""
+    at most one wave of resident CTAs on the ring kernel, which issues each
+    item's successor once the item's bytes land (order 1), or, for interleaved
+    calls of more than 256 MiB of q and k, two items ahead (order 2); 1-pass
+    items on the register kernel for a call too small to give every SM
+    several warps."""
     bf, fp = qknr.QKNR_BF16, qknr.QKNR_FP16 | qknr.QKNR_POS_I64
     m = qknr.work_map(4608, 24, 24, 128, 128, False, bf)           # DiT: 113 MB of q and k
-    assert m["kernel"] == "ring" and m["order"] == "interleaved"
+    assert m["kernel"] == "ring" and m["ring_order"] == 1 and m["order"] == "interleaved"
     assert m["unroll"] == 4 and m["passes_per_token"] == 12 and m["items_per_token"] == 3
     assert m["items"] == 4608 * 3 and m["threads"] == 256 and m["pdl"] == 1
-    assert m["prefetch_items"] == 4 and m["rope_dim_compiled"] == 128
+    assert m["prefetch_items"] == 1 and m["rope_dim_compiled"] == 128
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert m["grid"] <= m["ctas_per_sm"] * sms and m["ctas_per_sm"] == 2
-    assert qknr.work_map(65536, 16, 4, 256, 128, False, bf)["kernel"] == "register"   # 1.3 GB
-    assert qknr.work_map(16384, 32, 8, 128, 64, True, fp)["kernel"] == "ring"
-    assert qknr.work_map(65536, 32, 8, 128, 64, True, fp)["kernel"] == "ring"         # NeoX: any size
+    big = qknr.work_map(65536, 16, 4, 256, 128, False, bf)                      # 1.3 GB
+    assert big["kernel"] == "ring" and big["ring_order"] == 2
+    for T in (16384, 65536):                                                   # NeoX: any size
+        g = qknr.work_map(T, 32, 8, 128, 64, True, fp)
+        assert g["kernel"] == "ring" and g["ring_order"] == 1
     limit = (256 << 20) // (4 * 48 * 128)                            # tokens of 48 heads in 256 MiB
-    assert qknr.work_map(limit, 24, 24, 128, 128, False, bf)["kernel"] == "ring"
-    assert qknr.work_map(limit + 1, 24, 24, 128, 128, False, bf)["kernel"] == "register"
+    assert qknr.work_map(limit, 24, 24, 128, 128, False, bf)["ring_order"] == 1
+    assert qknr.work_map(limit + 1, 24, 24, 128, 128, False, bf)["ring_order"] == 2
     small = qknr.work_map(4, 4, 2, 128, 6, False, bf)
     assert small["kernel"] == "register" and small["items_per_token"] == small["passes_per_token"]
+    assert small["ring_order"] == 0 and small["prefetch_items"] == 4
     assert qknr.work_map(4, 4, 2, 128, 64, True, fp)["kernel"] == "register"
 
 
@@ -412,7 +396,7 @@ def test_independent_head_strides_errors(qknr):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("kernel", ["register", "ring"])
+@pytest.mark.parametrize("kernel", ["register", "ring", "ring2"])
 @pytest.mark.parametrize("pdl", [-1, 0])
 def test_cuda_graph_capture_and_replay(qknr, pdl, kernel):
     """Calls captured into a CUDA graph (two calls on different buffers, with
@@ -421,7 +405,7 @@ def test_cuda_graph_capture_and_replay(qknr, pdl, kernel):
     buffers."""
     base = workloads.get("gqa")
     ws = [workloads.scaled(base, 70, cache_len=4096), workloads.scaled(workloads.get("dit"), 33)]
-    qknr.set_tuning(pdl=pdl, kernel=kernel)
+    qknr.set_tuning(pdl=pdl, kernel=kernel.rstrip("2"), ring_order=2 if kernel == "ring2" else 0)
     try:
         devs = [workloads.to_device(workloads.make_inputs(w), w, "cuda") for w in ws]
         s = torch.cuda.Stream()
