@@ -285,9 +285,10 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
 #define QKNR_TUNE_THREADS 3     /* threads per CTA, 64/128/256/512 (0 auto = 256) */
 #define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy) */
 #define QKNR_TUNE_PDL 5         /* programmatic dependent launch: -1 auto (on), 0 off, 1 on */
-#define QKNR_TUNE_RING_ORDER 6  /* ring kernel's issue order: 0 auto (2 for interleaved calls with more
-                                   than 256 MiB of q and k, else 1), 1 each item's successor issued as
-                                   soon as the item's bytes land, 2 two items ahead after the first */
+#define QKNR_TUNE_RING_ORDER 6  /* ring kernel's issue order: 0 auto (2 for interleaved bf16 calls
+                                   with head_dim 64, 128 or 256 whose warps run at least 6.5 rounds
+                                   of items, else 1), 1 each item's successor issued as soon as the
+                                   item's bytes land, 2 two items ahead after the first */
 #define QKNR_TUNE_ORDER 9       /* item order: 0 auto (= 2), 1 a contiguous range per warp,
                                    2 interleaved (warp w takes items w, w + W, ...) */
 #define QKNR_TUNE_PREFETCH 10   /* items per warp whose q/k rows (and the first positions) are
@@ -319,11 +320,13 @@ int qknr_get_tuning(int key, int *value);
  *
  * The candidates (the register kernel and both orders of the ring kernel;
  * passes per item 4, 3, 2 or 1 where they chunk a token differently; prefetch
- * of 4, 2, 1 or no items) run on scratch buffers with
- * the given layout, zero-filled, never on the caller's data, each timed with
- * CUDA events over about 2 ms of launches in three alternating rounds; the
- * one with the lowest median time per launch is kept. Input replicas rotate so
- * that no timed launch finds its inputs in L2.
+ * of 4, 2, 1 or no items) run on scratch buffers with the given layout, every
+ * byte set to a constant nonzero value, never on the caller's data, each
+ * timed with CUDA events over about 2 ms of launches in three alternating
+ * rounds, beside the fixed rule's own launch. The one with the lowest median
+ * time per launch is kept if it beats the rule's by more than 1% (the timing
+ * noise); otherwise the rule's launch is kept. Input replicas rotate so that
+ * no timed launch finds its inputs in L2.
  *
  * Arguments as for qknr_apply (num_tokens >= 1), without pointers. The call
  * allocates and frees its scratch (q and k at most 8 GiB, plus weights, a

@@ -173,9 +173,10 @@ struct ShapeHash {
 };
 // The knobs qknr_tune chooses: the kernel (and the ring kernel's issue order,
 // 1 or 2 as QKNR_TUNE_RING_ORDER), warp passes per item and items per warp
-// prefetched into L2 before the wait (0: none).
+// prefetched into L2 before the wait (-1: none). A 0 in any field leaves that
+// knob to the fixed rule, so an all-zero map is the rule's own launch.
 struct TunedMap {
-    int kernel = QKNR_KERNEL_REGISTER;
+    int kernel = QKNR_KERNEL_AUTO;
     int ring_order = 0;
     int passes = 0;
     int prefetch = 0;
@@ -347,19 +348,27 @@ bool tuned_for(DeviceState &st, const Call &c, TunedMap *out) {
 }
 
 // The measured rule (GB300, same-box sweeps of both kernels and both ring
-// orders over call sizes): the ring kernel for every call whose items have
-// three or four passes (+4% to +13% over the register kernel at the
-// benchmark's sizes), the register kernel for decode-sized calls; the ring's
-// order 1 (two items ahead) for interleaved calls of more than this many
-// bytes of q and k, order 0 (next item after the wait) below it and for NeoX
-// pairing.
-constexpr long long kRingAheadMinBytes = 256LL << 20;
-
+// orders over call shapes and sizes): the ring kernel for every call whose
+// items have three or four passes (+4% to +14% over the register kernel at
+// the benchmark's sizes), the register kernel for decode-sized calls.
+//
+// The ring's issue order: order 2 (two items ahead, Params::ring_ahead = 1)
+// starts slower than order 1 and then sustains more bandwidth, but only where
+// an item's arithmetic is light for its bytes: interleaved pairing, bf16, and
+// a head_dim whose lane groups have no idle lanes (64, 128, 256). There it
+// pays from about 6.5 rounds of items per warp up (a 4608-token DiT call runs
+// 5.7 and keeps order 1: +3.5%; fused_qkv runs 81: +5.7% with order 2).
+// Everywhere else order 1 measured ahead at every size tried: NeoX (gqa +7%
+// at 20 rounds), fp16 (head_dim 64, 3-pass items: +4.4%), head_dim 96 and 192
+// (+4.5% and +3.4%).
 bool ring_by_rule(const WorkMap &wm) { return wm.u_idx == 1; }
 
-int ring_ahead_by_rule(const Call &c) {
-    const long long qk_bytes = 4LL * (c.n_qo + c.n_kv) * c.head_dim * c.num_tokens;
-    return (!c.is_neox && qk_bytes > kRingAheadMinBytes) ? 1 : 0;
+int ring_ahead_by_rule(const Call &c, const WorkMap &wm) {
+    const bool light = !c.is_neox && (c.dtype & 0xff) == QKNR_BF16 &&
+                       (c.head_dim == 64 || c.head_dim == 128 || c.head_dim == 256);
+    if (!light) return 0;
+    const long long warps = static_cast<long long>(wm.grid) * (wm.threads / qknr::kWarp);
+    return 2 * wm.items >= 13 * warps ? 1 : 0;   // rounds = items / warps >= 6.5
 }
 
 // Items are (token, chunk of warp passes); the default is the largest unroll
@@ -407,7 +416,6 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *f
     wm->kind = kind;
     int order = force ? force->ring_order : tune(QKNR_TUNE_RING_ORDER);
     if (order == 0 && tuned) order = tm.ring_order;
-    wm->ring_ahead = kind != QKNR_KERNEL_RING ? 0 : (order == 0 ? ring_ahead_by_rule(c) : order - 1);
     int occ = 0;
     int rc = QKNR_OK;
     if (kind == QKNR_KERNEL_RING) {
@@ -436,10 +444,12 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *f
     if (cap > 0) occ = std::min(occ, cap);
     wm->ctas_per_sm = occ;
     wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
+    wm->ring_ahead = kind != QKNR_KERNEL_RING ? 0 : (order == 0 ? ring_ahead_by_rule(c, *wm) : order - 1);
     wm->interleave = tune(QKNR_TUNE_ORDER) == 1 ? 0 : 1;   // interleaved unless asked otherwise
-    const int pf = force ? (force->prefetch > 0 ? force->prefetch : -1) : tune(QKNR_TUNE_PREFETCH);
+    int pf = force ? force->prefetch : tune(QKNR_TUNE_PREFETCH);
+    if (pf == 0 && tuned) pf = tm.prefetch;
     const int auto_pf = kind == QKNR_KERNEL_RING ? kAutoPrefetchRing : kAutoPrefetchItems;
-    wm->prefetch_items = pf < 0 ? 0 : (pf > 0 ? pf : (tuned ? tm.prefetch : auto_pf));
+    wm->prefetch_items = pf < 0 ? 0 : (pf > 0 ? pf : auto_pf);
     return QKNR_OK;
 }
 
@@ -1018,6 +1028,7 @@ Call make_call(void *q, void *k, const void *q_w, const void *k_w, const float *
 constexpr long long kTuneMaxScratch = 8LL << 30;   // bytes of q and k replicas at most
 constexpr int kTuneMaxReplicas = 16;
 constexpr int kTuneRounds = 3;
+constexpr float kTuneMargin = 0.01f;   // a candidate must beat the rule by this fraction
 
 struct Scratch {
     std::vector<void *> ptrs;
@@ -1077,12 +1088,16 @@ int tune_impl(const Call &shape, void *stream, TunedMap *best_out, double *best_
     }
     if (e != cudaSuccess) return fail_cuda(e, "qknr_tune: scratch allocation");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // zeros are a valid input (every head normalises to zero); positions walk the table
-    e = cudaMemsetAsync(w, 0, 2 * 2 * static_cast<size_t>(shape.head_dim), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(cache, 0, static_cast<size_t>(cache_len) * shape.rope_dim * sizeof(float), s);
+    // every byte 0x3f: finite, nonzero values in every buffer (bf16 0.746, fp16
+    // 1.81, fp32 0.747), so the candidates move and compute what real data
+    // does; positions walk the table
+    constexpr int kFill = 0x3f;
+    e = cudaMemsetAsync(w, kFill, 2 * 2 * static_cast<size_t>(shape.head_dim), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(cache, kFill, static_cast<size_t>(cache_len) * shape.rope_dim * sizeof(float), s);
     for (auto &c : calls) {
-        if (e == cudaSuccess) e = cudaMemsetAsync(c.q, 0, static_cast<size_t>(q_bytes), s);
-        if (e == cudaSuccess) e = cudaMemsetAsync(c.k, 0, static_cast<size_t>(k_bytes), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c.q, kFill, static_cast<size_t>(q_bytes), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c.k, kFill, static_cast<size_t>(k_bytes), s);
     }
     if (e == cudaSuccess) {
         std::vector<long long> p64(pos64 ? static_cast<size_t>(T) : 0);
@@ -1103,17 +1118,18 @@ int tune_impl(const Call &shape, void *stream, TunedMap *best_out, double *best_
         c.cache_len = 0;
     }
 
-    // candidates: distinct (kernel, passes per item, prefetch depth) triples
+    // candidates: the rule's own launch first, then distinct (kernel, passes per
+    // item, prefetch depth) triples
     const int hpw = heads_per_pass(shape.head_dim);
     const int ppt = (shape.n_qo + shape.n_kv + hpw - 1) / hpw;
-    std::vector<TunedMap> cands;
+    std::vector<TunedMap> cands(1);
     std::set<int> seen_chunks;
     for (int passes : {4, 3, 2, 1}) {
         const int chunks = (ppt + passes - 1) / passes;
         if (!seen_chunks.insert(chunks).second) continue;
-        if (passes < 4 && cands.size() >= 24) break;
+        if (passes < 4 && cands.size() >= 25) break;
         for (int variant : {0, 1, 2})    // register; ring, next after the wait; ring, two ahead
-            for (int pf : {4, 2, 1, 0}) {
+            for (int pf : {4, 2, 1, -1}) {
                 TunedMap m;
                 m.kernel = variant == 0 ? QKNR_KERNEL_REGISTER : QKNR_KERNEL_RING;
                 m.ring_order = variant;
@@ -1172,17 +1188,23 @@ int tune_impl(const Call &shape, void *stream, TunedMap *best_out, double *best_
     cudaEventDestroy(ev[1]);
     if (rc) return rc;
     if (e != cudaSuccess) return fail_cuda(e, "qknr_tune: timing");
-    // the candidate with the lowest median time per launch
+    // the candidate with the lowest median time per launch; the rule's launch
+    // (candidate 0) stays unless another beats it by more than the timing noise
     size_t best = 0;
-    float best_t = 0.f;
+    float best_t = 0.f, rule_t = 0.f;
     for (size_t i = 0; i < cands.size(); ++i) {
         std::vector<float> v = times[i];
         std::sort(v.begin(), v.end());
         const float med = v[v.size() / 2];
+        if (i == 0) rule_t = med;
         if (i == 0 || med < best_t) {
             best = i;
             best_t = med;
         }
+    }
+    if (best != 0 && best_t > rule_t * (1.0f - kTuneMargin)) {
+        best = 0;
+        best_t = rule_t;
     }
     {
         std::lock_guard<std::mutex> lock(st->tuned_mu);

@@ -282,9 +282,9 @@ def test_work_map_choice(qknr):
     """The automatic launch: 4-pass items interleaved over a persistent grid of
     at most one wave of resident CTAs on the ring kernel, which issues each
     item's successor once the item's bytes land (order 1), or, for interleaved
-    calls of more than 256 MiB of q and k, two items ahead (order 2); 1-pass
-    items on the register kernel for a call too small to give every SM
-    several warps."""
+    bf16 calls with head_dim 64/128/256 whose warps run at least 6.5 rounds of
+    items, two items ahead (order 2); 1-pass items on the register kernel for a
+    call too small to give every SM several warps."""
     bf, fp = qknr.QKNR_BF16, qknr.QKNR_FP16 | qknr.QKNR_POS_I64
     m = qknr.work_map(4608, 24, 24, 128, 128, False, bf)           # DiT: 113 MB of q and k
     assert m["kernel"] == "ring" and m["ring_order"] == 1 and m["order"] == "interleaved"
@@ -298,9 +298,13 @@ def test_work_map_choice(qknr):
     for T in (16384, 65536):                                                   # NeoX: any size
         g = qknr.work_map(T, 32, 8, 128, 64, True, fp)
         assert g["kernel"] == "ring" and g["ring_order"] == 1
-    limit = (256 << 20) // (4 * 48 * 128)                            # tokens of 48 heads in 256 MiB
-    assert qknr.work_map(limit, 24, 24, 128, 128, False, bf)["ring_order"] == 1
-    assert qknr.work_map(limit + 1, 24, 24, 128, 128, False, bf)["ring_order"] == 2
+    warps = m["grid"] * m["threads"] // 32                           # one wave, 3 items per token
+    first = -(-13 * warps // 6)                                      # 3 T / warps >= 6.5
+    assert qknr.work_map(first - 1, 24, 24, 128, 128, False, bf)["ring_order"] == 1
+    assert qknr.work_map(first, 24, 24, 128, 128, False, bf)["ring_order"] == 2
+    assert qknr.work_map(4 * first, 24, 24, 128, 128, True, bf)["ring_order"] == 1   # NeoX
+    assert qknr.work_map(4 * first, 24, 24, 128, 128, False, qknr.QKNR_FP16)["ring_order"] == 1
+    assert qknr.work_map(4 * first, 24, 24, 96, 96, False, bf)["ring_order"] == 1     # idle lanes
     small = qknr.work_map(4, 4, 2, 128, 6, False, bf)
     assert small["kernel"] == "register" and small["items_per_token"] == small["passes_per_token"]
     assert small["ring_order"] == 0 and small["prefetch_items"] == 4
