@@ -311,8 +311,14 @@ def test_work_map_choice(qknr):
     assert qknr.work_map(4, 4, 2, 128, 64, True, fp)["kernel"] == "register"
 
 
-def test_separate_strides_and_padded_heads(qknr):
-    """q and k views with different token strides and a head stride > head_dim."""
+KERNELS = {"register": dict(kernel="register"), "ring": dict(kernel="ring", ring_order=1),
+           "ring2": dict(kernel="ring", ring_order=2)}
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_separate_strides_and_padded_heads(qknr, kernel):
+    """q and k views with different token strides and a head stride > head_dim,
+    on each kernel and ring order."""
     T, D, R = 77, 128, 64
     g = np.random.default_rng(5)
     qbuf = torch.from_numpy(g.standard_normal((T, 6, 160), dtype=np.float32)).to(torch.bfloat16)
@@ -329,8 +335,12 @@ def test_separate_strides_and_padded_heads(qknr):
     eq, ek = oracle.apply(q, k, qw, kw, cache, pos, is_neox=True, eps=1e-6)
     dq_buf, dk_big = qbuf.cuda(), kbig.cuda()
     dq, dk = dq_buf[:, 1:5, :D], dk_big[:, 0:3, :D]
-    qknr.apply(dq, dk, qw.cuda(), kw.cuda(), cache.cuda(), pos.cuda(), is_neox=True, eps=1e-6)
-    torch.cuda.synchronize()
+    qknr.set_tuning(reset=True, **KERNELS[kernel])
+    try:
+        qknr.apply(dq, dk, qw.cuda(), kw.cuda(), cache.cuda(), pos.cuda(), is_neox=True, eps=1e-6)
+        torch.cuda.synchronize()
+    finally:
+        qknr.set_tuning(reset=True)
     _assert_close(dq.double().cpu().numpy(), eq, torch.bfloat16, "q")
     _assert_close(dk.double().cpu().numpy(), ek, torch.bfloat16, "k")
     # everything outside the two views keeps its bits
@@ -346,12 +356,14 @@ STRIDED = [(6, 2, 0, 32, 128, True), (4, 4, 64, 0, 64, False), (1, 3, 0, 16, 256
            (3, 1, 8, 0, 96, True), (5, 3, 8, 24, 192, False), (24, 24, 0, 128, 128, False)]
 
 
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("n_qo,n_kv,q_pad,k_pad,D,neox", STRIDED,
                          ids=[f"q{c[0]}+{c[2]}-k{c[1]}+{c[3]}-D{c[4]}" for c in STRIDED])
-def test_independent_head_strides(qknr, n_qo, n_kv, q_pad, k_pad, D, neox):
+def test_independent_head_strides(qknr, n_qo, n_kv, q_pad, k_pad, D, neox, kernel):
     """q and k heads with their own strides (qknr_apply_strided, through the
-    raw entry point and through apply()): the same bits as qknr_apply on
-    contiguous copies, within the oracle's tolerance, padding untouched."""
+    raw entry point and through apply()), each kernel and ring order forced:
+    the same bits as qknr_apply on contiguous copies, within the oracle's
+    tolerance, padding untouched."""
     T, R = 131, D // 2 if neox else D
     g = np.random.default_rng(n_qo * 7 + n_kv + D)
     qbuf = torch.from_numpy(g.standard_normal((T, n_qo, D + q_pad), dtype=np.float32)).to(torch.bfloat16)
@@ -368,6 +380,7 @@ def test_independent_head_strides(qknr, n_qo, n_kv, q_pad, k_pad, D, neox):
     for route in ("raw", "apply"):
         dq_buf, dk_buf = qbuf.cuda(), kbuf.cuda()
         dq, dk = dq_buf[:, :, :D], dk_buf[:, :, :D]
+        qknr.set_tuning(reset=True, **KERNELS[kernel])
         if route == "raw":
             rc = qknr.qknr_apply_strided(dq.data_ptr(), dk.data_ptr(), dw[0].data_ptr(),
                                          dw[1].data_ptr(), dw[2].data_ptr(), dw[3].data_ptr(), T,
@@ -377,6 +390,7 @@ def test_independent_head_strides(qknr, n_qo, n_kv, q_pad, k_pad, D, neox):
         else:
             qknr.apply(dq, dk, *dw, is_neox=neox, eps=1e-6)
         torch.cuda.synchronize()
+        qknr.set_tuning(reset=True)
         assert torch.equal(dq.cpu().view(torch.int16), ref_q.cpu().view(torch.int16)), route
         assert torch.equal(dk.cpu().view(torch.int16), ref_k.cpu().view(torch.int16)), route
         _assert_close(dq.double().cpu().numpy(), eq, torch.bfloat16, "q")
@@ -451,7 +465,8 @@ def test_guard_bands_around_q_and_k(qknr):
     cpu = workloads.make_inputs(w)
     eq, ek = _expected(cpu, w)
     nq, nk, pad = cpu["q"].numel(), cpu["k"].numel(), 4096
-    for tune in ({}, {"order": 1}, {"passes": 1, "threads": 64}):
+    for tune in ({}, {"order": 1}, {"passes": 1, "threads": 64}, {"kernel": "ring", "ring_order": 1},
+                 {"kernel": "ring", "ring_order": 2, "passes": 3}, {"kernel": "ring", "order": 1, "threads": 64}):
         buf = torch.full((pad + nq + pad + nk + pad,), -31.0, dtype=torch.float16, device="cuda")
         dq = buf[pad:pad + nq].view(cpu["q"].shape)
         dk = buf[2 * pad + nq:2 * pad + nq + nk].view(cpu["k"].shape)
