@@ -314,10 +314,7 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
     const uint4 wqa = active ? __ldg(p.q_w + va) : zero4, wqb = active ? __ldg(p.q_w + vb) : zero4;
     const uint4 wka = active ? __ldg(p.k_w + va) : zero4, wkb = active ? __ldg(p.k_w + vb) : zero4;
 
-    // cos and (sign-free) sin per owned element. Interleaved: c[m]/s[m] serve
-    // pair m of vector a (m < 4) and pair m-4 of vector b (m >= 4). NeoX split:
-    // c[e]/s[e] serve element e of both vectors. NeoX small: element e < R/2 of
-    // vector 0. Identity (1, 0) wherever nothing rotates.
+    // the current token's cos and sin per owned element (token_cos_sin)
     float c[8], s[8];
     long long cur_t = -1;
     bool tok_ok = true;
@@ -390,60 +387,7 @@ __global__ void __launch_bounds__(512) qknr_fused_kernel(const __grid_constant__
             cur_t = t;
             const long long pos = __shfl_sync(0xffffffffu, my_pos, jb);
             check_position(p, pos, t, ch, lane, tok_ok);
-            // token_cos_sin, written out: as a call it changed this kernel's
-            // register allocation and spills (ptxas), and this close to the
-            // bandwidth limit such changes move its time
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { c[e] = 1.f; s[e] = 0.f; }
-            if (tok_ok && rot_lane) {
-                const float *row = p.cache + pos * R;
-                if (MODE == kInterleaved) {
-                    if (p.cache_vec && 8 * va + 8 <= R) {
-                        const float4 ca = __ldg(reinterpret_cast<const float4 *>(row + 4 * va));
-                        const float4 sa = __ldg(reinterpret_cast<const float4 *>(row + half + 4 * va));
-                        c[0] = ca.x; c[1] = ca.y; c[2] = ca.z; c[3] = ca.w;
-                        s[0] = sa.x; s[1] = sa.y; s[2] = sa.z; s[3] = sa.w;
-                    } else {
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const int j = 4 * va + m;
-                            if (2 * j < R) { c[m] = __ldg(row + j); s[m] = __ldg(row + half + j); }
-                        }
-                    }
-                    if (p.cache_vec && 8 * vb + 8 <= R) {
-                        const float4 cb = __ldg(reinterpret_cast<const float4 *>(row + 4 * vb));
-                        const float4 sb = __ldg(reinterpret_cast<const float4 *>(row + half + 4 * vb));
-                        c[4] = cb.x; c[5] = cb.y; c[6] = cb.z; c[7] = cb.w;
-                        s[4] = sb.x; s[5] = sb.y; s[6] = sb.z; s[7] = sb.w;
-                    } else {
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const int j = 4 * vb + m;
-                            if (2 * j < R) { c[4 + m] = __ldg(row + j); s[4 + m] = __ldg(row + half + j); }
-                        }
-                    }
-                } else if (split) {
-                    const int j0 = 8 * va;      // dims [j0, j0+8) of the first half
-                    if (p.cache_vec) {
-                        const float4 c0 = __ldg(reinterpret_cast<const float4 *>(row + j0));
-                        const float4 c1 = __ldg(reinterpret_cast<const float4 *>(row + j0 + 4));
-                        const float4 s0 = __ldg(reinterpret_cast<const float4 *>(row + half + j0));
-                        const float4 s1 = __ldg(reinterpret_cast<const float4 *>(row + half + j0 + 4));
-                        c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
-                        c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-                        s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
-                        s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) { c[e] = __ldg(row + j0 + e); s[e] = __ldg(row + half + j0 + e); }
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (e < half) { c[e] = __ldg(row + e); s[e] = __ldg(row + half + e); }
-                    }
-                }
-            }
+            token_cos_sin<MODE>(p, pos, tok_ok && rot_lane, va, vb, split, R, half, c, s);
         }
         if (!tok_ok) continue;          // warp-uniform: t is the same for the whole warp
 
