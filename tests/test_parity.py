@@ -289,16 +289,17 @@ def test_work_map_choice(qknr):
     m = qknr.work_map(4608, 24, 24, 128, 128, False, bf)           # DiT: 113 MB of q and k
     assert m["kernel"] == "ring" and m["ring_order"] == 1 and m["order"] == "interleaved"
     assert m["unroll"] == 4 and m["passes_per_token"] == 12 and m["items_per_token"] == 3
-    assert m["items"] == 4608 * 3 and m["threads"] == 256 and m["pdl"] == 1
+    assert m["items"] == 4608 * 3 and m["threads"] == 64 and m["pdl"] == 1     # CTAs of two warps
     assert m["prefetch_items"] == 1 and m["rope_dim_compiled"] == 128
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert m["grid"] <= m["ctas_per_sm"] * sms and m["ctas_per_sm"] == 2
+    assert m["grid"] <= m["ctas_per_sm"] * sms and m["ctas_per_sm"] == 8
     big = qknr.work_map(65536, 16, 4, 256, 128, False, bf)                      # 1.3 GB
-    assert big["kernel"] == "ring" and big["ring_order"] == 2
+    assert big["kernel"] == "ring" and big["ring_order"] == 2 and big["threads"] == 256
     for T in (16384, 65536):                                                   # NeoX: any size
         g = qknr.work_map(T, 32, 8, 128, 64, True, fp)
-        assert g["kernel"] == "ring" and g["ring_order"] == 1
+        assert g["kernel"] == "ring" and g["ring_order"] == 1 and g["threads"] == 256
     warps = m["grid"] * m["threads"] // 32                           # one wave, 3 items per token
+    assert warps == 16 * sms
     first = -(-13 * warps // 6)                                      # 3 T / warps >= 6.5
     assert qknr.work_map(first - 1, 24, 24, 128, 128, False, bf)["ring_order"] == 1
     assert qknr.work_map(first, 24, 24, 128, 128, False, bf)["ring_order"] == 2
