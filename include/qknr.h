@@ -282,8 +282,9 @@ int qknr_apply_host(void *h_q, void *h_k, const void *q_w, const void *k_w,
                                    register kernel for decode-sized calls), 1 register, 2 ring */
 #define QKNR_TUNE_PASSES 2      /* warp passes per item, 1..4 (0 auto: 4, or 1 when the whole call has
                                    at most 16 warp passes per SM) */
-#define QKNR_TUNE_THREADS 3     /* threads per CTA, 64/128/256/512 (0 auto: 256; 64 for the ring kernel's
-                                   order 1 on interleaved calls, when no CTA cap is set) */
+#define QKNR_TUNE_THREADS 3     /* threads per CTA, 64/128/256/512 (0 auto: 256; when no CTA cap is set,
+                                   64 for the ring kernel's order 1 on interleaved calls and 512 for
+                                   its order 2 when warps run at least 32 rounds of items) */
 #define QKNR_TUNE_CTAS_PER_SM 4 /* cap on resident CTAs per SM (0 auto: occupancy) */
 #define QKNR_TUNE_PDL 5         /* programmatic dependent launch: -1 auto (on), 0 off, 1 on */
 #define QKNR_TUNE_RING_ORDER 6  /* ring kernel's issue order: 0 auto (2 for interleaved bf16 calls

@@ -362,7 +362,9 @@ bool tuned_for(DeviceState &st, const Call &c, TunedMap *out) {
 // at 20 rounds), fp16 (head_dim 64, 3-pass items: +4.4%), head_dim 96 and 192
 // (+4.5% and +3.4%).
 bool ring_by_rule(const WorkMap &wm) { return wm.u_idx == 1; }
-constexpr int kRingSmallCta = 64;   // threads per CTA of the ring kernel's order 1 on interleaved calls
+constexpr int kRingSmallCta = 64;         // threads per CTA: ring order 1 on interleaved calls
+constexpr int kRingLargeCta = 512;        // threads per CTA: ring order 2 on long calls
+constexpr long long kRingLargeCtaRounds = 32;   // rounds of items per warp from which order 2 takes 512
 
 int ring_ahead_by_rule(const Call &c, const WorkMap &wm) {
     const bool light = !c.is_neox && (c.dtype & 0xff) == QKNR_BF16 &&
@@ -446,20 +448,29 @@ int plan_register(DeviceState &st, const Call &c, WorkMap *wm, const TunedMap *f
     wm->ctas_per_sm = occ;
     wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
     wm->ring_ahead = kind != QKNR_KERNEL_RING ? 0 : (order == 0 ? ring_ahead_by_rule(c, *wm) : order - 1);
-    if (auto_threads && cap <= 0 && kind == QKNR_KERNEL_RING && wm->ring_ahead == 0 && !c.is_neox) {
+    if (auto_threads && cap <= 0 && kind == QKNR_KERNEL_RING) {
+        // The ring kernel's CTA size, at the same 16 resident warps per SM:
         // interleaved calls on issue order 1 measured faster in CTAs of two
-        // warps (dit +1.6%, 2304 tokens +2.6%, head_dim 192 +3%), at the same
-        // 16 resident warps per SM: the CTAs of the next launch in the stream
-        // take the SM's slots as soon as two warps of this one are done
-        threads = kRingSmallCta;
-        wm->threads = threads;
-        wm->smem = qknr::ring_smem_bytes(threads);
-        rc = cached_occupancy(st.ring_occ[early][dt][pos64][d_idx][mode][wm->r_idx][threads_index(threads)],
-                              wm->kernel, threads, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ring)", &occ,
-                              wm->smem);
-        if (rc) return rc;
-        wm->ctas_per_sm = occ;
-        wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
+        // warps (dit +1.6%, 2304 tokens +2.2%, head_dim 192 +3%; the next
+        // launch's CTAs take an SM's slots as soon as two warps of this one
+        // are done), calls on order 2 whose warps run at least 32 rounds of
+        // items in one CTA per SM (+0.35% to +1%: each SM's warps take
+        // consecutive items, a contiguous stretch of q and k per round).
+        const long long warps = static_cast<long long>(wm->grid) * (threads / qknr::kWarp);
+        int want = threads;
+        if (wm->ring_ahead == 0 && !c.is_neox) want = kRingSmallCta;
+        if (wm->ring_ahead == 1 && wm->items >= kRingLargeCtaRounds * warps) want = kRingLargeCta;
+        if (want != threads) {
+            threads = want;
+            wm->threads = threads;
+            wm->smem = qknr::ring_smem_bytes(threads);
+            rc = cached_occupancy(st.ring_occ[early][dt][pos64][d_idx][mode][wm->r_idx][threads_index(threads)],
+                                  wm->kernel, threads, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ring)", &occ,
+                                  wm->smem);
+            if (rc) return rc;
+            wm->ctas_per_sm = occ;
+            wm->grid = persistent_grid(wm->items, threads, occ, st.sm_count);
+        }
     }
     wm->interleave = tune(QKNR_TUNE_ORDER) == 1 ? 0 : 1;   // interleaved unless asked otherwise
     int pf = force ? force->prefetch : tune(QKNR_TUNE_PREFETCH);

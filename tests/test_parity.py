@@ -294,7 +294,8 @@ def test_work_map_choice(qknr):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert m["grid"] <= m["ctas_per_sm"] * sms and m["ctas_per_sm"] == 8
     big = qknr.work_map(65536, 16, 4, 256, 128, False, bf)                      # 1.3 GB
-    assert big["kernel"] == "ring" and big["ring_order"] == 2 and big["threads"] == 256
+    assert big["kernel"] == "ring" and big["ring_order"] == 2 and big["threads"] == 512   # 81 rounds
+    assert big["ctas_per_sm"] == 1 and big["grid"] == sms
     for T in (16384, 65536):                                                   # NeoX: any size
         g = qknr.work_map(T, 32, 8, 128, 64, True, fp)
         assert g["kernel"] == "ring" and g["ring_order"] == 1 and g["threads"] == 256
@@ -302,7 +303,10 @@ def test_work_map_choice(qknr):
     assert warps == 16 * sms
     first = -(-13 * warps // 6)                                      # 3 T / warps >= 6.5
     assert qknr.work_map(first - 1, 24, 24, 128, 128, False, bf)["ring_order"] == 1
-    assert qknr.work_map(first, 24, 24, 128, 128, False, bf)["ring_order"] == 2
+    mid = qknr.work_map(first, 24, 24, 128, 128, False, bf)
+    assert mid["ring_order"] == 2 and mid["threads"] == 256                       # 6.5 rounds
+    long_ = qknr.work_map(-(-32 * warps // 3), 24, 24, 128, 128, False, bf)
+    assert long_["ring_order"] == 2 and long_["threads"] == 512
     assert qknr.work_map(4 * first, 24, 24, 128, 128, True, bf)["ring_order"] == 1   # NeoX
     assert qknr.work_map(4 * first, 24, 24, 128, 128, False, qknr.QKNR_FP16)["ring_order"] == 1
     assert qknr.work_map(4 * first, 24, 24, 96, 96, False, bf)["ring_order"] == 1     # idle lanes
