@@ -207,6 +207,40 @@ def test_shape_grid(qknr, D, R, neox, pos, T, kernel, order):
         qknr.set_tuning(reset=True)
 
 
+RING_MULTIPASS = [(D, neox, order) for D in (64, 80, 96, 128, 192, 256) for neox in (False, True)
+                  for order in (1, 2)]
+
+
+@pytest.mark.parametrize("D,neox,order", RING_MULTIPASS,
+                         ids=[f"D{c[0]}-{'neox' if c[1] else 'inter'}-order{c[2]}" for c in RING_MULTIPASS])
+def test_ring_multi_pass_items(D, neox, order, qknr):
+    """The ring kernel on calls large enough for items of three or four warp
+    passes (the rule's launch for such calls), at every head_dim, including
+    80, 96 and 192 whose lane groups have idle lanes, in both issue orders:
+    against the oracle, and bit for bit against the register kernel."""
+    R = _neox_half(D) if neox else (D if D % 32 == 0 else D // 2)
+    w = _make(D, R, neox, "i64" if neox else "i32", 1200, 24, 8, dtype="fp16" if D % 64 else "bf16",
+              seed=D + 7 * order + int(neox), cache_len=2048)
+    m = qknr.work_map(w.num_tokens, w.n_qo, w.n_kv, D, R, neox,
+                      qknr.dtype_code(w.torch_dtype, w.pos_torch_dtype))
+    assert m["unroll"] == 4 and m["kernel"] == "ring", m
+    cpu = workloads.make_inputs(w)
+    ref = workloads.to_device(cpu, w, "cuda")
+    qknr.set_tuning(reset=True, kernel="register")
+    try:
+        _run_gpu(qknr, ref, w)
+        qknr.set_tuning(reset=True, kernel="ring", ring_order=order)
+        dev = workloads.to_device(cpu, w, "cuda")
+        _run_gpu(qknr, dev, w)
+    finally:
+        qknr.set_tuning(reset=True)
+    assert torch.equal(dev["q"].view(torch.int16), ref["q"].view(torch.int16))
+    assert torch.equal(dev["k"].view(torch.int16), ref["k"].view(torch.int16))
+    eq, ek = _expected(cpu, w)
+    _assert_close(dev["q"].double().cpu().numpy(), eq, w.torch_dtype, "q")
+    _assert_close(dev["k"].double().cpu().numpy(), ek, w.torch_dtype, "k")
+
+
 def _neox_half(D):
     """A NeoX rope_dim near half of head_dim that the op takes (a multiple of 16)."""
     return D // 2 if (D // 2) % 16 == 0 else (D // 2) // 16 * 16
