@@ -188,8 +188,9 @@ int qknr_apply_unfused(void *q, void *k, const void *q_w, const void *k_w,
  * of the library, which every GPU that loads the library holds until the
  * process exits. A call needs those 16 bytes whatever its num_tokens, so no
  * problem size exceeds the array. The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture. That set-up is kept for
+ * array's device address (cudaGetSymbolAddress) with that device current.
+ * No call of this entry point can be captured into a CUDA graph: each one
+ * reads its status back to the host and synchronises. That set-up is kept for
  * the life of the process: a device reset (cudaDeviceReset) after the first
  * call on a device is not supported by this entry point. Each call resets
  * the status it reads, and waits for `stream` before returning (it is
