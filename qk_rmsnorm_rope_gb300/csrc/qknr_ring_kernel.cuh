@@ -18,8 +18,8 @@
 //     few hundred MB and on NeoX pairing.
 //  1  after the first item, the item two ahead is issued once this item's
 //     stores are out, so two items can be in flight. More bytes in flight
-//     sustain more bandwidth on large interleaved calls (fused_qkv: 99.8% of
-//     the measured copy peak); the start is slower.
+//     sustain more bandwidth on large interleaved calls (fused_qkv: 99-99.7%
+//     of the measured copy peak); the start is slower.
 #pragma once
 
 #include <cstdint>
